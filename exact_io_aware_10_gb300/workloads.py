@@ -1,0 +1,149 @@
+"""Seeded synthetic inputs shared by the CUDA path's tests/bench and the oracle.
+
+This module draws random numbers and lays them out; it holds none of the
+attention arithmetic.  Every tensor is produced on the CPU with a seeded
+``torch.Generator`` (values drawn in fp32, rounded to bf16 round-to-nearest-even),
+so both sides read bit-identical inputs.
+
+Workload recipes (shapes follow the attention configurations this library is
+measured on; the pages' benchmark suites -- MLPerf BERT-large, OpenWebText GPT-2,
+Long Range Arena -- are stood in for by these synthetic tensors):
+
+* ``dense``      Q, K, V, dO ~ N(0, std^2), layout [B, H, N, d].
+* ``padded``     ``dense`` plus per-sequence key lengths L_b ~ U{lo..hi}.
+* ``boosted``    ``dense`` with std 0.5 plus a max-shift stressor: per (b, h) a
+                 random unit direction u; each Q row and each K row is picked
+                 with probability 0.1 and gets c*u added, c = sqrt(8*sqrt(d)),
+                 so about 1% of (query, key) pairs gain ~+8 in scaled logit.
+* ``paged``      decode queries [B, Hq, d], a paged KV cache
+                 [num_blocks, block_size, Hkv, d], context lengths
+                 L_b ~ U{lo..hi}, and a block table whose physical ids are a
+                 seeded random permutation (entries past a row's blocks are -1).
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+
+import torch
+
+__all__ = [
+    "AttentionInputs",
+    "PagedInputs",
+    "dense_inputs",
+    "padded_lengths",
+    "boosted_inputs",
+    "paged_inputs",
+    "config_seed",
+]
+
+
+def config_seed(seed: int, config_id: int) -> int:
+    """Per-configuration RNG stream id derived from (seed, config id)."""
+    return int(seed) * 1_000_003 + int(config_id) * 7919 + 17
+
+
+def _gen(seed: int) -> torch.Generator:
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    return g
+
+
+def _normal_bf16(shape, g, std=1.0):
+    x = torch.randn(*shape, generator=g, dtype=torch.float32)
+    if std != 1.0:
+        x = x * std
+    return x.to(torch.bfloat16)
+
+
+@dataclass
+class AttentionInputs:
+    Q: torch.Tensor  # [B, H, N, d] bf16 (CPU)
+    K: torch.Tensor
+    V: torch.Tensor
+    dO: torch.Tensor
+    kv_lens: torch.Tensor | None  # int32 [B] or None
+
+    @property
+    def shape(self):
+        return tuple(self.Q.shape)
+
+
+def dense_inputs(B, H, N, d, seed=0, std=1.0, kv_lens=None) -> AttentionInputs:
+    """Q, K, V, dO i.i.d. N(0, std^2) rounded to bf16, layout [B, H, N, d]."""
+    g = _gen(seed)
+    Q = _normal_bf16((B, H, N, d), g, std)
+    K = _normal_bf16((B, H, N, d), g, std)
+    V = _normal_bf16((B, H, N, d), g, std)
+    dO = _normal_bf16((B, H, N, d), g, 1.0)
+    return AttentionInputs(Q, K, V, dO, kv_lens)
+
+
+def padded_lengths(B, lo, hi, seed=0) -> torch.Tensor:
+    """Per-sequence valid key lengths, uniform integers in [lo, hi], int32 [B]."""
+    g = _gen(seed + 101)
+    return torch.randint(lo, hi + 1, (B,), generator=g, dtype=torch.int64).to(torch.int32)
+
+
+def boosted_inputs(B, H, N, d, seed=0, std=0.5, pick_prob=0.1, boost=8.0) -> AttentionInputs:
+    """``dense`` inputs (std 0.5) with ~1% of (q, k) pairs boosted by ~``boost``
+    in scaled logit, to exercise max-shift rescaling in a streaming softmax."""
+    g = _gen(seed)
+    Qf = torch.randn(B, H, N, d, generator=g, dtype=torch.float32) * std
+    Kf = torch.randn(B, H, N, d, generator=g, dtype=torch.float32) * std
+    V = _normal_bf16((B, H, N, d), g, std)
+    dO = _normal_bf16((B, H, N, d), g, 1.0)
+    u = torch.randn(B, H, 1, d, generator=g, dtype=torch.float32)
+    u = u / u.norm(dim=-1, keepdim=True)
+    c = math.sqrt(boost * math.sqrt(d))
+    qpick = (torch.rand(B, H, N, 1, generator=g) < pick_prob).to(torch.float32)
+    kpick = (torch.rand(B, H, N, 1, generator=g) < pick_prob).to(torch.float32)
+    Q = (Qf + qpick * c * u).to(torch.bfloat16)
+    K = (Kf + kpick * c * u).to(torch.bfloat16)
+    return AttentionInputs(Q, K, V, dO, None)
+
+
+@dataclass
+class PagedInputs:
+    q: torch.Tensor            # [B, Hq, d] bf16
+    k_cache: torch.Tensor      # [num_blocks, block_size, Hkv, d] bf16
+    v_cache: torch.Tensor      # [num_blocks, block_size, Hkv, d] bf16
+    block_table: torch.Tensor  # [B, max_blocks] int32, -1 past each row's blocks
+    seq_lens: torch.Tensor     # [B] int32
+    block_size: int
+
+    @property
+    def num_blocks(self):
+        return int(self.k_cache.shape[0])
+
+    @property
+    def max_blocks(self):
+        return int(self.block_table.shape[1])
+
+
+def paged_inputs(B, Hq, Hkv, d, L_lo, L_hi, block_size=16, seed=0, max_blocks=None,
+                 seq_lens=None, std=1.0, spare_blocks=0) -> PagedInputs:
+    """Paged decode inputs.
+
+    Physical block ids are a seeded random permutation of [0, NB) where
+    NB = sum_b ceil(L_b / block_size) (+ ``spare_blocks`` never referenced).
+    """
+    g = _gen(seed)
+    if seq_lens is None:
+        seq_lens = torch.randint(L_lo, L_hi + 1, (B,), generator=g, dtype=torch.int64)
+    seq_lens = torch.as_tensor(seq_lens, dtype=torch.int64).reshape(-1)
+    B = int(seq_lens.numel())
+    nblk = [(int(L) + block_size - 1) // block_size for L in seq_lens.tolist()]
+    NB = sum(nblk) + int(spare_blocks)
+    if max_blocks is None:
+        max_blocks = max(1, max(nblk) if nblk else 1)
+    perm = torch.randperm(NB, generator=g).to(torch.int32)
+    table = torch.full((B, max_blocks), -1, dtype=torch.int32)
+    pos = 0
+    for b, n in enumerate(nblk):
+        table[b, :n] = perm[pos:pos + n]
+        pos += n
+    q = _normal_bf16((B, Hq, d), g, std)
+    k_cache = _normal_bf16((max(NB, 1), block_size, Hkv, d), g, std)
+    v_cache = _normal_bf16((max(NB, 1), block_size, Hkv, d), g, std)
+    return PagedInputs(q, k_cache, v_cache, table, seq_lens.to(torch.int32), block_size)
