@@ -1,0 +1,184 @@
+// Public C entry points (include/fa.h): argument validation, the device
+// status word and tensor-map encoding.  The kernels live in fa_fwd.cu,
+// fa_bwd.cu and fa_decode.cu.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "fa_internal.h"
+
+namespace fa {
+
+// One status word per device (each device that loads the library holds its
+// own copy of this variable).
+__device__ unsigned g_fa_status;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+unsigned* g_status_ptr[kMaxDevices] = {};
+std::mutex g_mu;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+unsigned* device_status_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_status_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_fa_status) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<unsigned*>(p);
+  }
+  return g_status_ptr[dev];
+}
+
+bool encode_bf16_tmap(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                      const uint64_t* strides_bytes, const uint32_t* box) {
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_encode == nullptr) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+              cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return false;
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+  }
+  cuuint64_t gdim[5];
+  cuuint64_t gstr[4];
+  cuuint32_t bdim[5];
+  cuuint32_t estr[5];
+  for (int i = 0; i < rank; ++i) {
+    gdim[i] = dims[i];
+    bdim[i] = box[i];
+    estr[i] = 1;
+    if (i + 1 < rank) gstr[i] = strides_bytes[i];
+  }
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank), const_cast<void*>(base),
+                        gdim, gstr, bdim, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace fa
+
+using fa::aligned16;
+
+namespace {
+
+bool bad_scale(float s) { return !(s > 0.f) || !isfinite(s); }
+
+int check_attn(const void* Q, const void* K, const void* V, const void* O, const void* LSE, int B, int H, int N, int d,
+               float scale) {
+  if (B < 1 || H < 1 || N < 0) return FA_ERR_INVALID_ARG;
+  if (bad_scale(scale)) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (N == 0) return FA_OK;
+  if (!Q || !K || !V || !O || !LSE) return FA_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(LSE)) return FA_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * H > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  if ((static_cast<long long>(N) + 255) / 256 > 65535) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+}  // namespace
+
+extern "C" {
+
+const char* fa_status_string(int status) {
+  switch (status) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+    case FA_ERR_BAD_BLOCK_TABLE: return "FA_ERR_BAD_BLOCK_TABLE";
+    default: return "FA_ERR_UNKNOWN";
+  }
+}
+
+int fa_version(void) { return 100; }
+
+int fa_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d, int causal,
+              float scale, const int32_t* kv_lens, void* stream) {
+  int st = check_attn(Q, K, V, O, LSE, B, H, N, d, scale);
+  if (st != FA_OK || N == 0) return st;
+  return fa::fwd_launch(Q, K, V, O, LSE, B, H, N, d, causal, scale, kv_lens, static_cast<cudaStream_t>(stream));
+}
+
+int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d, int causal,
+           float scale, void* stream) {
+  return fa_fwd_ex(Q, K, V, O, LSE, B, H, N, d, causal, scale, nullptr, stream);
+}
+
+size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 0 || d < 1) return 0;
+  const size_t rows = static_cast<size_t>(B) * H * N;
+  return round256(rows * sizeof(float)) + round256(rows * d * sizeof(float));
+}
+
+int fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE, void* dQ,
+           void* dK, void* dV, int B, int H, int N, int d, int causal, float scale, const int32_t* kv_lens,
+           void* workspace, size_t ws_bytes, void* stream) {
+  int st = check_attn(Q, K, V, O, LSE, B, H, N, d, scale);
+  if (st != FA_OK || N == 0) return st;
+  if (!dO || !dQ || !dK || !dV || !workspace) return FA_ERR_INVALID_ARG;
+  if (!aligned16(dO) || !aligned16(dQ) || !aligned16(dK) || !aligned16(dV)) return FA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_INVALID_ARG;
+  if (ws_bytes < fa_bwd_workspace_size(B, H, N, d)) return FA_ERR_INVALID_ARG;
+  return fa::bwd_launch(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, causal, scale, kv_lens, workspace,
+                        static_cast<cudaStream_t>(stream));
+}
+
+size_t fa_paged_decode_workspace_size(int B, int Hq, int d, int num_splits) {
+  if (B < 1 || Hq < 1 || d < 1 || num_splits < 0 || num_splits > 16) return 0;
+  const int S = num_splits == 0 ? 16 : num_splits;
+  return round256(static_cast<size_t>(B) * Hq * S * (d + 2) * sizeof(float));
+}
+
+int fa_paged_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                    const int32_t* seq_lens, void* o, float* lse, int B, int Hq, int Hkv, int d, int block_size,
+                    int max_blocks, int num_blocks, int num_splits, float scale, void* workspace, size_t ws_bytes,
+                    void* stream) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || max_blocks < 1 || num_blocks < 1 || num_splits < 0) return FA_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
+  if (bad_scale(scale)) return FA_ERR_INVALID_ARG;
+  if (d != 128 || block_size != 16) return FA_ERR_UNSUPPORTED;
+  if (Hq / Hkv > 16 || num_splits > 16) return FA_ERR_UNSUPPORTED;
+  if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !o || !workspace) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o)) return FA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_INVALID_ARG;
+  if (static_cast<long long>(num_blocks) * block_size > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  const int S = num_splits == 0 ? 16 : num_splits;
+  if (ws_bytes < fa_paged_decode_workspace_size(B, Hq, d, S)) return FA_ERR_INVALID_ARG;
+  return fa::decode_launch(q, k_cache, v_cache, block_table, seq_lens, o, lse, B, Hq, Hkv, d, block_size, max_blocks,
+                           num_blocks, S, scale, workspace, static_cast<cudaStream_t>(stream));
+}
+
+int fa_get_device_status(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+  unsigned v = 0;
+  if (cudaMemcpyFromSymbol(&v, fa::g_fa_status, sizeof(v)) != cudaSuccess) return FA_ERR_CUDA;
+  if (v != 0) {
+    const unsigned zero = 0;
+    if (cudaMemcpyToSymbol(fa::g_fa_status, &zero, sizeof(zero)) != cudaSuccess) return FA_ERR_CUDA;
+  }
+  if (v & fa::kStatusTimeoutBit) return FA_ERR_TIMEOUT;
+  if (v & fa::kStatusBadTableBit) return FA_ERR_BAD_BLOCK_TABLE;
+  return FA_OK;
+}
+
+}  // extern "C"

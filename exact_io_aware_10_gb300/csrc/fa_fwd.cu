@@ -1,0 +1,435 @@
+// Forward attention on sm_103a: one CTA owns two 128-row query tiles of one
+// (batch, head) and streams all visible 128-key K/V tiles through shared
+// memory, computing
+//     S = Q K^T      (tcgen05 MMA, fp32 accumulator in TMEM)
+//     online softmax (one thread per query row, registers only)
+//     O += P V       (tcgen05 MMA, fp32 accumulator in TMEM)
+// so no score tile ever reaches device memory ("精读笔记 08：FlashAttention",
+// §3.2 tiling and §3.4 fusion; the recurrence is §3.1 / S12 "核心思路").
+//
+// Roles (10 warps):
+//   warps 0-3  softmax + epilogue for query tile 0 (TMEM lanes 0..127)
+//   warps 4-7  softmax + epilogue for query tile 1
+//   warp 8     TMA producer: Q tiles once, then K_j, V_j into a slot ring
+//   warp 9     MMA issuer (one thread)
+// MMA order per key tile j:  PV(0, j), S(0, j+1), PV(1, j), S(1, j+1), so the
+// tensor core works on one query tile while the other one's softmax runs.
+//
+// Online softmax with a stale reference max: a row keeps the reference m_ref
+// (log2 units) it last rescaled to; a tile whose max exceeds m_ref by more
+// than kRescaleLog2 moves the reference and rescales O (in TMEM) and l by
+// alpha = 2^(m_ref_old - m_ref_new).  Otherwise p = 2^(x - m_ref) <= 2^8 and
+// nothing is rescaled.  O and l share the reference, so O / l is exact
+// (S12: "one multiplication fixes everything accumulated so far").
+// A row whose running max is still -inf subtracts 0 instead of -inf, which
+// avoids exp(-inf - -inf) = NaN on fully masked tiles (S12 warning).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include "fa_internal.h"
+#include "sm103.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kThreads = 320;
+constexpr int kRows = 128;   // query rows per tile = TMEM lanes
+constexpr int kKeys = 128;   // keys per K/V tile
+constexpr float kRescaleLog2 = 8.0f;
+
+template <int D>
+struct FwdCfg {
+  static constexpr int kSub = D / 64;                // 128-byte swizzle sub-tiles per row
+  static constexpr int kSubBytes = kRows * 128;      // one sub-tile: 128 rows x 128 B
+  static constexpr int kTileBytes = kRows * D * 2;   // Q/K/V tile
+  static constexpr int kPBytes = kRows * kKeys * 2;  // P tile (bf16)
+  static constexpr int kSlots = (D == 128) ? 3 : 6;  // K/V ring slots
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffP = kOffQ + 2 * kTileBytes;
+  static constexpr int kOffKV = kOffP + 2 * kPBytes;
+  static constexpr int kOffBar = kOffKV + kSlots * kTileBytes;
+  static constexpr int kSmemBytes = kOffBar + 256 + 1024;  // barriers + alignment slack
+  static constexpr uint32_t kTmemCols = 512;
+  // TMEM columns: S of tile t at 128 t, O of tile t at 256 + D t
+  __device__ static constexpr uint32_t col_s(int t) { return 128u * static_cast<uint32_t>(t); }
+  __device__ static constexpr uint32_t col_o(int t) { return 256u + static_cast<uint32_t>(D * t); }
+};
+
+// barrier indices (8 bytes each) inside the barrier block
+enum : int {
+  BAR_Q = 0,
+  BAR_KV_FULL = 1,    // + slot (max 8)
+  BAR_KV_EMPTY = 9,   // + slot
+  BAR_S_FULL = 17,    // + tile
+  BAR_P_FULL = 19,    // + tile
+  BAR_O_FINAL = 21,   // + tile
+  BAR_DRAIN = 23,
+  kNumBars = 24,
+};
+constexpr int kOffTmemSlot = kNumBars * 8;
+constexpr int kOffAbort = kOffTmemSlot + 4;
+
+struct FwdArgs {
+  void* O;
+  float* LSE;
+  const int32_t* kv_lens;
+  int H, N;
+  int causal;
+  float scale_log2;  // scale * log2(e)
+  unsigned* status;
+};
+
+// Wait for a barrier phase ignoring the abort flag, for at most ~50 ms; used
+// only on the exit path to let in-flight asynchronous work land.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  const unsigned long long t0 = global_timer_ns();
+  while (!mbar_test(bar, parity)) {
+    if (global_timer_ns() - t0 > 50000000ull) break;
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+               const __grid_constant__ CUtensorMap tmV, const FwdArgs args) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t barbase = sbase + C::kOffBar;
+  auto bar = [&](int i) -> uint32_t { return barbase + 8u * static_cast<uint32_t>(i); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffBar + kOffTmemSlot);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffBar + kOffAbort);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int bh = blockIdx.x;
+  const int b = bh / args.H;
+  const int mblk = gridDim.y - 1 - blockIdx.y;  // longest causal work first
+  const int N = args.N;
+
+  int kv_len = N;
+  if (args.kv_lens != nullptr) kv_len = min(max(args.kv_lens[b], 0), N);
+  int n_t[2];
+  bool valid_t[2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int qt = 2 * mblk + t;
+    valid_t[t] = qt * kRows < N;
+    int end = kv_len;
+    if (args.causal) end = min(end, qt * kRows + kRows);
+    n_t[t] = valid_t[t] ? (end + kKeys - 1) / kKeys : 0;
+  }
+  const int nmax = max(n_t[0], n_t[1]);
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(BAR_Q), 1);
+    for (int s = 0; s < C::kSlots; ++s) {
+      mbar_init(bar(BAR_KV_FULL + s), 1);
+      mbar_init(bar(BAR_KV_EMPTY + s), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(BAR_S_FULL + t), 1);
+      mbar_init(bar(BAR_P_FULL + t), 4);
+      mbar_init(bar(BAR_O_FINAL + t), 1);
+    }
+    mbar_init(bar(BAR_DRAIN), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 8 && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtx wc{abort_flag, args.status};
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t qbytes = 0;
+      for (int t = 0; t < 2; ++t)
+        if (valid_t[t]) qbytes += C::kTileBytes;
+      if (qbytes != 0 && nmax > 0) {
+        mbar_arrive_expect_tx(bar(BAR_Q), qbytes);
+        for (int t = 0; t < 2; ++t) {
+          if (!valid_t[t]) continue;
+          for (int s = 0; s < C::kSub; ++s)
+            tma_load_3d(sbase + C::kOffQ + t * C::kTileBytes + s * C::kSubBytes, &tmQ, bar(BAR_Q), s * 64,
+                        (2 * mblk + t) * kRows, bh);
+        }
+      }
+      int issued = 0;
+      for (int u = 0; u < 2 * nmax; ++u) {
+        const int slot = u % C::kSlots;
+        const uint32_t ph = static_cast<uint32_t>(u / C::kSlots) & 1u;
+        if (!mbar_wait(bar(BAR_KV_EMPTY + slot), ph ^ 1u, wc)) break;
+        mbar_arrive_expect_tx(bar(BAR_KV_FULL + slot), C::kTileBytes);
+        const CUtensorMap* tm = (u & 1) ? &tmV : &tmK;
+        for (int s = 0; s < C::kSub; ++s)
+          tma_load_3d(sbase + C::kOffKV + slot * C::kTileBytes + s * C::kSubBytes, tm, bar(BAR_KV_FULL + slot), s * 64,
+                      (u >> 1) * kKeys, bh);
+        issued = u + 1;
+      }
+      // let every issued copy land before the CTA can exit
+      if (qbytes != 0 && nmax > 0) drain_wait(bar(BAR_Q), 0);
+      for (int s = 0; s < C::kSlots && s < issued; ++s) {
+        const int u_last = s + C::kSlots * ((issued - 1 - s) / C::kSlots);
+        drain_wait(bar(BAR_KV_FULL + s), static_cast<uint32_t>(u_last / C::kSlots) & 1u);
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && nmax > 0) {
+      constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t idPV = idesc_bf16_f32(128, D, false, true);
+      auto issue_S = [&](int t, int slot) {
+        const uint32_t a0 = sbase + C::kOffQ + t * C::kTileBytes;
+        const uint32_t b0 = sbase + C::kOffKV + slot * C::kTileBytes;
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * C::kSubBytes + (k & 3) * 32;
+          mma_ss(tmem + C::col_s(t), sdesc_sw128(a0 + off, 16, 1024), sdesc_sw128(b0 + off, 16, 1024), idS,
+                 k > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_PV = [&](int t, int slot, bool acc) {
+        const uint32_t a0 = sbase + C::kOffP + t * C::kPBytes;
+        const uint32_t b0 = sbase + C::kOffKV + slot * C::kTileBytes;
+#pragma unroll
+        for (int k = 0; k < kKeys / 16; ++k) {
+          const uint32_t aoff = (k >> 2) * (kRows * 128) + (k & 3) * 32;
+          const uint32_t boff = k * 16 * 128;
+          mma_ss(tmem + C::col_o(t), sdesc_sw128(a0 + aoff, 16, 1024), sdesc_sw128(b0 + boff, C::kSubBytes, 1024), idPV,
+                 (acc || k > 0) ? 1u : 0u);
+        }
+      };
+      bool ok = mbar_wait(bar(BAR_Q), 0, wc);
+      if (ok) ok = mbar_wait(bar(BAR_KV_FULL + 0), 0, wc);
+      if (ok) {
+        tc_fence_after();
+        for (int t = 0; t < 2; ++t)
+          if (n_t[t] > 0) {
+            issue_S(t, 0);
+            mma_commit(bar(BAR_S_FULL + t));
+          }
+        mma_commit(bar(BAR_KV_EMPTY + 0));
+      }
+      for (int j = 0; ok && j < nmax; ++j) {
+        const int uV = 2 * j + 1, uK = 2 * j + 2;
+        const int sV = uV % C::kSlots, sK = uK % C::kSlots;
+        const bool next = (j + 1) < nmax;
+        if (!mbar_wait(bar(BAR_KV_FULL + sV), static_cast<uint32_t>(uV / C::kSlots) & 1u, wc)) break;
+        if (next && !mbar_wait(bar(BAR_KV_FULL + sK), static_cast<uint32_t>(uK / C::kSlots) & 1u, wc)) break;
+        tc_fence_after();
+        for (int t = 0; t < 2; ++t) {
+          if (j < n_t[t]) {
+            if (!mbar_wait(bar(BAR_P_FULL + t), static_cast<uint32_t>(j) & 1u, wc)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_PV(t, sV, j > 0);
+            if (j == n_t[t] - 1) mma_commit(bar(BAR_O_FINAL + t));
+          }
+          if (j + 1 < n_t[t]) {
+            issue_S(t, sK);
+            mma_commit(bar(BAR_S_FULL + t));
+          }
+        }
+        if (!ok) break;
+        mma_commit(bar(BAR_KV_EMPTY + sV));
+        if (next) mma_commit(bar(BAR_KV_EMPTY + sK));
+      }
+      // every MMA issued above completes before the CTA releases TMEM
+      mma_commit(bar(BAR_DRAIN));
+      drain_wait(bar(BAR_DRAIN), 0);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax / epilogue
+    const int t = warp >> 2;
+    const int q4 = warp & 3;
+    const int r_in_tile = q4 * 32 + lane;
+    const int row = (2 * mblk + t) * kRows + r_in_tile;
+    const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
+    const uint32_t tS = tmem + lane_off + C::col_s(t);
+    const uint32_t tO = tmem + lane_off + C::col_o(t);
+    const uint32_t pbase = sbase + C::kOffP + t * C::kPBytes + r_in_tile * 128;
+    const int swz = r_in_tile & 7;
+    const float sl2 = args.scale_log2;
+    int last_key = kv_len - 1;
+    if (args.causal) last_key = min(last_key, row);
+
+    float m_ref = -INFINITY;
+    float l_sum = 0.f;
+    bool aborted = false;
+    const int n = n_t[t];
+    for (int j = 0; j < n; ++j) {
+      if (!mbar_wait(bar(BAR_S_FULL + t), static_cast<uint32_t>(j) & 1u, wc)) {
+        aborted = true;
+        break;
+      }
+      tc_fence_after();
+      float s[kKeys];
+      {
+        uint32_t r[64];
+        tmem_ld64(tS, r);
+#pragma unroll
+        for (int i = 0; i < 64; ++i) s[i] = __uint_as_float(r[i]);
+        tmem_ld64(tS + 64, r);
+#pragma unroll
+        for (int i = 0; i < 64; ++i) s[64 + i] = __uint_as_float(r[i]);
+      }
+      const int lim = last_key - j * kKeys;  // last visible key index within this tile
+      if (lim < kKeys - 1) {
+#pragma unroll
+        for (int i = 0; i < kKeys; ++i)
+          if (i > lim) s[i] = -INFINITY;
+      }
+      float mx[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx[i] = s[i];
+#pragma unroll
+      for (int i = 8; i < kKeys; ++i) mx[i & 7] = fmaxf(mx[i & 7], s[i]);
+      const float tile_max =
+          fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      const float x_max = tile_max * sl2;
+      const bool resc = x_max > m_ref + kRescaleLog2;
+      float alpha = 1.f;
+      if (resc) {
+        alpha = ex2_approx(m_ref - x_max);  // 0 when m_ref = -inf
+        m_ref = x_max;
+        l_sum *= alpha;
+      }
+      if (j > 0 && __any_sync(0xffffffffu, resc)) {
+        // O <- alpha * O for this warp's 32 rows (alpha = 1 in rows that keep their reference)
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t r[32];
+          tmem_ld32(tO + c0, r);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+          tmem_st32(tO + c0, r);
+        }
+        tmem_st_wait();
+      }
+      const float neg_ref = (m_ref == -INFINITY) ? 0.f : -m_ref;
+      float part[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int c = 0; c < kKeys / 8; ++c) {
+        float p[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          p[i] = ex2_approx(fmaf(s[8 * c + i], sl2, neg_ref));
+          part[i & 3] += p[i];
+        }
+        const uint32_t addr = pbase + (c >> 3) * (kRows * 128) + ((((c & 7) ^ swz)) << 4);
+        st_shared_v4(addr, pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]), pack_bf16x2(p[4], p[5]),
+                     pack_bf16x2(p[6], p[7]));
+      }
+      l_sum += (part[0] + part[1]) + (part[2] + part[3]);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(BAR_P_FULL + t));
+    }
+
+    if (valid_t[t] && !aborted) {
+      bool have_o = n > 0;
+      if (have_o) {
+        have_o = mbar_wait(bar(BAR_O_FINAL + t), 0, wc);
+        if (!have_o) aborted = true;
+      }
+      if (!aborted) {
+        tc_fence_after();
+        const bool empty = !(l_sum > 0.f);
+        const float inv = empty ? 0.f : 1.f / l_sum;
+        const bool in_range = row < N;
+        uint8_t* orow = static_cast<uint8_t*>(args.O) + (static_cast<size_t>(bh) * N + row) * (D * 2);
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t r[32];
+          if (have_o) {
+            tmem_ld32(tO + c0, r);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = 0u;
+          }
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            w[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * inv, __uint_as_float(r[2 * i + 1]) * inv);
+          if (in_range) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c0 * 2);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          }
+        }
+        if (in_range) {
+          const float lse = empty ? -INFINITY : (m_ref + lg2_approx(l_sum)) * 0.69314718055994531f;
+          args.LSE[static_cast<size_t>(bh) * N + row] = lse;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int D>
+fa_status fwd_launch_d(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N,
+                       int causal, float scale, const int32_t* kv_lens, cudaStream_t stream) {
+  using C = FwdCfg<D>;
+  const uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(N), static_cast<uint64_t>(B) * H};
+  const uint64_t strides[2] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(N) * D * 2};
+  const uint32_t box[3] = {64, kRows, 1};
+  CUtensorMap tq, tk, tv;
+  if (!encode_bf16_tmap(&tq, Q, 3, dims, strides, box) || !encode_bf16_tmap(&tk, K, 3, dims, strides, box) ||
+      !encode_bf16_tmap(&tv, V, 3, dims, strides, box))
+    return FA_ERR_CUDA;
+  static bool attr_set = false;  // per template instance; setting it twice is harmless
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
+      return FA_ERR_CUDA;
+    attr_set = true;
+  }
+  unsigned* status = device_status_ptr();
+  if (status == nullptr) return FA_ERR_CUDA;
+  FwdArgs a;
+  a.O = O;
+  a.LSE = LSE;
+  a.kv_lens = kv_lens;
+  a.H = H;
+  a.N = N;
+  a.causal = causal ? 1 : 0;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.status = status;
+  dim3 grid(B * H, ceil_div(N, 2 * kRows));
+  fwd_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, a);
+  return launch_status();
+}
+
+}  // namespace
+
+fa_status fwd_launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d,
+                     int causal, float scale, const int32_t* kv_lens, cudaStream_t stream) {
+  if (d == 64) return fwd_launch_d<64>(Q, K, V, O, LSE, B, H, N, causal, scale, kv_lens, stream);
+  if (d == 128) return fwd_launch_d<128>(Q, K, V, O, LSE, B, H, N, causal, scale, kv_lens, stream);
+  return FA_ERR_UNSUPPORTED;
+}
+
+}  // namespace fa

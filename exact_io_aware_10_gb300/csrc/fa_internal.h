@@ -1,0 +1,45 @@
+// Host-side plumbing shared by the library's translation units: tensor-map
+// encoding through the driver entry point, the per-device status word and
+// small launch helpers.  Not part of the public ABI (see include/fa.h).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/fa.h"
+#include "fa_status_bits.h"
+
+namespace fa {
+
+// Address of the library's device status word on the current device
+// (nullptr if CUDA fails).  Obtained once per device from a file-scope
+// __device__ variable; the library allocates no memory for it.
+unsigned* device_status_ptr();
+
+// Encode a tiled bf16 tensor map with the 128-byte swizzle.
+// dims/strides follow the CUDA driver convention: dims[0] innermost (elements),
+// strides_bytes[i] is the stride of dims[i + 1].  Returns false on failure.
+bool encode_bf16_tmap(CUtensorMap* map, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
+                      const uint32_t* box);
+
+inline int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
+
+inline fa_status launch_status() {
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+// Launchers implemented by the kernel translation units.  Arguments are
+// validated by the public entry points before these are called.
+fa_status fwd_launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d,
+                     int causal, float scale, const int32_t* kv_lens, cudaStream_t stream);
+fa_status bwd_launch(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
+                     void* dQ, void* dK, void* dV, int B, int H, int N, int d, int causal, float scale,
+                     const int32_t* kv_lens, void* workspace, cudaStream_t stream);
+fa_status decode_launch(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                        const int32_t* seq_lens, void* o, float* lse, int B, int Hq, int Hkv, int d, int block_size,
+                        int max_blocks, int num_blocks, int num_splits, float scale, void* workspace,
+                        cudaStream_t stream);
+
+}  // namespace fa

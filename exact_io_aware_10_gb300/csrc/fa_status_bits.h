@@ -1,0 +1,7 @@
+// Bits of the library's device status word (see fa_get_device_status).
+#pragma once
+
+namespace fa {
+constexpr unsigned kStatusTimeoutBit = 1u << 0;   // a bounded pipeline wait gave up
+constexpr unsigned kStatusBadTableBit = 1u << 1;  // a block-table entry was out of range
+}  // namespace fa

@@ -1,0 +1,197 @@
+"""Python binding of the C ABI in ``include/fa.h``.
+
+Argument marshalling only: tensors are checked for dtype/shape/contiguity,
+their device pointers and the current CUDA stream are handed to the shared
+library, and outputs / workspaces the caller did not pass are allocated with
+torch (device memory plumbing).  Every step of the attention path runs in the
+library's CUDA kernels; there is no fallback: if the library is missing the
+call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+from . import build as _build
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = 1
+FA_ERR_UNSUPPORTED = 2
+FA_ERR_CUDA = 3
+FA_ERR_TIMEOUT = 4
+FA_ERR_BAD_BLOCK_TABLE = 5
+
+# name -> (restype, argtypes); mirrors include/fa.h
+_vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+SIGNATURES = {
+    "fa_status_string": (ctypes.c_char_p, [_i]),
+    "fa_version": (_i, []),
+    "fa_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp]),
+    "fa_fwd_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp, _vp]),
+    "fa_bwd_workspace_size": (_sz, [_i, _i, _i, _i]),
+    "fa_bwd": (_i, [_vp] * 9 + [_i, _i, _i, _i, _i, _f, _vp, _vp, _sz, _vp]),
+    "fa_paged_decode_workspace_size": (_sz, [_i, _i, _i, _i]),
+    "fa_paged_decode": (_i, [_vp] * 7 + [_i] * 8 + [_f, _vp, _sz, _vp]),
+    "fa_get_device_status": (_i, [_vp]),
+}
+
+_LIB = None
+
+
+class FAError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        super().__init__(f"{where}: {status_string(status)} ({status})")
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load():
+    """Load the shared library (built by ``__graft_entry__.build()``)."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = library_path()
+    if not os.path.exists(path):
+        raise FileNotFoundError(f"{path} is missing: build it with __graft_entry__.build() "
+                                f"(python -m exact_io_aware_10_gb300.build)")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _LIB = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return load().fa_status_string(int(status)).decode()
+    except (FileNotFoundError, OSError):
+        return f"status {status}"
+
+
+def _check(status: int, where: str):
+    if status != FA_OK:
+        raise FAError(status, where)
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _need(t, dtype, shape, name):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def fa_fwd(Q, K, V, causal=False, scale=None, kv_lens=None, O=None, LSE=None, stream=None):
+    """O, LSE = attention(Q, K, V) for [B, H, N, d] bf16 CUDA tensors."""
+    lib = load()
+    B, H, N, d = Q.shape
+    for t, n in ((Q, "Q"), (K, "K"), (V, "V")):
+        _need(t, torch.bfloat16, (B, H, N, d), n)
+    if O is None:
+        O = torch.empty_like(Q)
+    if LSE is None:
+        LSE = torch.empty((B, H, N), dtype=torch.float32, device=Q.device)
+    _need(O, torch.bfloat16, (B, H, N, d), "O")
+    _need(LSE, torch.float32, (B, H, N), "LSE")
+    if kv_lens is not None:
+        _need(kv_lens, torch.int32, (B,), "kv_lens")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    st = lib.fa_fwd_ex(_p(Q), _p(K), _p(V), _p(O), _p(LSE), B, H, N, d, int(bool(causal)), scale, _p(kv_lens),
+                       _stream(stream))
+    _check(st, "fa_fwd")
+    return O, LSE
+
+
+def fa_bwd_workspace_size(B, H, N, d) -> int:
+    return int(load().fa_bwd_workspace_size(B, H, N, d))
+
+
+def fa_bwd(Q, K, V, O, dO, LSE, causal=False, scale=None, kv_lens=None, dQ=None, dK=None, dV=None,
+           workspace=None, stream=None):
+    """dQ, dK, dV of sum(dO * O) by recomputation from O and LSE."""
+    lib = load()
+    B, H, N, d = Q.shape
+    for t, n in ((Q, "Q"), (K, "K"), (V, "V"), (O, "O"), (dO, "dO")):
+        _need(t, torch.bfloat16, (B, H, N, d), n)
+    _need(LSE, torch.float32, (B, H, N), "LSE")
+    dQ = torch.empty_like(Q) if dQ is None else dQ
+    dK = torch.empty_like(K) if dK is None else dK
+    dV = torch.empty_like(V) if dV is None else dV
+    for t, n in ((dQ, "dQ"), (dK, "dK"), (dV, "dV")):
+        _need(t, torch.bfloat16, (B, H, N, d), n)
+    if kv_lens is not None:
+        _need(kv_lens, torch.int32, (B,), "kv_lens")
+    ws_bytes = fa_bwd_workspace_size(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=Q.device)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    st = lib.fa_bwd(_p(Q), _p(K), _p(V), _p(O), _p(dO), _p(LSE), _p(dQ), _p(dK), _p(dV), B, H, N, d,
+                    int(bool(causal)), scale, _p(kv_lens), _p(workspace), workspace.numel() * workspace.element_size(),
+                    _stream(stream))
+    _check(st, "fa_bwd")
+    return dQ, dK, dV
+
+
+def fa_paged_decode_workspace_size(B, Hq, d, num_splits=0) -> int:
+    return int(load().fa_paged_decode_workspace_size(B, Hq, d, num_splits))
+
+
+def fa_paged_decode(q, k_cache, v_cache, block_table, seq_lens, scale=None, num_splits=0, o=None, lse=None,
+                    workspace=None, stream=None, want_lse=True):
+    """Paged split-KV GQA decode: o [B, Hq, d] bf16 (and lse [B, Hq] fp32)."""
+    lib = load()
+    B, Hq, d = q.shape
+    NB, bs, Hkv, d2 = k_cache.shape
+    _need(q, torch.bfloat16, None, "q")
+    _need(k_cache, torch.bfloat16, None, "k_cache")
+    _need(v_cache, torch.bfloat16, (NB, bs, Hkv, d2), "v_cache")
+    _need(block_table, torch.int32, None, "block_table")
+    _need(seq_lens, torch.int32, (B,), "seq_lens")
+    if d2 != d:
+        raise ValueError("k_cache head dimension must match q")
+    if block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("block_table must be [B, max_blocks]")
+    max_blocks = int(block_table.shape[1])
+    o = torch.empty_like(q) if o is None else o
+    _need(o, torch.bfloat16, (B, Hq, d), "o")
+    if want_lse and lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _need(lse, torch.float32, (B, Hq), "lse")
+    ws_bytes = fa_paged_decode_workspace_size(B, Hq, d, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=q.device)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    st = lib.fa_paged_decode(_p(q), _p(k_cache), _p(v_cache), _p(block_table), _p(seq_lens), _p(o), _p(lse),
+                             B, Hq, Hkv, d, bs, max_blocks, NB, int(num_splits), scale, _p(workspace),
+                             workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "fa_paged_decode")
+    return o, lse
+
+
+def fa_get_device_status(stream=None) -> int:
+    """Synchronise the stream and return (then clear) the device status code."""
+    return int(load().fa_get_device_status(_stream(stream)))

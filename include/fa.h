@@ -1,0 +1,149 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) exact IO-aware attention library.
+ *
+ * The library computes exact softmax attention without writing the N x N
+ * score matrix to device memory, following the FlashAttention method as the
+ * study notes "精读笔记 08：FlashAttention" describe it (§2.1 standard
+ * attention, §3.1 online softmax, §3.2 tiling, §3.3 recomputation, §3.4
+ * fusion) and the paged / split-KV decode of the tutorial chapter
+ * "S12 FlashAttention" ("实现", flash-decoding, grouped-query heads).
+ *
+ * Conventions for every entry point
+ *   - Pointers are DEVICE pointers unless stated; the caller owns every
+ *     buffer (inputs, outputs, workspaces).  No entry point allocates device
+ *     memory.
+ *   - bf16 tensors are IEEE bfloat16 stored as 16-bit words; "bf16*" below is
+ *     written as void*.  Layout [B, H, N, d] is row-major and contiguous
+ *     (d fastest).  Base addresses must be 16-byte aligned.
+ *   - d (head dimension) must be 64 or 128, else FA_ERR_UNSUPPORTED.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call
+ *     is asynchronous: the returned status covers argument validation and
+ *     launch errors only.  Errors the GPU detects (a timed-out pipeline wait,
+ *     an out-of-range block-table entry) are latched in a device status word
+ *     and returned by fa_get_device_status().
+ *   - Scores are s_ij = scale * <q_i, k_j>; LSE_i = ln sum_j exp(s_ij) over
+ *     the visible keys (natural log).  A query row with no visible key gets
+ *     O_i = 0 and LSE_i = -inf; no NaN is produced for finite inputs.
+ *   - Return values are fa_status codes (as int).
+ */
+#ifndef FA_GB300_H_
+#define FA_GB300_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fa_status {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,     /* null pointer, negative size, bad combination */
+  FA_ERR_UNSUPPORTED = 2,     /* valid request outside what the kernels cover (e.g. d = 96) */
+  FA_ERR_CUDA = 3,            /* a CUDA runtime/driver call or launch failed */
+  FA_ERR_TIMEOUT = 4,         /* device: a bounded pipeline wait gave up */
+  FA_ERR_BAD_BLOCK_TABLE = 5  /* device: a block-table entry was outside [0, num_blocks) */
+} fa_status;
+
+/* Human-readable name of a status code; never NULL. */
+const char* fa_status_string(int status);
+
+/* ABI version of this header (major * 100 + minor). */
+int fa_version(void);
+
+/*
+ * Forward attention (the tiled, fused forward of the notes' §3.2 / §3.4 with
+ * the online-softmax recurrence of §3.1).
+ *   Q, K, V : [B, H, N, d] bf16, read only.
+ *   O       : [B, H, N, d] bf16, written: O = softmax(scale Q K^T) V per (b, h).
+ *   LSE     : [B, H, N] fp32, written: per-row log-sum-exp (the row statistic
+ *             that replaces the notes' (m, l) pair, §3.3).
+ *   causal  : non-zero masks key j > query i (top-left aligned, square).
+ *   scale   : logit scale, typically 1/sqrt(d); must be finite and > 0.
+ * B, H >= 1, N >= 0 (N = 0 is a no-op).  Errors: FA_ERR_INVALID_ARG,
+ * FA_ERR_UNSUPPORTED, FA_ERR_CUDA.
+ */
+int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d, int causal,
+           float scale, void* stream);
+
+/*
+ * fa_fwd with a key-padding mask: kv_lens (device int32 [B], may be NULL)
+ * gives the number of valid keys L_b of each batch entry; keys j >= L_b are
+ * masked for every query row (values are clamped to [0, N]).  All N query
+ * rows are still computed and written.
+ */
+int fa_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d,
+              int causal, float scale, const int32_t* kv_lens, void* stream);
+
+/*
+ * Bytes of device workspace fa_bwd needs: an fp32 [B, H, N] row-dot buffer
+ * D = rowsum(dO * O) and an fp32 [B, H, N, d] dQ accumulator, each rounded up
+ * to 256 bytes.  0 on invalid sizes.
+ */
+size_t fa_bwd_workspace_size(int B, int H, int N, int d);
+
+/*
+ * Backward attention by recomputation (notes §3.3: keep O and the row
+ * statistics, rebuild the score tiles on chip).  Gradients of
+ * sum(dO * O) for O = fa_fwd(Q, K, V):
+ *   dV = P^T dO,  dP = dO V^T,  D = rowsum(dO * O),  dS = P * (dP - D),
+ *   dQ = scale dS K,  dK = scale dS^T Q,   with P = exp(scale Q K^T - LSE).
+ *   Q, K, V, O, dO : [B, H, N, d] bf16 (O and LSE from fa_fwd/fa_fwd_ex with
+ *                    the same causal, scale and kv_lens).
+ *   LSE            : [B, H, N] fp32.
+ *   dQ, dK, dV     : [B, H, N, d] bf16, written.  Padded keys get dK = dV = 0.
+ *   kv_lens        : as in fa_fwd_ex, may be NULL.
+ *   workspace      : device buffer of at least fa_bwd_workspace_size() bytes,
+ *                    256-byte aligned; contents on entry are ignored.
+ * Errors: FA_ERR_INVALID_ARG (including ws_bytes too small),
+ * FA_ERR_UNSUPPORTED, FA_ERR_CUDA.
+ */
+int fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE, void* dQ,
+           void* dK, void* dV, int B, int H, int N, int d, int causal, float scale, const int32_t* kv_lens,
+           void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Bytes of device workspace fa_paged_decode needs for `num_splits` partial
+ * (m, l, o) states per (batch, query head): fp32 [B, Hq, num_splits, d + 2],
+ * rounded up to 256 bytes.  num_splits = 0 means the automatic choice (16).
+ */
+size_t fa_paged_decode_workspace_size(int B, int Hq, int d, int num_splits);
+
+/*
+ * Paged, split-KV, grouped-query decode (S12 "实现" paged loop, flash-decoding
+ * split + (m, l, o) merge, GQA head sharing).
+ *   q           : [B, Hq, d] bf16, one query token per sequence.
+ *   k_cache,
+ *   v_cache     : [num_blocks, block_size, Hkv, d] bf16; key t of sequence b
+ *                 and KV head g is k_cache[block_table[b][t / block_size],
+ *                 t % block_size, g, :].
+ *   block_table : [B, max_blocks] int32; entries past ceil(L_b / block_size)
+ *                 are never read.  An entry outside [0, num_blocks) is skipped
+ *                 (its keys are treated as masked) and latches
+ *                 FA_ERR_BAD_BLOCK_TABLE in the device status word.
+ *   seq_lens    : [B] int32 context lengths L_b, 0 <= L_b <= max_blocks *
+ *                 block_size (larger values are clamped to that bound).
+ *   o           : [B, Hq, d] bf16, written.  lse: [B, Hq] fp32 or NULL.
+ *   Query head h reads KV head h / (Hq / Hkv); Hq % Hkv must be 0.
+ *   block_size  : 16.  num_splits: 1..16, or 0 for automatic (16).
+ *   workspace   : at least fa_paged_decode_workspace_size(B, Hq, d,
+ *                 num_splits) bytes, 256-byte aligned.
+ * Errors: FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA.
+ */
+int fa_paged_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                    const int32_t* seq_lens, void* o, float* lse, int B, int Hq, int Hkv, int d, int block_size,
+                    int max_blocks, int num_blocks, int num_splits, float scale, void* workspace, size_t ws_bytes,
+                    void* stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the device status word of
+ * the current device: FA_OK, FA_ERR_TIMEOUT or FA_ERR_BAD_BLOCK_TABLE (the
+ * first two bits latched since the last call, timeout first), or FA_ERR_CUDA.
+ */
+int fa_get_device_status(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H_ */

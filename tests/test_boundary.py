@@ -1,0 +1,97 @@
+"""The C-ABI library loads on the host, exports every entry point declared in
+include/fa.h, and rejects invalid arguments before touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from exact_io_aware_10_gb300 import build as fab
+from exact_io_aware_10_gb300 import lib as fl
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+
+@pytest.fixture(scope="module")
+def so():
+    fab.build()
+    return fl.load()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("fa_fwd", "fa_fwd_ex", "fa_bwd", "fa_bwd_workspace_size", "fa_paged_decode",
+              "fa_paged_decode_workspace_size", "fa_get_device_status", "fa_status_string", "fa_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(so):
+    for n in declared_functions():
+        assert hasattr(so, n), n
+    assert set(declared_functions()) <= set(fl.SIGNATURES)
+
+
+def test_status_strings(so):
+    for code, name in [(0, "FA_OK"), (1, "FA_ERR_INVALID_ARG"), (2, "FA_ERR_UNSUPPORTED"), (3, "FA_ERR_CUDA"),
+                       (4, "FA_ERR_TIMEOUT"), (5, "FA_ERR_BAD_BLOCK_TABLE")]:
+        assert so.fa_status_string(code).decode() == name
+    assert so.fa_status_string(99).decode() == "FA_ERR_UNKNOWN"
+    assert so.fa_version() == 100
+
+
+def _fake(n=1):
+    # 256-byte aligned fake device addresses; validation rejects before any use
+    return [ctypes.c_void_p(0x10000000 + 0x1000 * i) for i in range(n)]
+
+
+def test_forward_argument_validation(so):
+    Q, K, V, O, L = _fake(5)
+    s = ctypes.c_void_p(0)
+    assert so.fa_fwd(Q, K, V, O, L, 1, 1, 16, 96, 0, 0.1, s) == fl.FA_ERR_UNSUPPORTED
+    assert so.fa_fwd(Q, K, V, O, L, 0, 1, 16, 64, 0, 0.1, s) == fl.FA_ERR_INVALID_ARG
+    assert so.fa_fwd(Q, K, V, O, L, 1, 1, -1, 64, 0, 0.1, s) == fl.FA_ERR_INVALID_ARG
+    assert so.fa_fwd(None, K, V, O, L, 1, 1, 16, 64, 0, 0.1, s) == fl.FA_ERR_INVALID_ARG
+    assert so.fa_fwd(Q, K, V, O, L, 1, 1, 16, 64, 0, 0.0, s) == fl.FA_ERR_INVALID_ARG
+    assert so.fa_fwd(Q, K, V, O, L, 1, 1, 16, 64, 0, float("nan"), s) == fl.FA_ERR_INVALID_ARG
+    assert so.fa_fwd(ctypes.c_void_p(0x10000008), K, V, O, L, 1, 1, 16, 64, 0, 0.1, s) == fl.FA_ERR_INVALID_ARG
+    # N = 0 is a valid no-op and launches nothing
+    assert so.fa_fwd(Q, K, V, O, L, 1, 1, 0, 64, 0, 0.1, s) == fl.FA_OK
+
+
+def test_backward_argument_validation(so):
+    ptrs = _fake(10)
+    s = ctypes.c_void_p(0)
+    need = so.fa_bwd_workspace_size(2, 3, 100, 64)
+    rows = 2 * 3 * 100
+    assert need == ((rows * 4 + 255) // 256) * 256 + ((rows * 64 * 4 + 255) // 256) * 256
+    assert so.fa_bwd_workspace_size(0, 1, 1, 64) == 0
+    assert so.fa_bwd(*ptrs[:9], 2, 3, 100, 64, 0, 0.1, None, ptrs[9], need - 1, s) == fl.FA_ERR_INVALID_ARG
+    assert so.fa_bwd(*ptrs[:9], 2, 3, 100, 64, 0, 0.1, None, None, need, s) == fl.FA_ERR_INVALID_ARG
+    assert so.fa_bwd(*ptrs[:9], 2, 3, 100, 80, 0, 0.1, None, ptrs[9], need, s) == fl.FA_ERR_UNSUPPORTED
+
+
+def test_decode_argument_validation(so):
+    q, kc, vc, bt, sl, o, lse, ws = _fake(8)
+    s = ctypes.c_void_p(0)
+    need = so.fa_paged_decode_workspace_size(4, 32, 128, 0)
+    assert need == ((4 * 32 * 16 * 130 * 4 + 255) // 256) * 256
+    assert so.fa_paged_decode_workspace_size(4, 32, 128, 17) == 0
+    args = dict(B=4, Hq=32, Hkv=8, d=128, bs=16, mb=8, nb=32, S=0)
+
+    def call(**kw):
+        a = {**args, **kw}
+        return so.fa_paged_decode(q, kc, vc, bt, sl, o, lse, a["B"], a["Hq"], a["Hkv"], a["d"], a["bs"], a["mb"],
+                                  a["nb"], a["S"], 0.088, ws, need, s)
+
+    assert call(Hkv=5) == fl.FA_ERR_INVALID_ARG          # Hq % Hkv != 0
+    assert call(d=64) == fl.FA_ERR_UNSUPPORTED
+    assert call(bs=32) == fl.FA_ERR_UNSUPPORTED
+    assert call(S=17) == fl.FA_ERR_UNSUPPORTED
+    assert call(nb=0) == fl.FA_ERR_INVALID_ARG
