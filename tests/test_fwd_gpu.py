@@ -24,11 +24,12 @@ def _run(fa, x, causal, kv_lens=None, scale=None):
     return O.float().cpu().numpy(), L.cpu().numpy()
 
 
-def _check(O, L, Oref, Lref):
+def _check(O, L, Oref, Lref, v_std=1.0):
+    # the O bounds are stated for unit-variance values; they scale with |V|
     err = np.abs(O - Oref)
     assert np.isfinite(O).all()
-    assert err.max() <= O_MAX, err.max()
-    assert err.mean() <= O_MEAN, err.mean()
+    assert err.max() <= O_MAX * v_std, err.max()
+    assert err.mean() <= O_MEAN * v_std, err.mean()
     fin = np.isfinite(Lref)
     assert np.array_equal(np.isfinite(L), fin)
     assert np.abs(L[fin] - Lref[fin]).max(initial=0) <= LSE_TOL
@@ -94,7 +95,7 @@ def test_large_logits_and_custom_scale(fa):
     for causal in (False, True):
         O, L = _run(fa, x, causal, scale=1.0)
         Oref, Lref = oracle.attention_forward(x.Q, x.K, x.V, causal=causal, scale=1.0)
-        _check(O, L, Oref, Lref)
+        _check(O, L, Oref, Lref, v_std=3.0)
 
 
 def test_deterministic(fa):
