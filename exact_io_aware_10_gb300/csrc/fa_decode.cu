@@ -1,9 +1,384 @@
-// Paged decode (placeholder until the split-KV kernels land).
+// Paged, split-KV, grouped-query decode ("S12 FlashAttention": the paged loop
+// of "实现", flash-decoding's split + (m, l, o) merge, and GQA head sharing).
+//
+// Kernel 1 (split): one CTA per (split s, KV head g, sequence b).  The split's
+// logical blocks are gathered through the block table by TMA (each 16-token
+// block of KV head g is a 16 x 128 bf16 box, K and V) into an 8-stage shared-
+// memory ring.  Four consumer warps take the blocks round-robin; each keeps
+// its own online-softmax state for the G = Hq / Hkv query heads of the group
+// (one KV read serves all G heads).  The 16-row tensor-core tile holds the G
+// heads (rows >= G are zero), so scores and P V are mma.sync m16n8k16
+// products; the kernel is bound by the KV stream from HBM, not by them.
+// At the end the four warp states merge in shared memory into one partial
+// (m, l, o) per (b, head, split), written to the workspace.
+//
+// Kernel 2 (combine): one warp per (b, query head) merges the splits:
+// m = max m_s, l = sum 2^(m_s - m) l_s, o = sum 2^(m_s - m) o_s / l, skipping
+// empty splits ("精读笔记 08：FlashAttention" §3.1 merge rule).
+//
+// All maxima are kept in log2 units of the scaled logit (x = scale log2(e) q.k).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+
 #include "fa_internal.h"
+#include "sm103.cuh"
 
 namespace fa {
-fa_status decode_launch(const void*, const void*, const void*, const int32_t*, const int32_t*, void*, float*, int, int,
-                        int, int, int, int, int, int, float, void*, cudaStream_t) {
-  return FA_ERR_UNSUPPORTED;
+namespace {
+
+constexpr int kD = 128;            // head dimension
+constexpr int kBlk = 16;           // tokens per cache block
+constexpr int kConsumers = 4;      // consumer warps
+constexpr int kThreads = 32 * (kConsumers + 1);
+constexpr int kStages = 8;
+constexpr int kHalfBytes = kBlk * 128;           // 16 rows x 128 B (64 bf16)
+constexpr int kStageBytes = 4 * kHalfBytes;      // K lo, K hi, V lo, V hi
+constexpr int kOffBar = kStages * kStageBytes;   // 64 KiB of stages
+constexpr int kMergeBytes = kConsumers * (16 * kD + 32) * 4;  // per-warp O rows + m, l
+constexpr int kSmemBytes = kOffBar + 256 + 1024;
+static_assert(kMergeBytes <= kOffBar, "merge scratch reuses the stage ring");
+constexpr int kMinBlocksPerSplit = 32;  // at most one split per 512 keys
+
+__host__ __device__ inline int splits_for(int nblocks, int max_splits) {
+  int s = (nblocks + kMinBlocksPerSplit - 1) / kMinBlocksPerSplit;
+  return max(1, min(max_splits, s));
 }
+
+struct DecArgs {
+  const __nv_bfloat16* q;  // [B, Hq, D]
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  float* part;  // [B, Hq, S, D + 2]: o (unnormalised), m (log2 units), l
+  __nv_bfloat16* o;
+  float* lse;
+  int B, Hq, Hkv, G, max_blocks, num_blocks, S;
+  float scale_log2;
+  unsigned* status;
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Address of 16-byte chunk `cd` (0..15 along d) of row `row` in a K or V block
+// stored as two 128-byte-swizzled halves of 16 rows.
+__device__ __forceinline__ uint32_t chunk_addr(uint32_t base, int row, int cd) {
+  return base + (cd >> 3) * kHalfBytes + row * 128 + ((((cd & 7) ^ (row & 7))) << 4);
+}
+
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  const unsigned long long t0 = global_timer_ns();
+  while (!mbar_test(bar, parity)) {
+    if (global_timer_ns() - t0 > 50000000ull) break;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 3)
+    decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                        const DecArgs a) {
+  const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int L = min(max(a.seq_lens[b], 0), a.max_blocks * kBlk);
+  const int nb = (L + kBlk - 1) / kBlk;
+  const int S_b = splits_for(nb, a.S);
+  if (s >= S_b) return;  // this sequence uses fewer splits
+  const int lo = static_cast<int>((static_cast<long long>(s) * nb) / S_b);
+  const int hi = static_cast<int>((static_cast<long long>(s + 1) * nb) / S_b);
+  const int nblk = hi - lo;
+  const int32_t* table = a.block_table + static_cast<size_t>(b) * a.max_blocks;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  auto full = [&](int i) -> uint32_t { return sbase + kOffBar + 8u * i; };
+  auto empty = [&](int i) -> uint32_t { return sbase + kOffBar + 8u * (kStages + i); };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffBar + 8 * 2 * kStages);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(full(i), 1);
+      mbar_init(empty(i), 1);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const WaitCtx wc{abort_flag, a.status};
+
+  // per-thread softmax state for rows r0 = lane / 4 and r0 + 8 of the group
+  float m_run[2] = {-INFINITY, -INFINITY};
+  float l_run[2] = {0.f, 0.f};
+  float acc[16][4];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+
+  if (warp == kConsumers) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      int issued = 0;
+      for (int i = 0; i < nblk; ++i) {
+        const int st = i % kStages;
+        if (!mbar_wait(empty(st), ((i / kStages) & 1) ^ 1, wc)) break;
+        const int phys = __ldg(table + lo + i);
+        if (phys >= 0 && phys < a.num_blocks) {
+          mbar_arrive_expect_tx(full(st), kStageBytes);
+          const uint32_t dst = sbase + st * kStageBytes;
+          const int z = phys * kBlk;
+          tma_load_3d(dst, &tmK, full(st), 0, g, z);
+          tma_load_3d(dst + kHalfBytes, &tmK, full(st), 64, g, z);
+          tma_load_3d(dst + 2 * kHalfBytes, &tmV, full(st), 0, g, z);
+          tma_load_3d(dst + 3 * kHalfBytes, &tmV, full(st), 64, g, z);
+        } else {
+          atomicOr(a.status, kStatusBadTableBit);
+          mbar_arrive(full(st));  // nothing to load: the consumer masks this block
+        }
+        issued = i + 1;
+      }
+      for (int st = 0; st < kStages && st < issued; ++st) {
+        const int i_last = st + kStages * ((issued - 1 - st) / kStages);
+        drain_wait(full(st), (i_last / kStages) & 1);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ consumers
+    const int r0 = lane >> 2;
+    const int c2 = 2 * (lane & 3);
+    const int h0 = g * a.G;
+    // Q as the A operand (16 x 128, rows >= G are zero), kept in registers
+    uint32_t qa[8][4];
+    {
+      const uint32_t* q0 = reinterpret_cast<const uint32_t*>(a.q + (static_cast<size_t>(b) * a.Hq + h0 + r0) * kD);
+      const uint32_t* q8 = reinterpret_cast<const uint32_t*>(a.q + (static_cast<size_t>(b) * a.Hq + h0 + r0 + 8) * kD);
+      const bool v0 = r0 < a.G, v8 = r0 + 8 < a.G;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const int col = (16 * ks + c2) >> 1;  // in bf16 pairs
+        qa[ks][0] = v0 ? __ldg(q0 + col) : 0u;
+        qa[ks][1] = v8 ? __ldg(q8 + col) : 0u;
+        qa[ks][2] = v0 ? __ldg(q0 + col + 4) : 0u;
+        qa[ks][3] = v8 ? __ldg(q8 + col + 4) : 0u;
+      }
+    }
+    const float sl2 = a.scale_log2;
+    // ldmatrix lane roles: matrix m = lane / 8, row i = lane % 8
+    const int lm = lane >> 3, li = lane & 7;
+    for (int i = warp; i < nblk; i += kConsumers) {
+      const int st = i % kStages;
+      if (!mbar_wait(full(st), (i / kStages) & 1, wc)) break;
+      const uint32_t stK = sbase + st * kStageBytes;
+      const uint32_t stV = stK + 2 * kHalfBytes;
+      const int phys = __ldg(table + lo + i);
+      const bool bad = !(phys >= 0 && phys < a.num_blocks);
+      // ---- S = Q K^T over 16 keys (two n8 tiles)
+      float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        uint32_t k0, k1, k2, k3;
+        const int key = 8 * (lm >> 1) + li;
+        ldsm_x4(chunk_addr(stK, key, 2 * ks + (lm & 1)), k0, k1, k2, k3);
+        mma_16816(sc[0], qa[ks], k0, k1);
+        mma_16816(sc[1], qa[ks], k2, k3);
+      }
+      // ---- mask keys past the sequence end (and whole skipped blocks)
+      const int kbase = (lo + i) * kBlk + c2;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int kidx = kbase + 8 * nt + (e & 1);
+          sc[nt][e] = (bad || kidx >= L) ? -INFINITY : sc[nt][e] * sl2;
+        }
+      // ---- online softmax for rows r0 (e = 0, 1) and r0 + 8 (e = 2, 3)
+      float alpha[2];
+      uint32_t pa[4];
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr) {
+        float mx = fmaxf(fmaxf(sc[0][2 * rr], sc[0][2 * rr + 1]), fmaxf(sc[1][2 * rr], sc[1][2 * rr + 1]));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float m_new = fmaxf(m_run[rr], mx);
+        const float sub = (m_new == -INFINITY) ? 0.f : m_new;
+        alpha[rr] = ex2_approx(m_run[rr] - sub);
+        m_run[rr] = m_new;
+        const float p0 = ex2_approx(sc[0][2 * rr] - sub), p1 = ex2_approx(sc[0][2 * rr + 1] - sub);
+        const float p2 = ex2_approx(sc[1][2 * rr] - sub), p3 = ex2_approx(sc[1][2 * rr + 1] - sub);
+        l_run[rr] = l_run[rr] * alpha[rr] + ((p0 + p1) + (p2 + p3));
+        pa[rr] = pack_bf16x2(p0, p1);      // keys 0-7 : a0a1 (row r0) / a2a3 (row r0+8)
+        pa[2 + rr] = pack_bf16x2(p2, p3);  // keys 8-15: a4a5 / a6a7
+      }
+#pragma unroll
+      for (int dn = 0; dn < 16; ++dn) {
+        acc[dn][0] *= alpha[0];
+        acc[dn][1] *= alpha[0];
+        acc[dn][2] *= alpha[1];
+        acc[dn][3] *= alpha[1];
+      }
+      // ---- O += P V  (V^T fragments through ldmatrix.trans)
+#pragma unroll
+      for (int dn2 = 0; dn2 < 8; ++dn2) {
+        uint32_t v0, v1, v2, v3;
+        const int key = 8 * (lm & 1) + li;
+        ldsm_x4_t(chunk_addr(stV, key, 2 * dn2 + (lm >> 1)), v0, v1, v2, v3);
+        mma_16816(acc[2 * dn2], pa, v0, v1);
+        mma_16816(acc[2 * dn2 + 1], pa, v2, v3);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty(st));
+    }
+    // quad-reduce the row sums (each lane summed its own key columns)
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      l_run[rr] += __shfl_xor_sync(0xffffffffu, l_run[rr], 1);
+      l_run[rr] += __shfl_xor_sync(0xffffffffu, l_run[rr], 2);
+    }
+  }
+
+  // ---------------------------------------------------------------- merge warps
+  __syncthreads();  // every stage consumed; the ring becomes merge scratch
+  float* sO = reinterpret_cast<float*>(smem);               // [warp][16][D]
+  float* sML = sO + kConsumers * 16 * kD;                   // [warp][16][2]
+  if (warp < kConsumers) {
+    const int r0 = lane >> 2, c2 = 2 * (lane & 3);
+    float* w = sO + warp * 16 * kD;
+#pragma unroll
+    for (int dn = 0; dn < 16; ++dn) {
+      *reinterpret_cast<float2*>(w + r0 * kD + 8 * dn + c2) = make_float2(acc[dn][0], acc[dn][1]);
+      *reinterpret_cast<float2*>(w + (r0 + 8) * kD + 8 * dn + c2) = make_float2(acc[dn][2], acc[dn][3]);
+    }
+    if ((lane & 3) == 0) {
+      sML[(warp * 16 + r0) * 2 + 0] = m_run[0];
+      sML[(warp * 16 + r0) * 2 + 1] = l_run[0];
+      sML[(warp * 16 + r0 + 8) * 2 + 0] = m_run[1];
+      sML[(warp * 16 + r0 + 8) * 2 + 1] = l_run[1];
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x < kD) {
+    const int dcol = threadIdx.x;
+    for (int r = 0; r < a.G; ++r) {
+      float m = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kConsumers; ++w) m = fmaxf(m, sML[(w * 16 + r) * 2]);
+      float o = 0.f, l = 0.f;
+      if (m != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < kConsumers; ++w) {
+          const float wm = sML[(w * 16 + r) * 2];
+          const float f = ex2_approx(wm - m);  // 0 for warps that saw nothing
+          o += f * sO[(w * 16 + r) * kD + dcol];
+          l += f * sML[(w * 16 + r) * 2 + 1];
+        }
+      }
+      float* dst = a.part + ((static_cast<size_t>(b) * a.Hq + g * a.G + r) * a.S + s) * (kD + 2);
+      dst[dcol] = o;
+      if (dcol == 0) {
+        dst[kD] = m;
+        dst[kD + 1] = l;
+      }
+    }
+  }
+}
+
+// One warp per (b, query head): merge the sequence's split states.
+__global__ void __launch_bounds__(256) decode_combine_kernel(const DecArgs a) {
+  const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (gw >= a.B * a.Hq) return;
+  const int b = gw / a.Hq;
+  const int L = min(max(a.seq_lens[b], 0), a.max_blocks * kBlk);
+  const int S_b = splits_for((L + kBlk - 1) / kBlk, a.S);
+  const float* base = a.part + static_cast<size_t>(gw) * a.S * (kD + 2);
+  float m = -INFINITY;
+  for (int s = 0; s < S_b; ++s) {
+    const float* p = base + s * (kD + 2);
+    if (p[kD + 1] > 0.f) m = fmaxf(m, p[kD]);
+  }
+  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+  float l = 0.f;
+  if (m != -INFINITY) {
+    for (int s = 0; s < S_b; ++s) {
+      const float* p = base + s * (kD + 2);
+      const float ls = p[kD + 1];
+      if (!(ls > 0.f)) continue;
+      const float f = ex2_approx(p[kD] - m);
+      const float4 v = *reinterpret_cast<const float4*>(p + 4 * lane);
+      o.x += f * v.x;
+      o.y += f * v.y;
+      o.z += f * v.z;
+      o.w += f * v.w;
+      l += f * ls;
+    }
+  }
+  const float inv = (l > 0.f) ? 1.f / l : 0.f;
+  uint2 w;
+  w.x = pack_bf16x2(o.x * inv, o.y * inv);
+  w.y = pack_bf16x2(o.z * inv, o.w * inv);
+  *reinterpret_cast<uint2*>(a.o + static_cast<size_t>(gw) * kD + 4 * lane) = w;
+  if (a.lse != nullptr && lane == 0)
+    a.lse[gw] = (l > 0.f) ? (m + lg2_approx(l)) * 0.69314718055994531f : -INFINITY;
+}
+
+}  // namespace
+
+fa_status decode_launch(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                        const int32_t* seq_lens, void* o, float* lse, int B, int Hq, int Hkv, int d, int block_size,
+                        int max_blocks, int num_blocks, int num_splits, float scale, void* workspace,
+                        cudaStream_t stream) {
+  if (d != kD || block_size != kBlk) return FA_ERR_UNSUPPORTED;
+  const uint64_t dims[3] = {static_cast<uint64_t>(kD), static_cast<uint64_t>(Hkv),
+                            static_cast<uint64_t>(num_blocks) * kBlk};
+  const uint64_t strides[2] = {static_cast<uint64_t>(kD) * 2, static_cast<uint64_t>(Hkv) * kD * 2};
+  const uint32_t box[3] = {64, 1, kBlk};
+  CUtensorMap tk, tv;
+  if (!encode_bf16_tmap(&tk, k_cache, 3, dims, strides, box) || !encode_bf16_tmap(&tv, v_cache, 3, dims, strides, box))
+    return FA_ERR_CUDA;
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(decode_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+        cudaSuccess)
+      return FA_ERR_CUDA;
+    attr_set = true;
+  }
+  unsigned* status = device_status_ptr();
+  if (status == nullptr) return FA_ERR_CUDA;
+  DecArgs a;
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.block_table = block_table;
+  a.seq_lens = seq_lens;
+  a.part = static_cast<float*>(workspace);
+  a.o = static_cast<__nv_bfloat16*>(o);
+  a.lse = lse;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.G = Hq / Hkv;
+  a.max_blocks = max_blocks;
+  a.num_blocks = num_blocks;
+  a.S = num_splits;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.status = status;
+  dim3 grid(num_splits, Hkv, B);
+  decode_split_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tk, tv, a);
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+  decode_combine_kernel<<<ceil_div(static_cast<long long>(B) * Hq, 8), 256, 0, stream>>>(a);
+  return launch_status();
+}
+
 }  // namespace fa
