@@ -146,7 +146,8 @@ int fa_bwd(const void* Q, const void* K, const void* V, const void* O, const voi
 size_t fa_paged_decode_workspace_size(int B, int Hq, int d, int num_splits) {
   if (B < 1 || Hq < 1 || d < 1 || num_splits < 0 || num_splits > 16) return 0;
   const int S = num_splits == 0 ? 16 : num_splits;
-  return round256(static_cast<size_t>(B) * Hq * S * (d + 2) * sizeof(float));
+  const size_t n = static_cast<size_t>(B) * Hq * S;
+  return round256(n * d * sizeof(float)) + round256(n * 2 * sizeof(float));
 }
 
 int fa_paged_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,

@@ -49,7 +49,8 @@ struct DecArgs {
   const __nv_bfloat16* q;  // [B, Hq, D]
   const int32_t* block_table;
   const int32_t* seq_lens;
-  float* part;  // [B, Hq, S, D + 2]: o (unnormalised), m (log2 units), l
+  float* part_o;   // [B, Hq, S, D] unnormalised o of each split (rows 512 B, 16-byte aligned)
+  float* part_ml;  // [B, Hq, S, 2] m (log2 units), l
   __nv_bfloat16* o;
   float* lse;
   int B, Hq, Hkv, G, max_blocks, num_blocks, S;
@@ -286,11 +287,11 @@ __global__ void __launch_bounds__(kThreads, 3)
           l += f * sML[(w * 16 + r) * 2 + 1];
         }
       }
-      float* dst = a.part + ((static_cast<size_t>(b) * a.Hq + g * a.G + r) * a.S + s) * (kD + 2);
-      dst[dcol] = o;
+      const size_t idx = (static_cast<size_t>(b) * a.Hq + g * a.G + r) * a.S + s;
+      a.part_o[idx * kD + dcol] = o;
       if (dcol == 0) {
-        dst[kD] = m;
-        dst[kD + 1] = l;
+        a.part_ml[2 * idx] = m;
+        a.part_ml[2 * idx + 1] = l;
       }
     }
   }
@@ -304,21 +305,19 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecArgs a) {
   const int b = gw / a.Hq;
   const int L = min(max(a.seq_lens[b], 0), a.max_blocks * kBlk);
   const int S_b = splits_for((L + kBlk - 1) / kBlk, a.S);
-  const float* base = a.part + static_cast<size_t>(gw) * a.S * (kD + 2);
+  const float* po = a.part_o + static_cast<size_t>(gw) * a.S * kD;
+  const float* pml = a.part_ml + static_cast<size_t>(gw) * a.S * 2;
   float m = -INFINITY;
-  for (int s = 0; s < S_b; ++s) {
-    const float* p = base + s * (kD + 2);
-    if (p[kD + 1] > 0.f) m = fmaxf(m, p[kD]);
-  }
+  for (int s = 0; s < S_b; ++s)
+    if (pml[2 * s + 1] > 0.f) m = fmaxf(m, pml[2 * s]);
   float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
   float l = 0.f;
   if (m != -INFINITY) {
     for (int s = 0; s < S_b; ++s) {
-      const float* p = base + s * (kD + 2);
-      const float ls = p[kD + 1];
+      const float ls = pml[2 * s + 1];
       if (!(ls > 0.f)) continue;
-      const float f = ex2_approx(p[kD] - m);
-      const float4 v = *reinterpret_cast<const float4*>(p + 4 * lane);
+      const float f = ex2_approx(pml[2 * s] - m);
+      const float4 v = *reinterpret_cast<const float4*>(po + static_cast<size_t>(s) * kD + 4 * lane);
       o.x += f * v.x;
       o.y += f * v.y;
       o.z += f * v.z;
@@ -362,7 +361,9 @@ fa_status decode_launch(const void* q, const void* k_cache, const void* v_cache,
   a.q = static_cast<const __nv_bfloat16*>(q);
   a.block_table = block_table;
   a.seq_lens = seq_lens;
-  a.part = static_cast<float*>(workspace);
+  const size_t n_part = static_cast<size_t>(B) * Hq * num_splits;
+  a.part_o = static_cast<float*>(workspace);
+  a.part_ml = a.part_o + ((n_part * kD + 63) & ~static_cast<size_t>(63));
   a.o = static_cast<__nv_bfloat16*>(o);
   a.lse = lse;
   a.B = B;

@@ -104,8 +104,9 @@ int fa_bwd(const void* Q, const void* K, const void* V, const void* O, const voi
 
 /*
  * Bytes of device workspace fa_paged_decode needs for `num_splits` partial
- * (m, l, o) states per (batch, query head): fp32 [B, Hq, num_splits, d + 2],
- * rounded up to 256 bytes.  num_splits = 0 means the automatic choice (16).
+ * (m, l, o) states per (batch, query head): fp32 o [B, Hq, num_splits, d] and
+ * fp32 (m, l) [B, Hq, num_splits, 2], each rounded up to 256 bytes.
+ * num_splits = 0 means the automatic choice (16).
  */
 size_t fa_paged_decode_workspace_size(int B, int Hq, int d, int num_splits);
 

@@ -81,7 +81,8 @@ def test_decode_argument_validation(so):
     q, kc, vc, bt, sl, o, lse, ws = _fake(8)
     s = ctypes.c_void_p(0)
     need = so.fa_paged_decode_workspace_size(4, 32, 128, 0)
-    assert need == ((4 * 32 * 16 * 130 * 4 + 255) // 256) * 256
+    n = 4 * 32 * 16
+    assert need == ((n * 128 * 4 + 255) // 256) * 256 + ((n * 2 * 4 + 255) // 256) * 256
     assert so.fa_paged_decode_workspace_size(4, 32, 128, 17) == 0
     args = dict(B=4, Hq=32, Hkv=8, d=128, bs=16, mb=8, nb=32, S=0)
 
