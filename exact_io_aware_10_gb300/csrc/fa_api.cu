@@ -126,8 +126,9 @@ int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int
 
 size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
   if (B < 1 || H < 1 || N < 0 || d < 1) return 0;
-  const size_t rows = static_cast<size_t>(B) * H * N;
-  return round256(rows * sizeof(float)) + round256(rows * d * sizeof(float));
+  const size_t bh = static_cast<size_t>(B) * H;
+  const size_t npad = (static_cast<size_t>(N) + 127) / 128 * 128;
+  return 2 * round256(bh * npad * sizeof(float)) + round256(bh * N * d * sizeof(float));
 }
 
 int fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE, void* dQ,

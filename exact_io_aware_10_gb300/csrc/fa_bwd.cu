@@ -1,9 +1,554 @@
-// Backward attention (placeholder until the recomputation kernels land).
+// Backward attention by recomputation on sm_103a ("精读笔记 08：FlashAttention"
+// §3.3: keep O and the row statistics, rebuild the score tiles on chip; the
+// IO-explained page: "more FLOPs, fewer HBM accesses").  With P recomputed as
+// P = exp(scale Q K^T - LSE), the gradients of sum(dO * O) are
+//     dV = P^T dO,  dP = dO V^T,  D = rowsum(dO * O),  dS = P * (dP - D),
+//     dK = scale dS^T Q,  dQ = scale dS K.
+//
+// Three launches on one stream:
+//  1. bwd_pre_kernel   D_i = sum_c dO_ic O_ic and LSE_i * log2(e) into padded
+//                      fp32 rows (+inf / 0 past N), and dQacc <- 0.
+//  2. bwd_main_kernel  one CTA per (batch*head, 128-key tile j).  K_j and V_j
+//                      stay in shared memory; the CTA streams the query tiles
+//                      i that see tile j and, per tile, runs five tcgen05 MMAs
+//                      with fp32 accumulators in TMEM:
+//                        S^T = K_j Q_i^T          (TMEM cols   0..127)
+//                        dP^T = V_j dO_i^T        (TMEM cols 128..255)
+//                        dV_j += P^T dO_i         (TMEM cols 256..256+d)
+//                        dK_j += dS^T Q_i         (TMEM cols 256+d..256+2d)
+//                        dQ_i  = dS K_j           (TMEM cols   0..d, reusing S^T)
+//                      P^T and dS^T (bf16) go through one shared-memory tile;
+//                      dQ_i is added into the fp32 accumulator with vector
+//                      reductions (red.global.add.v4.f32).
+//  3. bwd_dq_kernel    dQ = bf16(dQacc).
+//
+// Roles of the main kernel (10 warps): warps 0-7 compute (thread = key row of
+// S^T / dP^T / dK / dV and query row of dQ; warps 0-3 take the first half of
+// the columns, 4-7 the second), warp 8 loads (TMA), warp 9 issues the MMAs.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+
 #include "fa_internal.h"
+#include "sm103.cuh"
 
 namespace fa {
-fa_status bwd_launch(const void*, const void*, const void*, const void*, const void*, const float*, void*, void*, void*,
-                     int, int, int, int, int, float, const int32_t*, void*, cudaStream_t) {
+namespace {
+
+constexpr int kThreads = 320;
+constexpr int kTile = 128;  // keys per CTA and queries per step
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct BwdCfg {
+  static constexpr int kSub = D / 64;
+  static constexpr int kSubBytes = kTile * 128;
+  static constexpr int kTileBytes = kTile * D * 2;
+  static constexpr int kPBytes = kTile * kTile * 2;
+  static constexpr int kSlots = 3;  // Q / dO ring
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kOffK + kTileBytes;
+  static constexpr int kOffP = kOffV + kTileBytes;  // P^T, then dS^T
+  static constexpr int kOffRing = kOffP + kPBytes;
+  static constexpr int kOffSide = kOffRing + kSlots * kTileBytes;  // 2 x (LSE2[128], D[128])
+  static constexpr int kOffBar = kOffSide + 2 * 1024;
+  static constexpr int kSmemBytes = kOffBar + 256 + 1024;
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D, kColDQ = 0;
+};
+
+enum : int {
+  BAR_KV = 0,
+  BAR_RING_FULL = 1,   // + slot (3)
+  BAR_RING_EMPTY = 4,  // + slot (3)
+  BAR_SIDE_FULL = 7,   // + 2
+  BAR_SIDE_EMPTY = 9,  // + 2
+  BAR_SDP = 11,
+  BAR_P = 12,
+  BAR_DV = 13,
+  BAR_DS = 14,
+  BAR_DQ_FULL = 15,
+  BAR_DQ_READ = 16,
+  BAR_FINAL = 17,
+  BAR_DRAIN = 18,
+  kNumBars = 19,
+};
+constexpr int kOffTmemSlot = kNumBars * 8;
+constexpr int kOffAbort = kOffTmemSlot + 4;
+constexpr int kComputeWarps = 8;
+
+struct BwdArgs {
+  float* Dpad;      // [BH, Npad]
+  float* Lpad;      // [BH, Npad] LSE * log2(e), +inf past N
+  float* dQacc;     // [BH, N, D] fp32
+  void* dK;         // [BH, N, D] bf16
+  void* dV;
+  const int32_t* kv_lens;
+  int H, N, Npad, nq;
+  int causal;
+  float scale;
+  float scale_log2;
+  unsigned* status;
+};
+
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  const unsigned long long t0 = global_timer_ns();
+  while (!mbar_test(bar, parity)) {
+    if (global_timer_ns() - t0 > 50000000ull) break;
+  }
+}
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
+// --------------------------------------------------------------------------- 1. preprocess
+// One warp per row: D = rowsum(dO * O) in fp32, LSE in log2 units, dQacc row = 0.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ O,
+                                                      const __nv_bfloat16* __restrict__ dO,
+                                                      const float* __restrict__ LSE, BwdArgs a, int BH) {
+  const long long gw = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const long long rows = static_cast<long long>(BH) * a.Npad;
+  if (gw >= rows) return;
+  const int bh = static_cast<int>(gw / a.Npad);
+  const int r = static_cast<int>(gw % a.Npad);
+  if (r >= a.N) {
+    if (lane == 0) {
+      a.Dpad[gw] = 0.f;
+      a.Lpad[gw] = INFINITY;
+    }
+    return;
+  }
+  const size_t row = static_cast<size_t>(bh) * a.N + r;
+  constexpr int kPer = D / 32;  // 2 or 4 elements per lane
+  float acc = 0.f;
+  if constexpr (kPer == 4) {
+    const uint2 o = *reinterpret_cast<const uint2*>(O + row * D + 4 * lane);
+    const uint2 g = *reinterpret_cast<const uint2*>(dO + row * D + 4 * lane);
+    const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&o);
+    const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const float2 of = __bfloat1622float2(o2[i]);
+      const float2 gf = __bfloat1622float2(g2[i]);
+      acc = fmaf(of.x, gf.x, acc);
+      acc = fmaf(of.y, gf.y, acc);
+    }
+    *reinterpret_cast<float4*>(a.dQacc + row * D + 4 * lane) = make_float4(0.f, 0.f, 0.f, 0.f);
+  } else {
+    const __nv_bfloat162 o = *reinterpret_cast<const __nv_bfloat162*>(O + row * D + 2 * lane);
+    const __nv_bfloat162 g = *reinterpret_cast<const __nv_bfloat162*>(dO + row * D + 2 * lane);
+    const float2 of = __bfloat1622float2(o), gf = __bfloat1622float2(g);
+    acc = fmaf(of.x, gf.x, of.y * gf.y);
+    *reinterpret_cast<float2*>(a.dQacc + row * D + 2 * lane) = make_float2(0.f, 0.f);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (lane == 0) {
+    a.Dpad[gw] = acc;
+    a.Lpad[gw] = LSE[row] * kLog2e;
+  }
+}
+
+// --------------------------------------------------------------------------- 3. dQ convert
+__global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ dQacc, __nv_bfloat16* __restrict__ dQ,
+                                                     long long n4) {
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n4) return;
+  const float4 v = reinterpret_cast<const float4*>(dQacc)[i];
+  uint2 w;
+  w.x = pack_bf16x2(v.x, v.y);
+  w.y = pack_bf16x2(v.z, v.w);
+  reinterpret_cast<uint2*>(dQ)[i] = w;
+}
+
+// --------------------------------------------------------------------------- 2. main
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                    const BwdArgs a) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t barbase = sbase + C::kOffBar;
+  auto bar = [&](int i) -> uint32_t { return barbase + 8u * static_cast<uint32_t>(i); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffBar + kOffTmemSlot);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffBar + kOffAbort);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int bh = blockIdx.x;
+  const int b = bh / a.H;
+  const int j = gridDim.y - 1 - blockIdx.y;  // key tile; causal: most query tiles first
+  const int N = a.N;
+  int kv_len = N;
+  if (a.kv_lens != nullptr) kv_len = min(max(a.kv_lens[b], 0), N);
+  const bool live = j * kTile < kv_len;  // any unmasked key in this tile
+  const int i0 = a.causal ? j : 0;
+  const int nt = live ? (a.nq - i0) : 0;  // query tiles to visit
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(BAR_KV), 1);
+    for (int s = 0; s < C::kSlots; ++s) {
+      mbar_init(bar(BAR_RING_FULL + s), 1);
+      mbar_init(bar(BAR_RING_EMPTY + s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(BAR_SIDE_FULL + s), 1);
+      mbar_init(bar(BAR_SIDE_EMPTY + s), kComputeWarps);
+    }
+    mbar_init(bar(BAR_SDP), 1);
+    mbar_init(bar(BAR_P), kComputeWarps);
+    mbar_init(bar(BAR_DV), 1);
+    mbar_init(bar(BAR_DS), kComputeWarps);
+    mbar_init(bar(BAR_DQ_FULL), 1);
+    mbar_init(bar(BAR_DQ_READ), kComputeWarps);
+    mbar_init(bar(BAR_FINAL), 1);
+    mbar_init(bar(BAR_DRAIN), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtx wc{abort_flag, a.status};
+  const size_t side_row = static_cast<size_t>(bh) * a.Npad;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && nt > 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmdO);
+      mbar_arrive_expect_tx(bar(BAR_KV), 2 * C::kTileBytes);
+      for (int s = 0; s < C::kSub; ++s) {
+        tma_load_3d(sbase + C::kOffK + s * C::kSubBytes, &tmK, bar(BAR_KV), s * 64, j * kTile, bh);
+        tma_load_3d(sbase + C::kOffV + s * C::kSubBytes, &tmV, bar(BAR_KV), s * 64, j * kTile, bh);
+      }
+      int issued = 0, side_issued = 0;
+      bool ok = true;
+      for (int it = 0; ok && it < nt; ++it) {
+        const int i = i0 + it;
+        const int sd = it & 1;
+        if (!mbar_wait(bar(BAR_SIDE_EMPTY + sd), ((it >> 1) & 1) ^ 1, wc)) break;
+        mbar_arrive_expect_tx(bar(BAR_SIDE_FULL + sd), 1024);
+        bulk_load(sbase + C::kOffSide + sd * 1024, a.Lpad + side_row + i * kTile, 512, bar(BAR_SIDE_FULL + sd));
+        bulk_load(sbase + C::kOffSide + sd * 1024 + 512, a.Dpad + side_row + i * kTile, 512,
+                  bar(BAR_SIDE_FULL + sd));
+        side_issued = it + 1;
+        for (int w = 0; w < 2; ++w) {  // Q_i then dO_i
+          const int u = 2 * it + w;
+          const int slot = u % C::kSlots;
+          if (!mbar_wait(bar(BAR_RING_EMPTY + slot), ((u / C::kSlots) & 1) ^ 1, wc)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar(BAR_RING_FULL + slot), C::kTileBytes);
+          const CUtensorMap* tm = w ? &tmdO : &tmQ;
+          for (int s = 0; s < C::kSub; ++s)
+            tma_load_3d(sbase + C::kOffRing + slot * C::kTileBytes + s * C::kSubBytes, tm, bar(BAR_RING_FULL + slot),
+                        s * 64, i * kTile, bh);
+          issued = u + 1;
+        }
+      }
+      drain_wait(bar(BAR_KV), 0);
+      for (int s = 0; s < C::kSlots && s < issued; ++s) {
+        const int u_last = s + C::kSlots * ((issued - 1 - s) / C::kSlots);
+        drain_wait(bar(BAR_RING_FULL + s), (u_last / C::kSlots) & 1);
+      }
+      for (int s = 0; s < 2 && s < side_issued; ++s) {
+        const int it_last = s + 2 * ((side_issued - 1 - s) / 2);
+        drain_wait(bar(BAR_SIDE_FULL + s), (it_last >> 1) & 1);
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && nt > 0) {
+      constexpr uint32_t idSS = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
+      constexpr uint32_t idKN = idesc_bf16_f32(128, D, false, true);     // dV, dK
+      constexpr uint32_t idNN = idesc_bf16_f32(128, D, true, true);      // dQ
+      const uint32_t sK = sbase + C::kOffK, sV = sbase + C::kOffV, sP = sbase + C::kOffP;
+      // A and B both K-major, K extent = D (head dim)
+      auto mma_kmajor_d = [&](uint32_t dcol, uint32_t a0, uint32_t b0) {
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * C::kSubBytes + (k & 3) * 32;
+          mma_ss(tmem + dcol, sdesc_sw128(a0 + off, 16, 1024), sdesc_sw128(b0 + off, 16, 1024), idSS, k > 0 ? 1u : 0u);
+        }
+      };
+      // A = P^T / dS^T (K-major over 128 queries), B MN-major (rows = queries)
+      auto mma_p_b = [&](uint32_t dcol, uint32_t b0, bool acc) {
+#pragma unroll
+        for (int k = 0; k < kTile / 16; ++k) {
+          const uint32_t aoff = (k >> 2) * C::kSubBytes + (k & 3) * 32;
+          mma_ss(tmem + dcol, sdesc_sw128(sP + aoff, 16, 1024), sdesc_sw128(b0 + k * 2048, C::kSubBytes, 1024), idKN,
+                 (acc || k > 0) ? 1u : 0u);
+        }
+      };
+      bool ok = mbar_wait(bar(BAR_KV), 0, wc);
+      for (int it = 0; ok && it < nt; ++it) {
+        const int uQ = 2 * it, uO = 2 * it + 1;
+        const int sQ = uQ % C::kSlots, sO = uO % C::kSlots;
+        const uint32_t aQ = sbase + C::kOffRing + sQ * C::kTileBytes;
+        const uint32_t aO = sbase + C::kOffRing + sO * C::kTileBytes;
+        // dP^T = V_j dO_i^T
+        if (!(ok = mbar_wait(bar(BAR_RING_FULL + sO), (uO / C::kSlots) & 1, wc))) break;
+        tc_fence_after();
+        mma_kmajor_d(C::kColDP, sV, aO);
+        // S^T = K_j Q_i^T  (its columns hold dQ_{i-1} until that has been read)
+        if (it > 0 && !(ok = mbar_wait(bar(BAR_DQ_READ), (it - 1) & 1, wc))) break;
+        if (!(ok = mbar_wait(bar(BAR_RING_FULL + sQ), (uQ / C::kSlots) & 1, wc))) break;
+        tc_fence_after();
+        mma_kmajor_d(C::kColS, sK, aQ);
+        mma_commit(bar(BAR_SDP));
+        // dV_j += P^T dO_i
+        if (!(ok = mbar_wait(bar(BAR_P), it & 1, wc))) break;
+        tc_fence_after();
+        mma_p_b(C::kColDV, aO, it > 0);
+        mma_commit(bar(BAR_DV));
+        mma_commit(bar(BAR_RING_EMPTY + sO));
+        // dK_j += dS^T Q_i ;  dQ_i = dS K_j
+        if (!(ok = mbar_wait(bar(BAR_DS), it & 1, wc))) break;
+        tc_fence_after();
+        mma_p_b(C::kColDK, aQ, it > 0);
+#pragma unroll
+        for (int k = 0; k < kTile / 16; ++k)
+          mma_ss(tmem + C::kColDQ, sdesc_sw128(sP + k * 2048, C::kSubBytes, 1024),
+                 sdesc_sw128(sK + k * 2048, C::kSubBytes, 1024), idNN, k > 0 ? 1u : 0u);
+        mma_commit(bar(BAR_DQ_FULL));
+        mma_commit(bar(BAR_RING_EMPTY + sQ));
+      }
+      if (ok) mma_commit(bar(BAR_FINAL));
+      mma_commit(bar(BAR_DRAIN));
+      drain_wait(bar(BAR_DRAIN), 0);
+    }
+  } else {
+    // ------------------------------------------------------------ compute warps
+    const int half = warp >> 2;  // column half
+    const int q4 = warp & 3;
+    const int r = q4 * 32 + lane;  // key row (S^T, dP^T, dK, dV) / query row (dQ)
+    const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
+    const int key = j * kTile + r;
+    const bool key_ok = key < kv_len;
+    const uint32_t prow = sbase + C::kOffP + half * C::kSubBytes + r * 128;
+    const int swz = r & 7;
+    const float sl2 = a.scale_log2;
+    bool aborted = false;
+    for (int it = 0; it < nt; ++it) {
+      const int i = i0 + it;
+      const int sd = it & 1;
+      if (!mbar_wait(bar(BAR_SIDE_FULL + sd), (it >> 1) & 1, wc) || !mbar_wait(bar(BAR_SDP), it & 1, wc)) {
+        aborted = true;
+        break;
+      }
+      tc_fence_after();
+      const float* lse2 = reinterpret_cast<const float*>(smem + C::kOffSide + sd * 1024) + half * 64;
+      const float* dsum = lse2 + 128;
+      // ---- P^T = exp2(S^T * scale * log2e - LSE2[q]) on this thread's 64 query columns
+      float p[64];
+      {
+        uint32_t rr[64];
+        tmem_ld64(tmem + lane_off + C::kColS + half * 64, rr);
+        // causal: key > query is masked; queries past N have LSE2 = +inf -> 0
+        const int qlo = i * kTile + half * 64;
+        const int first_vis = a.causal ? (key - qlo) : 0;  // columns c >= first_vis are visible
+#pragma unroll
+        for (int c = 0; c < 64; c += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c);
+          p[c + 0] = ex2_approx(fmaf(__uint_as_float(rr[c + 0]), sl2, -l4.x));
+          p[c + 1] = ex2_approx(fmaf(__uint_as_float(rr[c + 1]), sl2, -l4.y));
+          p[c + 2] = ex2_approx(fmaf(__uint_as_float(rr[c + 2]), sl2, -l4.z));
+          p[c + 3] = ex2_approx(fmaf(__uint_as_float(rr[c + 3]), sl2, -l4.w));
+        }
+        if (!key_ok || first_vis > 0) {
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            if (!key_ok || c < first_vis) p[c] = 0.f;
+        }
+      }
+#pragma unroll
+      for (int c8 = 0; c8 < 8; ++c8) {
+        st_shared_v4(prow + (((c8 ^ swz)) << 4), pack_bf16x2(p[8 * c8 + 0], p[8 * c8 + 1]),
+                     pack_bf16x2(p[8 * c8 + 2], p[8 * c8 + 3]), pack_bf16x2(p[8 * c8 + 4], p[8 * c8 + 5]),
+                     pack_bf16x2(p[8 * c8 + 6], p[8 * c8 + 7]));
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(BAR_P));
+      // ---- dS^T = scale * P^T * (dP^T - D[q])
+      {
+        uint32_t rr[64];
+        tmem_ld64(tmem + lane_off + C::kColDP + half * 64, rr);
+#pragma unroll
+        for (int c = 0; c < 64; c += 4) {
+          const float4 d4 = *reinterpret_cast<const float4*>(dsum + c);
+          p[c + 0] = a.scale * p[c + 0] * (__uint_as_float(rr[c + 0]) - d4.x);
+          p[c + 1] = a.scale * p[c + 1] * (__uint_as_float(rr[c + 1]) - d4.y);
+          p[c + 2] = a.scale * p[c + 2] * (__uint_as_float(rr[c + 2]) - d4.z);
+          p[c + 3] = a.scale * p[c + 3] * (__uint_as_float(rr[c + 3]) - d4.w);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(BAR_SIDE_EMPTY + sd));
+      if (!mbar_wait(bar(BAR_DV), it & 1, wc)) {  // P^T no longer read by the dV MMA
+        aborted = true;
+        break;
+      }
+#pragma unroll
+      for (int c8 = 0; c8 < 8; ++c8) {
+        st_shared_v4(prow + (((c8 ^ swz)) << 4), pack_bf16x2(p[8 * c8 + 0], p[8 * c8 + 1]),
+                     pack_bf16x2(p[8 * c8 + 2], p[8 * c8 + 3]), pack_bf16x2(p[8 * c8 + 4], p[8 * c8 + 5]),
+                     pack_bf16x2(p[8 * c8 + 6], p[8 * c8 + 7]));
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(BAR_DS));
+      // ---- dQ_i rows (thread = query row r) += this tile's dS K_j
+      if (!mbar_wait(bar(BAR_DQ_FULL), it & 1, wc)) {
+        aborted = true;
+        break;
+      }
+      tc_fence_after();
+      {
+        const int qrow = i * kTile + r;
+        float* dst = a.dQacc + (static_cast<size_t>(bh) * N + qrow) * D + half * (D / 2);
+#pragma unroll
+        for (int c0 = 0; c0 < D / 2; c0 += 32) {
+          uint32_t rr[32];
+          tmem_ld32(tmem + lane_off + C::kColDQ + half * (D / 2) + c0, rr);
+          if (qrow < N) {
+#pragma unroll
+            for (int c = 0; c < 32; c += 4)
+              red_add_v4(dst + c0 + c, __uint_as_float(rr[c]), __uint_as_float(rr[c + 1]), __uint_as_float(rr[c + 2]),
+                         __uint_as_float(rr[c + 3]));
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(BAR_DQ_READ));
+    }
+    // ---- epilogue: dV_j, dK_j rows (thread = key row r), this warp's column half
+    if (!aborted) {
+      const bool have = nt > 0;
+      if (have && !mbar_wait(bar(BAR_FINAL), 0, wc)) aborted = true;
+      if (!aborted) {
+        tc_fence_after();
+        const bool in_range = key < N;
+        const size_t rowoff = (static_cast<size_t>(bh) * N + key) * D + half * (D / 2);
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {
+          uint8_t* out = static_cast<uint8_t*>(which ? a.dK : a.dV) + rowoff * 2;
+          const uint32_t col = (which ? C::kColDK : C::kColDV) + half * (D / 2);
+#pragma unroll
+          for (int c0 = 0; c0 < D / 2; c0 += 32) {
+            uint32_t rr[32];
+            if (have) {
+              tmem_ld32(tmem + lane_off + col + c0, rr);
+            } else {
+#pragma unroll
+              for (int c = 0; c < 32; ++c) rr[c] = 0u;
+            }
+            if (in_range) {
+              uint4* dst = reinterpret_cast<uint4*>(out + c0 * 2);
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                dst[q] = make_uint4(pack_bf16x2(__uint_as_float(rr[8 * q + 0]), __uint_as_float(rr[8 * q + 1])),
+                                    pack_bf16x2(__uint_as_float(rr[8 * q + 2]), __uint_as_float(rr[8 * q + 3])),
+                                    pack_bf16x2(__uint_as_float(rr[8 * q + 4]), __uint_as_float(rr[8 * q + 5])),
+                                    pack_bf16x2(__uint_as_float(rr[8 * q + 6]), __uint_as_float(rr[8 * q + 7])));
+            }
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int D>
+fa_status bwd_launch_d(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
+                       void* dQ, void* dK, void* dV, int B, int H, int N, int causal, float scale,
+                       const int32_t* kv_lens, void* workspace, cudaStream_t stream) {
+  using C = BwdCfg<D>;
+  const int BH = B * H;
+  const int nq = ceil_div(N, kTile);
+  const int Npad = nq * kTile;
+  const size_t side = (static_cast<size_t>(BH) * Npad * sizeof(float) + 255) & ~static_cast<size_t>(255);
+  BwdArgs a;
+  a.Dpad = static_cast<float*>(workspace);
+  a.Lpad = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + side);
+  a.dQacc = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + 2 * side);
+  a.dK = dK;
+  a.dV = dV;
+  a.kv_lens = kv_lens;
+  a.H = H;
+  a.N = N;
+  a.Npad = Npad;
+  a.nq = nq;
+  a.causal = causal ? 1 : 0;
+  a.scale = scale;
+  a.scale_log2 = scale * kLog2e;
+  a.status = device_status_ptr();
+  if (a.status == nullptr) return FA_ERR_CUDA;
+
+  const uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(N), static_cast<uint64_t>(BH)};
+  const uint64_t strides[2] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(N) * D * 2};
+  const uint32_t box[3] = {64, kTile, 1};
+  CUtensorMap tq, tk, tv, tdo;
+  if (!encode_bf16_tmap(&tq, Q, 3, dims, strides, box) || !encode_bf16_tmap(&tk, K, 3, dims, strides, box) ||
+      !encode_bf16_tmap(&tv, V, 3, dims, strides, box) || !encode_bf16_tmap(&tdo, dO, 3, dims, strides, box))
+    return FA_ERR_CUDA;
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
+        cudaSuccess)
+      return FA_ERR_CUDA;
+    attr_set = true;
+  }
+  const long long pre_rows = static_cast<long long>(BH) * Npad;
+  bwd_pre_kernel<D><<<static_cast<unsigned>((pre_rows + 7) / 8), 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), LSE, a, BH);
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+  bwd_main_kernel<D><<<dim3(BH, nq), kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, a);
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+  const long long n4 = static_cast<long long>(BH) * N * D / 4;
+  bwd_dq_kernel<<<static_cast<unsigned>((n4 + 255) / 256), 256, 0, stream>>>(a.dQacc,
+                                                                             static_cast<__nv_bfloat16*>(dQ), n4);
+  return launch_status();
+}
+
+}  // namespace
+
+fa_status bwd_launch(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
+                     void* dQ, void* dK, void* dV, int B, int H, int N, int d, int causal, float scale,
+                     const int32_t* kv_lens, void* workspace, cudaStream_t stream) {
+  if (d == 64) return bwd_launch_d<64>(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, causal, scale, kv_lens, workspace, stream);
+  if (d == 128) return bwd_launch_d<128>(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, causal, scale, kv_lens, workspace, stream);
   return FA_ERR_UNSUPPORTED;
 }
+
 }  // namespace fa

@@ -76,9 +76,10 @@ int fa_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* LSE, 
               int causal, float scale, const int32_t* kv_lens, void* stream);
 
 /*
- * Bytes of device workspace fa_bwd needs: an fp32 [B, H, N] row-dot buffer
- * D = rowsum(dO * O) and an fp32 [B, H, N, d] dQ accumulator, each rounded up
- * to 256 bytes.  0 on invalid sizes.
+ * Bytes of device workspace fa_bwd needs: two fp32 [B, H, Npad] row buffers
+ * (D = rowsum(dO * O) and LSE in log2 units; Npad = N rounded up to 128) and
+ * an fp32 [B, H, N, d] dQ accumulator, each rounded up to 256 bytes.
+ * 0 on invalid sizes.
  */
 size_t fa_bwd_workspace_size(int B, int H, int N, int d);
 

@@ -69,8 +69,8 @@ def test_backward_argument_validation(so):
     ptrs = _fake(10)
     s = ctypes.c_void_p(0)
     need = so.fa_bwd_workspace_size(2, 3, 100, 64)
-    rows = 2 * 3 * 100
-    assert need == ((rows * 4 + 255) // 256) * 256 + ((rows * 64 * 4 + 255) // 256) * 256
+    bh, npad = 2 * 3, 128
+    assert need == 2 * ((bh * npad * 4 + 255) // 256) * 256 + ((bh * 100 * 64 * 4 + 255) // 256) * 256
     assert so.fa_bwd_workspace_size(0, 1, 1, 64) == 0
     assert so.fa_bwd(*ptrs[:9], 2, 3, 100, 64, 0, 0.1, None, ptrs[9], need - 1, s) == fl.FA_ERR_INVALID_ARG
     assert so.fa_bwd(*ptrs[:9], 2, 3, 100, 64, 0, 0.1, None, None, need, s) == fl.FA_ERR_INVALID_ARG
