@@ -1,0 +1,439 @@
+#!/usr/bin/env python
+"""Benchmark of the exact IO-aware attention hot path on GB300.
+
+One step = one pass of the whole path over one batch of synthetic input:
+  1. forward   B=1, H=16, N=16384, d=128, causal          (fa_fwd)
+  2. backward  same tensors, by recomputation              (fa_bwd)
+  3. forward   B=1, H=16, N=65536, d=128, causal          (fa_fwd)
+  4. paged GQA decode: B=64, Hq=32, Hkv=8, d=128, L ~ U[512, 32768],
+     16-token blocks, random physical placement, 16 splits (fa_paged_decode)
+Metric: attention fwd/bwd TFLOP/s (steps 1-3, algorithmic FLOPs: 4 B H N^2 d
+halved for causal, backward 2.5x) and paged-decode HBM GB/s (step 4), each
+also as a fraction of the measured peaks.  `value` is the fwd/bwd TFLOP/s;
+the decode figure is in `decode`.  Inputs are seeded synthetic tensors drawn
+on the device; every per-kernel input is larger than the 129 MB L2.
+
+`--impl reference` times the fp64 CPU oracle on a bounded sample of the same
+workload instead (rank 0 only).  Under torchrun every rank runs an
+independent replica (the path has no exchange step); rank 0 prints one JSON
+line with the max-over-ranks timing.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+NCORES = len(os.sched_getaffinity(0))
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, str(NCORES))
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from exact_io_aware_10_gb300 import accounting as acc  # noqa: E402
+from exact_io_aware_10_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "attention fwd/bwd TFLOP/s (% of BF16 peak); paged-decode HBM GB/s (% of peak)"
+PREFILL = dict(B=1, H=16, d=128, N_fb=16384, N_f=65536)
+DECODE = dict(B=64, Hq=32, Hkv=8, d=128, L_lo=512, L_hi=32768, block=16, max_blocks=2048, splits=16)
+WORKLOAD = ("long-context causal prefill B1 H16 d128 (fwd+bwd N=16384, fwd N=65536) + paged GQA decode "
+            "B64 Hq32 Hkv8 d128 L~U[512,32768] block16 splits16")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# ncu dram bytes (read + write) per launch of the dominant kernel, with the
+# hash of the kernel source they were taken on (null once the source changes)
+TRAFFIC_RECORD = {"kernel": "fwd_kernel<128>", "source": "exact_io_aware_10_gb300/csrc/fa_fwd.cu",
+                  "sha256": None, "bytes_per_launch_N16384": None, "bytes_per_launch_N65536": None}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in FALLBACK_PEAKS}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of SM clock and throttle reasons."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.proc = None
+        self.device_index = device_index
+
+    def start(self):
+        try:
+            uuid = str(torch.cuda.get_device_properties(self.device_index).uuid)
+            sel = ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        except Exception:
+            sel = []
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", *sel, f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons, n = [], [], set(), 0
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            n += 1
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": n}
+
+
+# --------------------------------------------------------------------------- our arm
+class Workload:
+    """Device-resident inputs, outputs and workspaces of one step."""
+
+    def __init__(self, dev, seed=0):
+        from exact_io_aware_10_gb300 import lib
+
+        self.lib = lib
+        lib.load()
+        P = PREFILL
+        s4 = wl.config_seed(seed, 4)
+        shp = (P["B"], P["H"], P["N_fb"], P["d"])
+        self.Q, self.K, self.V, self.dO = (wl.device_normal_bf16(shp, s4 + i, dev) for i in range(4))
+        self.O = torch.empty_like(self.Q)
+        self.L = torch.empty(shp[:3], dtype=torch.float32, device=dev)
+        self.dQ, self.dK, self.dV = (torch.empty_like(self.Q) for _ in range(3))
+        self.ws_b = torch.empty(lib.fa_bwd_workspace_size(*shp), dtype=torch.uint8, device=dev)
+        shp64 = (P["B"], P["H"], P["N_f"], P["d"])
+        self.Q64, self.K64, self.V64 = (wl.device_normal_bf16(shp64, s4 + 10 + i, dev) for i in range(3))
+        self.O64 = torch.empty_like(self.Q64)
+        self.L64 = torch.empty(shp64[:3], dtype=torch.float32, device=dev)
+        D = DECODE
+        sl, table, NB, _ = wl.paged_layout(D["B"], D["L_lo"], D["L_hi"], D["block"], wl.config_seed(seed, 5),
+                                           D["max_blocks"])
+        self.seq_lens_host = sl
+        self.seq_lens = sl.to(dev)
+        self.table = table.to(dev)
+        cshape = (NB, D["block"], D["Hkv"], D["d"])
+        s5 = wl.config_seed(seed, 5)
+        self.q = wl.device_normal_bf16((D["B"], D["Hq"], D["d"]), s5 + 1, dev)
+        self.kc = wl.device_normal_bf16(cshape, s5 + 2, dev)
+        self.vc = wl.device_normal_bf16(cshape, s5 + 3, dev)
+        self.o = torch.empty_like(self.q)
+        self.lse = torch.empty((D["B"], D["Hq"]), dtype=torch.float32, device=dev)
+        self.ws_d = torch.empty(lib.fa_paged_decode_workspace_size(D["B"], D["Hq"], D["d"], D["splits"]),
+                                dtype=torch.uint8, device=dev)
+
+    # the four parts of a step, each a single C-ABI call on the current stream
+    def fwd16(self):
+        self.lib.fa_fwd(self.Q, self.K, self.V, causal=True, O=self.O, LSE=self.L)
+
+    def bwd16(self):
+        self.lib.fa_bwd(self.Q, self.K, self.V, self.O, self.dO, self.L, causal=True, dQ=self.dQ, dK=self.dK,
+                        dV=self.dV, workspace=self.ws_b)
+
+    def fwd64(self):
+        self.lib.fa_fwd(self.Q64, self.K64, self.V64, causal=True, O=self.O64, LSE=self.L64)
+
+    def decode(self):
+        self.lib.fa_paged_decode(self.q, self.kc, self.vc, self.table, self.seq_lens, num_splits=DECODE["splits"],
+                                 o=self.o, lse=self.lse, workspace=self.ws_d)
+
+    PARTS = ("fwd16", "bwd16", "fwd64", "decode")
+    LAUNCHES = {"fwd16": 1, "bwd16": 3, "fwd64": 1, "decode": 2}
+
+    def flops(self):
+        P = PREFILL
+        f16 = acc.fwd_flops(P["B"], P["H"], P["N_fb"], P["d"], True)
+        return {"fwd16": f16, "bwd16": acc.bwd_flops(P["B"], P["H"], P["N_fb"], P["d"], True),
+                "fwd64": acc.fwd_flops(P["B"], P["H"], P["N_f"], P["d"], True)}
+
+    def decode_bytes(self):
+        D = DECODE
+        return acc.decode_bytes(self.seq_lens_host.tolist(), D["Hq"], D["Hkv"], D["d"], D["block"])
+
+
+class HostBuffers:
+    """Pinned host copies of a step's inputs and outputs for the end-to-end run."""
+
+    def __init__(self, w: Workload):
+        self.w = w
+        self.inputs = {"fwd16": [w.Q, w.K, w.V], "bwd16": [w.dO], "fwd64": [w.Q64, w.K64, w.V64],
+                       "decode": [w.q, w.kc, w.vc, w.table, w.seq_lens]}
+        self.outputs = {"fwd16": [w.O, w.L], "bwd16": [w.dQ, w.dK, w.dV], "fwd64": [w.O64, w.L64],
+                        "decode": [w.o, w.lse]}
+        self.h_in = {k: [t.cpu().pin_memory() for t in v] for k, v in self.inputs.items()}
+        self.h_out = {k: [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in v]
+                      for k, v in self.outputs.items()}
+
+    def bytes(self, part):
+        h2d = sum(t.numel() * t.element_size() for t in self.h_in[part])
+        d2h = sum(t.numel() * t.element_size() for t in self.h_out[part])
+        return h2d, d2h
+
+    def run(self, part):
+        for d, h in zip(self.inputs[part], self.h_in[part]):
+            d.copy_(h, non_blocking=True)
+        getattr(self.w, part)()
+        for h, d in zip(self.h_out[part], self.outputs[part]):
+            h.copy_(d, non_blocking=True)
+
+
+def source_sha(rel):
+    with open(os.path.join(ROOT, rel), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def time_parts(fn_for_part, parts, steps, warmup, barrier):
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        for p in parts:
+            fn_for_part(p)
+    torch.cuda.synchronize()
+    barrier()
+    ev = {p: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+          for p in parts}
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for k in range(steps):
+        for p in parts:
+            ev[p][k][0].record(stream)
+            fn_for_part(p)
+            ev[p][k][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    per_part = {p: sum(a.elapsed_time(b) for a, b in ev[p]) for p in parts}  # ms over all steps
+    return t0.elapsed_time(t1), per_part
+
+
+def run_ours(args):
+    rank, world, local = dist_env()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    def max_over_ranks(x):
+        if dist is None:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    w = Workload(dev, seed=args.seed)
+    peaks, peak_src = load_peaks()
+    flops = w.flops()
+    dbytes = w.decode_bytes()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    total_ms, part_ms = time_parts(lambda p: getattr(w, p)(), Workload.PARTS, args.steps, args.warmup, barrier)
+    clocks = sampler.stop()
+    assert w.lib.fa_get_device_status() == w.lib.FA_OK, "device status word reported an error"
+    total_ms = max_over_ranks(total_ms)
+    part_ms = {p: max_over_ranks(v) for p, v in part_ms.items()}
+
+    K = args.steps
+    prefill_parts = ("fwd16", "bwd16", "fwd64")
+    prefill_ms = sum(part_ms[p] for p in prefill_parts)
+    prefill_flops = sum(flops.values())
+    value = world * K * prefill_flops / (prefill_ms * 1e-3) / 1e12
+    dec_gbs = world * K * dbytes / (part_ms["decode"] * 1e-3) / 1e9
+    peak_tf, peak_hbm = peaks["bf16_tflops"], peaks["hbm_gbs"]
+
+    def tf(p):
+        return K * flops[p] / (part_ms[p] * 1e-3) / 1e12
+
+    parts = {
+        "fwd_N16384": {"TFLOP/s": tf("fwd16"), "frac": tf("fwd16") / peak_tf, "ms": part_ms["fwd16"] / K},
+        "bwd_N16384": {"TFLOP/s": tf("bwd16"), "frac": tf("bwd16") / peak_tf, "ms": part_ms["bwd16"] / K},
+        "fwd_N65536": {"TFLOP/s": tf("fwd64"), "frac": tf("fwd64") / peak_tf, "ms": part_ms["fwd64"] / K},
+        "decode": {"GB/s": dec_gbs / world, "frac": dec_gbs / world / peak_hbm, "ms": part_ms["decode"] / K},
+    }
+
+    # roofline of the dominant kernel: the forward kernel (one launch per fa_fwd call)
+    fwd_ms = part_ms["fwd16"] + part_ms["fwd64"]
+    fwd_flops_step = flops["fwd16"] + flops["fwd64"]
+    achieved = K * fwd_flops_step / (fwd_ms * 1e-3) / 1e12
+    traffic = None
+    rec = TRAFFIC_RECORD
+    if rec["sha256"] and rec["sha256"] == source_sha(rec["source"]) and rec["bytes_per_launch_N65536"]:
+        traffic = (rec["bytes_per_launch_N16384"] + rec["bytes_per_launch_N65536"]) / 2.0
+    roofline = {"kernel": "fwd_kernel<128> (fa_fwd)", "bound": "tensor", "achieved": achieved, "peak": peak_tf,
+                "unit": "TFLOP/s", "frac": achieved / peak_tf, "traffic": traffic,
+                "peak_source": f"{peak_src} bf16_tflops (burst)",
+                "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
+                "launches_per_step": 2, "flops_per_step": fwd_flops_step}
+
+    # end to end: the same parts through the C ABI with pinned host buffers,
+    # host->device inputs and device->host outputs inside the timed region
+    hb = HostBuffers(w)
+    e2e_steps = max(3, min(args.steps, 10))
+    e2e_total, e2e_part = time_parts(hb.run, Workload.PARTS, e2e_steps, 1, barrier)
+    e2e_part = {p: max_over_ranks(v) for p, v in e2e_part.items()}
+    e2e_prefill_ms = sum(e2e_part[p] for p in prefill_parts)
+    e2e_value = world * e2e_steps * prefill_flops / (e2e_prefill_ms * 1e-3) / 1e12
+    h2d = sum(hb.bytes(p)[0] for p in Workload.PARTS)
+    d2h = sum(hb.bytes(p)[1] for p in Workload.PARTS)
+    e2e = {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "decode_GB/s": world * e2e_steps * dbytes / (e2e_part["decode"] * 1e-3) / 1e9,
+           "ms_per_step": max_over_ranks(e2e_total) / e2e_steps}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_sample(args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+            "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "parallelism": f"replicas{world}",
+                       "l2": "every kernel's inputs exceed the 129 MB L2 (no flush needed)",
+                       "value_is": "fwd+bwd TFLOP/s over parts 1-3; decode GB/s in 'decode'"},
+            "decode": {"value": dec_gbs, "unit": "GB/s", "frac": dec_gbs / world / peak_hbm,
+                       "peak": peak_hbm, "peak_source": f"{peak_src} hbm_gbs", "bytes_per_step": dbytes},
+            "parts": parts, "roofline": roofline, "e2e": e2e, "cpu_baseline": cpu,
+            "gpu_launches": K * sum(Workload.LAUNCHES.values()), "clocks": clocks,
+        }
+        print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+# --------------------------------------------------------------------------- oracle (CPU)
+def _oracle_prefill_sample(seed, head, n_prefix):
+    """Oracle forward + backward of one head of the long-prefill workload,
+    restricted to its first ``n_prefix`` positions (a causal prefix is itself a
+    causal attention problem).  Returns (seconds, algorithmic FLOPs)."""
+    import oracle
+
+    P = PREFILL
+    g = torch.Generator().manual_seed(wl.config_seed(seed, 4) * 31 + head)
+    shp = (1, 1, n_prefix, P["d"])
+    Q, K, V, dO = (torch.randn(*shp, generator=g).to(torch.bfloat16) for _ in range(4))
+    t0 = time.perf_counter()
+    oracle.attention_forward(Q, K, V, causal=True)
+    oracle.attention_backward(Q, K, V, dO, causal=True)
+    dt = time.perf_counter() - t0
+    return dt, acc.fwd_flops(1, 1, n_prefix, P["d"], True) + acc.bwd_flops(1, 1, n_prefix, P["d"], True)
+
+
+def _oracle_decode_sample(seed, n_seq):
+    import oracle
+
+    D = DECODE
+    sl, _, _, g = wl.paged_layout(D["B"], D["L_lo"], D["L_hi"], D["block"], wl.config_seed(seed, 5), D["max_blocks"])
+    lens = sl[:n_seq].tolist()
+    P = wl.paged_inputs(n_seq, D["Hq"], D["Hkv"], D["d"], 0, 0, D["block"], seed=seed + 77, seq_lens=lens)
+    t0 = time.perf_counter()
+    oracle.paged_decode(P.q, P.k_cache, P.v_cache, P.block_table, P.seq_lens, D["block"])
+    dt = time.perf_counter() - t0
+    return dt, acc.decode_bytes(lens, D["Hq"], D["Hkv"], D["d"], D["block"])
+
+
+def cpu_baseline_sample(budget_s=15.0, seed=0):
+    """The oracle as it stands, timed on this host's cores on bounded samples."""
+    t_start = time.perf_counter()
+    secs, fl, heads = 0.0, 0.0, 0
+    while heads < 16 and (time.perf_counter() - t_start) < budget_s * 0.7:
+        dt, f = _oracle_prefill_sample(seed, heads, 4096)
+        secs += dt
+        fl += f
+        heads += 1
+    d_dt, d_bytes = _oracle_decode_sample(seed, 2)
+    return {"value": fl / secs / 1e12, "unit": "TFLOP/s", "cores": NCORES, "kind": "oracle",
+            "sample": f"fp64 numpy oracle fwd+bwd on {heads} head(s) of the long-prefill workload, causal prefix "
+                      f"N=4096, d=128 ({secs:.1f} s); decode GB/s on 2 sequences of the decode workload",
+            "decode_GB/s": d_bytes / d_dt / 1e9}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    fl_tot, t_tot = 0.0, 0.0
+    for k in range(args.warmup + args.steps):
+        dt, f = _oracle_prefill_sample(args.seed, k % PREFILL["H"], args.ref_prefix)
+        if k >= args.warmup:
+            fl_tot += f
+            t_tot += dt
+    value = fl_tot / t_tot / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * t_tot / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+        "config": {"workload": WORKLOAD, "sample": f"one head per step, causal prefix N={args.ref_prefix}",
+                   "parallelism": "cpu"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": NCORES, "kind": "oracle",
+                         "sample": f"fp64 numpy oracle fwd+bwd, one head of the long-prefill workload per step, "
+                                   f"causal prefix N={args.ref_prefix}, d=128"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=40)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-prefix", type=int, default=2048)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,44 @@
+"""Algorithmic FLOP and byte counts used for throughput and roofline figures.
+
+Conventions (matmul work only; exp, masking and reductions are not counted):
+  forward   4 * B * H * N^2 * d     (QK^T and PV, 2 N^2 d each), halved when causal
+  backward  2.5 x the forward       (five N^2 d products instead of two)
+  key padding: the effective forward count is 4 * H * N * d * sum_b L_b
+  decode    bytes = K and V of every visible key, read once per KV head
+            (sum_b L_b * Hkv * d * 2 B * 2) + q + o + lse + the block-table
+            entries and sequence lengths read.
+Compulsory forward bytes are Q, K, V, O (2 B each) + LSE (4 B).
+"""
+from __future__ import annotations
+
+
+def fwd_flops(B, H, N, d, causal=False):
+    f = 4.0 * B * H * N * N * d
+    return f * 0.5 if causal else f
+
+
+def bwd_flops(B, H, N, d, causal=False):
+    return 2.5 * fwd_flops(B, H, N, d, causal)
+
+
+def fwd_flops_padded(H, N, d, kv_lens):
+    return 4.0 * H * N * d * float(sum(int(x) for x in kv_lens))
+
+
+def fwd_bytes(B, H, N, d):
+    return 8.0 * B * H * N * d + 4.0 * B * H * N
+
+
+def bwd_bytes(B, H, N, d):
+    # read Q, K, V, O, dO, LSE; write dQ, dK, dV (bf16) -- compulsory only
+    return 2.0 * B * H * N * d * 8 + 4.0 * B * H * N
+
+
+def decode_bytes(seq_lens, Hq, Hkv, d, block_size=16, with_lse=True):
+    L = [int(x) for x in seq_lens]
+    B = len(L)
+    kv = sum(L) * Hkv * d * 2.0 * 2
+    qo = 2.0 * B * Hq * d * 2
+    lse = 4.0 * B * Hq if with_lse else 0.0
+    table = 4.0 * sum((x + block_size - 1) // block_size for x in L) + 4.0 * B
+    return kv + qo + lse + table

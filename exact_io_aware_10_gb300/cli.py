@@ -1,0 +1,69 @@
+"""Run one attention entry point on seeded synthetic inputs, e.g. for a
+profiler:  python -m exact_io_aware_10_gb300.cli fwd --N 16384 --iters 2
+
+Subcommands: fwd, bwd (runs fwd once to produce O/LSE, then bwd), decode.
+Prints the CUDA-event time of the last iteration.
+"""
+from __future__ import annotations
+
+import argparse
+import os
+import sys
+
+import torch
+
+sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+
+from exact_io_aware_10_gb300 import lib  # noqa: E402
+from exact_io_aware_10_gb300 import workloads as wl  # noqa: E402
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("op", choices=["fwd", "bwd", "decode"])
+    ap.add_argument("--B", type=int, default=1)
+    ap.add_argument("--H", type=int, default=16)
+    ap.add_argument("--N", type=int, default=16384)
+    ap.add_argument("--d", type=int, default=128)
+    ap.add_argument("--noncausal", action="store_true")
+    ap.add_argument("--iters", type=int, default=2)
+    ap.add_argument("--Hq", type=int, default=32)
+    ap.add_argument("--Hkv", type=int, default=8)
+    ap.add_argument("--L-lo", type=int, default=512)
+    ap.add_argument("--L-hi", type=int, default=32768)
+    ap.add_argument("--splits", type=int, default=16)
+    ap.add_argument("--seed", type=int, default=0)
+    a = ap.parse_args(argv)
+    dev = torch.device("cuda")
+    lib.load()
+    causal = not a.noncausal
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if a.op in ("fwd", "bwd"):
+        shp = (a.B, a.H, a.N, a.d)
+        Q, K, V, dO = (wl.device_normal_bf16(shp, a.seed + i, dev) for i in range(4))
+        O, L = lib.fa_fwd(Q, K, V, causal=causal)
+        for _ in range(a.iters):
+            start.record()
+            if a.op == "fwd":
+                lib.fa_fwd(Q, K, V, causal=causal, O=O, LSE=L)
+            else:
+                lib.fa_bwd(Q, K, V, O, dO, L, causal=causal)
+            end.record()
+    else:
+        sl, table, NB, _ = wl.paged_layout(a.B, a.L_lo, a.L_hi, 16, a.seed, None)
+        q = wl.device_normal_bf16((a.B, a.Hq, a.d), a.seed + 1, dev)
+        kc = wl.device_normal_bf16((NB, 16, a.Hkv, a.d), a.seed + 2, dev)
+        vc = wl.device_normal_bf16((NB, 16, a.Hkv, a.d), a.seed + 3, dev)
+        sl, table = sl.to(dev), table.to(dev)
+        for _ in range(a.iters):
+            start.record()
+            lib.fa_paged_decode(q, kc, vc, table, sl, num_splits=a.splits)
+            end.record()
+    torch.cuda.synchronize()
+    st = lib.fa_get_device_status()
+    print(f"{a.op}: {start.elapsed_time(end):.3f} ms (last iteration), status {lib.status_string(st)}")
+    return 0 if st == lib.FA_OK else 1
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -34,6 +34,8 @@ __all__ = [
     "padded_lengths",
     "boosted_inputs",
     "paged_inputs",
+    "paged_layout",
+    "device_normal_bf16",
     "config_seed",
 ]
 
@@ -121,14 +123,16 @@ class PagedInputs:
         return int(self.block_table.shape[1])
 
 
-def paged_inputs(B, Hq, Hkv, d, L_lo, L_hi, block_size=16, seed=0, max_blocks=None,
-                 seq_lens=None, std=1.0, spare_blocks=0) -> PagedInputs:
-    """Paged decode inputs.
+def paged_layout(B, L_lo, L_hi, block_size=16, seed=0, max_blocks=None, seq_lens=None, spare_blocks=0,
+                 g=None):
+    """Context lengths and block table of a paged KV cache (CPU int32).
 
-    Physical block ids are a seeded random permutation of [0, NB) where
-    NB = sum_b ceil(L_b / block_size) (+ ``spare_blocks`` never referenced).
+    L_b ~ U{L_lo..L_hi} unless ``seq_lens`` is given; physical block ids are a
+    seeded random permutation of [0, NB), NB = sum_b ceil(L_b / block_size)
+    (+ ``spare_blocks`` never referenced); entries past a row's blocks are -1.
+    Returns (seq_lens, block_table, NB, generator).
     """
-    g = _gen(seed)
+    g = _gen(seed) if g is None else g
     if seq_lens is None:
         seq_lens = torch.randint(L_lo, L_hi + 1, (B,), generator=g, dtype=torch.int64)
     seq_lens = torch.as_tensor(seq_lens, dtype=torch.int64).reshape(-1)
@@ -143,7 +147,27 @@ def paged_inputs(B, Hq, Hkv, d, L_lo, L_hi, block_size=16, seed=0, max_blocks=No
     for b, n in enumerate(nblk):
         table[b, :n] = perm[pos:pos + n]
         pos += n
+    return seq_lens.to(torch.int32), table, NB, g
+
+
+def paged_inputs(B, Hq, Hkv, d, L_lo, L_hi, block_size=16, seed=0, max_blocks=None,
+                 seq_lens=None, std=1.0, spare_blocks=0) -> PagedInputs:
+    """Paged decode inputs on the CPU (layout from ``paged_layout``; q and the
+    K/V caches ~ N(0, std^2) in bf16)."""
+    seq_lens, table, NB, g = paged_layout(B, L_lo, L_hi, block_size, seed, max_blocks, seq_lens, spare_blocks)
+    B = int(seq_lens.numel())
     q = _normal_bf16((B, Hq, d), g, std)
     k_cache = _normal_bf16((max(NB, 1), block_size, Hkv, d), g, std)
     v_cache = _normal_bf16((max(NB, 1), block_size, Hkv, d), g, std)
-    return PagedInputs(q, k_cache, v_cache, table, seq_lens.to(torch.int32), block_size)
+    return PagedInputs(q, k_cache, v_cache, table, seq_lens, block_size)
+
+
+def device_normal_bf16(shape, seed, device, std=1.0):
+    """N(0, std^2) bf16 tensor drawn on the device with a seeded generator
+    (benchmark-sized inputs that would be slow to draw on the host)."""
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    x = torch.randn(*shape, generator=g, device=device, dtype=torch.float32)
+    if std != 1.0:
+        x.mul_(std)
+    return x.to(torch.bfloat16)
