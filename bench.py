@@ -52,7 +52,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # ncu dram bytes (read + write) per launch of the dominant kernel, with the
 # hash of the kernel source they were taken on (null once the source changes)
 TRAFFIC_RECORD = {"kernel": "fwd_kernel<128>", "source": "exact_io_aware_10_gb300/csrc/fa_fwd.cu",
-                  "sha256": None, "bytes_per_launch_N16384": None, "bytes_per_launch_N65536": None}
+                  "sha256": "931fd1edebd5850635034c29d844fcad7d0ea307b9c17336c0f86681ab749ba9",
+                  "bytes_per_launch_N16384": 554.180096e6 + 60.245248e6, "bytes_per_launch_N65536": None}
 
 
 def load_peaks():
@@ -300,8 +301,12 @@ def run_ours(args):
     achieved = K * fwd_flops_step / (fwd_ms * 1e-3) / 1e12
     traffic = None
     rec = TRAFFIC_RECORD
-    if rec["sha256"] and rec["sha256"] == source_sha(rec["source"]) and rec["bytes_per_launch_N65536"]:
-        traffic = (rec["bytes_per_launch_N16384"] + rec["bytes_per_launch_N65536"]) / 2.0
+    if rec["sha256"] and rec["sha256"] == source_sha(rec["source"]):
+        per = [rec[k] for k in ("bytes_per_launch_N16384", "bytes_per_launch_N65536") if rec[k]]
+        if len(per) == 2:
+            traffic = sum(per) / 2.0
+        elif per:
+            traffic = {"N16384_only": per[0]}
     roofline = {"kernel": "fwd_kernel<128> (fa_fwd)", "bound": "tensor", "achieved": achieved, "peak": peak_tf,
                 "unit": "TFLOP/s", "frac": achieved / peak_tf, "traffic": traffic,
                 "peak_source": f"{peak_src} bf16_tflops (burst)",
