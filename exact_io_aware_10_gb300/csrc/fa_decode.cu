@@ -21,6 +21,8 @@
 #include <cuda_runtime.h>
 #include <math.h>
 
+#include <mutex>
+
 #include "fa_internal.h"
 #include "sm103.cuh"
 
@@ -383,3 +385,69 @@ fa_status decode_launch(const void* q, const void* k_cache, const void* v_cache,
 }
 
 }  // namespace fa
+
+// ---------------------------------------------------------------------------
+// Paged decode without a caller workspace.
+//
+// Some callers cannot call cudaMalloc at the point where they decode: an
+// inference-engine plugin whose device memory is handed out by the engine at
+// build time and which may not allocate while enqueuing work, or a serving
+// loop that must not allocate because cudaMalloc/cudaFree can synchronise the
+// device and stall every other stream.  Such callers cannot pass the split
+// workspace fa_paged_decode needs, so this variant keeps the split partials in
+// a fixed file-scope device array.
+//
+// Capacity: B * Hq * num_splits <= kNoAllocMaxStates partial states at d = 128
+// (fp32 o [states, 128] followed by fp32 (m, l) [states, 2]: 16.25 MiB).  Every
+// device that loads the library holds one copy of the array until the process
+// exits.  All calls on a device share it and it keeps the last call's
+// contents; nothing in it needs to start at zero, because the split kernel
+// writes every partial state that the combine kernel later reads.  Calls that
+// overlap on the GPU (different streams, or different host threads without
+// ordering) race on the array.
+namespace fa {
+namespace {
+
+constexpr size_t kNoAllocMaxStates = 32768;
+static __device__ __align__(256) float g_decode_scratch[kNoAllocMaxStates * (kD + 2)];
+
+std::mutex g_scratch_mu;
+float* g_scratch_ptr[64] = {};
+
+// Device address of the scratch array on the current device, looked up once
+// per device (the host-side symbol is only a stand-in, not a device address).
+float* decode_scratch_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  if (g_scratch_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr) return nullptr;
+    g_scratch_ptr[dev] = static_cast<float*>(p);
+  }
+  return g_scratch_ptr[dev];
+}
+
+}  // namespace
+}  // namespace fa
+
+extern "C" int fa_paged_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                       const int32_t* block_table, const int32_t* seq_lens, void* o, float* lse, int B,
+                                       int Hq, int Hkv, int d, int block_size, int max_blocks, int num_blocks,
+                                       int num_splits, float scale, void* stream) {
+  auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  if (B < 1 || Hq < 1 || Hkv < 1 || max_blocks < 1 || num_blocks < 1 || num_splits < 0) return FA_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !isfinite(scale)) return FA_ERR_INVALID_ARG;
+  if (d != fa::kD || block_size != fa::kBlk) return FA_ERR_UNSUPPORTED;
+  if (Hq / Hkv > 16 || num_splits > 16) return FA_ERR_UNSUPPORTED;
+  if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !o) return FA_ERR_INVALID_ARG;
+  if (!al16(q) || !al16(k_cache) || !al16(v_cache) || !al16(o)) return FA_ERR_INVALID_ARG;
+  if (static_cast<long long>(num_blocks) * block_size > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  const int S = num_splits == 0 ? 16 : num_splits;
+  if (static_cast<size_t>(B) * Hq * S > fa::kNoAllocMaxStates) return FA_ERR_UNSUPPORTED;  // scratch too small
+  float* scratch = fa::decode_scratch_ptr();
+  if (scratch == nullptr) return FA_ERR_CUDA;
+  return fa::decode_launch(q, k_cache, v_cache, block_table, seq_lens, o, lse, B, Hq, Hkv, d, block_size, max_blocks,
+                           num_blocks, S, scale, scratch, static_cast<cudaStream_t>(stream));
+}

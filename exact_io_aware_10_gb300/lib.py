@@ -36,6 +36,7 @@ SIGNATURES = {
     "fa_paged_decode_workspace_size": (_sz, [_i, _i, _i, _i]),
     "fa_paged_decode": (_i, [_vp] * 7 + [_i] * 8 + [_f, _vp, _sz, _vp]),
     "fa_get_device_status": (_i, [_vp]),
+    "fa_paged_decode_noalloc": (_i, [_vp] * 7 + [_i] * 8 + [_f, _vp]),
 }
 
 _LIB = None
@@ -189,6 +190,37 @@ def fa_paged_decode(q, k_cache, v_cache, block_table, seq_lens, scale=None, num_
                              B, Hq, Hkv, d, bs, max_blocks, NB, int(num_splits), scale, _p(workspace),
                              workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st, "fa_paged_decode")
+    return o, lse
+
+
+def fa_paged_decode_noalloc(q, k_cache, v_cache, block_table, seq_lens, scale=None, num_splits=0, o=None, lse=None,
+                            stream=None, want_lse=True):
+    """fa_paged_decode for callers that cannot allocate device memory: the
+    split partials live in the library's fixed device array (at most
+    B * Hq * num_splits = 32768 states; calls that overlap on the GPU race).
+    Outputs are still passed in by the caller (``o``/``lse``); the ones left
+    as None are allocated here only as a convenience of this binding."""
+    lib = load()
+    B, Hq, d = q.shape
+    NB, bs, Hkv, d2 = k_cache.shape
+    _need(q, torch.bfloat16, None, "q")
+    _need(k_cache, torch.bfloat16, None, "k_cache")
+    _need(v_cache, torch.bfloat16, (NB, bs, Hkv, d2), "v_cache")
+    _need(block_table, torch.int32, None, "block_table")
+    _need(seq_lens, torch.int32, (B,), "seq_lens")
+    if block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("block_table must be [B, max_blocks]")
+    o = torch.empty_like(q) if o is None else o
+    _need(o, torch.bfloat16, (B, Hq, d), "o")
+    if want_lse and lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _need(lse, torch.float32, (B, Hq), "lse")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    st = lib.fa_paged_decode_noalloc(_p(q), _p(k_cache), _p(v_cache), _p(block_table), _p(seq_lens), _p(o), _p(lse),
+                                     B, Hq, Hkv, d, bs, int(block_table.shape[1]), NB, int(num_splits), scale,
+                                     _stream(stream))
+    _check(st, "fa_paged_decode_noalloc")
     return o, lse
 
 

@@ -138,6 +138,35 @@ int fa_paged_decode(const void* q, const void* k_cache, const void* v_cache, con
                     void* stream);
 
 /*
+ * fa_paged_decode without a caller workspace.  (The pages have no counterpart
+ * to this entry point; it exists for callers of this library.)
+ *
+ * Some callers cannot allocate device memory where they decode: an
+ * inference-engine plugin whose device memory is assigned by the engine ahead
+ * of time and which may not allocate while it enqueues work, or a serving loop
+ * that avoids cudaMalloc/cudaFree because they can synchronise the device.
+ * This entry point takes the same arguments as fa_paged_decode minus the
+ * workspace, and calls no allocating routine: the split partials live in a
+ * fixed device array inside the library.
+ *   Limit: B * Hq * num_splits (num_splits = 0 counts as 16) must be at most
+ *   32768, else FA_ERR_UNSUPPORTED is returned and nothing is launched.  The
+ *   array (16.25 MiB) is held on every device that loads the library until
+ *   the process exits.
+ *   The first call on a device looks up the array's device address (once per
+ *   device, with that device current); make that first call before any stream
+ *   capture.
+ *   All calls on a device share the array and it keeps the last call's
+ *   contents (nothing in it needs clearing between calls).  Calls that overlap
+ *   on the GPU -- on different streams, or from host threads without ordering
+ *   between them -- race on the array and give undefined results.
+ * Other errors as fa_paged_decode.
+ */
+int fa_paged_decode_noalloc(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                            const int32_t* seq_lens, void* o, float* lse, int B, int Hq, int Hkv, int d,
+                            int block_size, int max_blocks, int num_blocks, int num_splits, float scale,
+                            void* stream);
+
+/*
  * Synchronises `stream`, then returns and clears the device status word of
  * the current device: FA_OK, FA_ERR_TIMEOUT or FA_ERR_BAD_BLOCK_TABLE (the
  * first two bits latched since the last call, timeout first), or FA_ERR_CUDA.
