@@ -70,6 +70,21 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
+def reduce_max(x, dist=None, device="cpu"):
+    """Max of a per-rank float over all ranks (identity without a process group)."""
+    if dist is None:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank, world, seconds):
+    """Replicas: every rank does the same units; the job's rate is all ranks'
+    units over the slowest rank's time."""
+    return world * units_per_rank / seconds
+
+
 # --------------------------------------------------------------------------- clocks
 class ClockSampler:
     """nvidia-smi samples (200 ms) of SM clock and throttle reasons."""
@@ -258,11 +273,7 @@ def run_ours(args):
             dist.barrier()
 
     def max_over_ranks(x):
-        if dist is None:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return reduce_max(x, dist, dev)
 
     w = Workload(dev, seed=args.seed)
     peaks, peak_src = load_peaks()
@@ -281,8 +292,8 @@ def run_ours(args):
     prefill_parts = ("fwd16", "bwd16", "fwd64")
     prefill_ms = sum(part_ms[p] for p in prefill_parts)
     prefill_flops = sum(flops.values())
-    value = world * K * prefill_flops / (prefill_ms * 1e-3) / 1e12
-    dec_gbs = world * K * dbytes / (part_ms["decode"] * 1e-3) / 1e9
+    value = whole_job_rate(K * prefill_flops, world, prefill_ms * 1e-3) / 1e12
+    dec_gbs = whole_job_rate(K * dbytes, world, part_ms["decode"] * 1e-3) / 1e9
     peak_tf, peak_hbm = peaks["bf16_tflops"], peaks["hbm_gbs"]
 
     def tf(p):
