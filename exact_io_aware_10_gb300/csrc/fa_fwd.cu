@@ -1,17 +1,21 @@
 // Forward attention on sm_103a: one CTA owns two 128-row query tiles of one
 // (batch, head) and streams all visible 128-key K/V tiles through shared
 // memory, computing
-//     S = Q K^T      (tcgen05 MMA, fp32 accumulator in TMEM)
-//     online softmax (one thread per query row, registers only)
-//     O += P V       (tcgen05 MMA, fp32 accumulator in TMEM)
+//     S = Q K^T      (tcgen05 MMA, operands in shared memory, fp32 accumulator in TMEM)
+//     online softmax (one thread per query row, registers only); P is written
+//                    back as packed bf16 over the first 64 columns of its S tile
+//     O += P V       (tcgen05 MMA with A = P read from TMEM, B = V from shared memory)
 // so no score tile ever reaches device memory ("精读笔记 08：FlashAttention",
 // §3.2 tiling and §3.4 fusion; the recurrence is §3.1 / S12 "核心思路").
 //
-// Roles (10 warps):
+// Roles (12 warps = 3 warpgroups):
 //   warps 0-3  softmax + epilogue for query tile 0 (TMEM lanes 0..127)
 //   warps 4-7  softmax + epilogue for query tile 1
 //   warp 8     TMA producer: Q tiles once, then K_j, V_j into a slot ring
 //   warp 9     MMA issuer (one thread)
+//   warps 10-11 idle (they complete the third warpgroup)
+// The third warpgroup gives registers to the two softmax warpgroups
+// (setmaxnreg), so each softmax thread holds its 128 scores without spilling.
 // MMA order per key tile j:  PV(0, j), S(0, j+1), PV(1, j), S(1, j+1), so the
 // tensor core works on one query tile while the other one's softmax runs.
 //
@@ -33,7 +37,9 @@
 namespace fa {
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;
+constexpr uint32_t kRegsSoftmax = 216;  // 2 x 128 x 216 + 128 x 72 = 384 x 168 (the launch pool)
+constexpr uint32_t kRegsOther = 72;
 constexpr int kRows = 128;   // query rows per tile = TMEM lanes
 constexpr int kKeys = 128;   // keys per K/V tile
 constexpr float kRescaleLog2 = 8.0f;
@@ -43,11 +49,9 @@ struct FwdCfg {
   static constexpr int kSub = D / 64;                // 128-byte swizzle sub-tiles per row
   static constexpr int kSubBytes = kRows * 128;      // one sub-tile: 128 rows x 128 B
   static constexpr int kTileBytes = kRows * D * 2;   // Q/K/V tile
-  static constexpr int kPBytes = kRows * kKeys * 2;  // P tile (bf16)
-  static constexpr int kSlots = (D == 128) ? 3 : 6;  // K/V ring slots
+  static constexpr int kSlots = (D == 128) ? 5 : 8;  // K/V ring slots
   static constexpr int kOffQ = 0;
-  static constexpr int kOffP = kOffQ + 2 * kTileBytes;
-  static constexpr int kOffKV = kOffP + 2 * kPBytes;
+  static constexpr int kOffKV = kOffQ + 2 * kTileBytes;
   static constexpr int kOffBar = kOffKV + kSlots * kTileBytes;
   static constexpr int kSmemBytes = kOffBar + 256 + 1024;  // barriers + alignment slack
   static constexpr uint32_t kTmemCols = 512;
@@ -153,7 +157,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const WaitCtx wc{abort_flag, args.status};
 
-  if (warp == 8) {
+  if (warp >= 8) {
+   regs_dealloc<kRegsOther>();
+   if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       uint32_t qbytes = 0;
@@ -202,14 +208,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                  k > 0 ? 1u : 0u);
         }
       };
+      // A = P in TMEM: row = lane, 16 keys per MMA = 8 columns of packed bf16 pairs
       auto issue_PV = [&](int t, int slot, bool acc) {
-        const uint32_t a0 = sbase + C::kOffP + t * C::kPBytes;
         const uint32_t b0 = sbase + C::kOffKV + slot * C::kTileBytes;
 #pragma unroll
         for (int k = 0; k < kKeys / 16; ++k) {
-          const uint32_t aoff = (k >> 2) * (kRows * 128) + (k & 3) * 32;
           const uint32_t boff = k * 16 * 128;
-          mma_ss(tmem + C::col_o(t), sdesc_sw128(a0 + aoff, 16, 1024), sdesc_sw128(b0 + boff, C::kSubBytes, 1024), idPV,
+          mma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + 8 * k, sdesc_sw128(b0 + boff, C::kSubBytes, 1024), idPV,
                  (acc || k > 0) ? 1u : 0u);
         }
       };
@@ -254,7 +259,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(bar(BAR_DRAIN));
       drain_wait(bar(BAR_DRAIN), 0);
     }
+   }
   } else {
+    regs_alloc<kRegsSoftmax>();
     // ------------------------------------------------------------ softmax / epilogue
     const int t = warp >> 2;
     const int q4 = warp & 3;
@@ -263,8 +270,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
     const uint32_t tS = tmem + lane_off + C::col_s(t);
     const uint32_t tO = tmem + lane_off + C::col_o(t);
-    const uint32_t pbase = sbase + C::kOffP + t * C::kPBytes + r_in_tile * 128;
-    const int swz = r_in_tile & 7;
     const float sl2 = args.scale_log2;
     int last_key = kv_len - 1;
     if (args.causal) last_key = min(last_key, row);
@@ -280,28 +285,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       float s[kKeys];
-      {
-        uint32_t r[64];
-        tmem_ld64(tS, r);
-#pragma unroll
-        for (int i = 0; i < 64; ++i) s[i] = __uint_as_float(r[i]);
-        tmem_ld64(tS + 64, r);
-#pragma unroll
-        for (int i = 0; i < 64; ++i) s[64 + i] = __uint_as_float(r[i]);
-      }
+      tmem_ld128f(tS, s);
       const int lim = last_key - j * kKeys;  // last visible key index within this tile
       if (lim < kKeys - 1) {
 #pragma unroll
         for (int i = 0; i < kKeys; ++i)
           if (i > lim) s[i] = -INFINITY;
       }
-      float mx[8];
+      float mx[4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = s[i];
+      for (int i = 0; i < 4; ++i) mx[i] = s[i];
 #pragma unroll
-      for (int i = 8; i < kKeys; ++i) mx[i & 7] = fmaxf(mx[i & 7], s[i]);
-      const float tile_max =
-          fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      for (int i = 4; i < kKeys; i += 8) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) mx[k] = fmax3f(mx[k], s[i + k], s[i + 4 + k < kKeys ? i + 4 + k : i + k]);
+      }
+      const float tile_max = fmax3f(fmaxf(mx[0], mx[1]), mx[2], mx[3]);
       const float x_max = tile_max * sl2;
       const bool resc = x_max > m_ref + kRescaleLog2;
       float alpha = 1.f;
@@ -323,21 +322,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st_wait();
       }
       const float neg_ref = (m_ref == -INFINITY) ? 0.f : -m_ref;
-      float part[4] = {0.f, 0.f, 0.f, 0.f};
+      const float2 sl2v = make_float2(sl2, sl2), negv = make_float2(neg_ref, neg_ref);
+      float2 part[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      uint32_t pk[kKeys / 2];  // P row as packed bf16 pairs, key 2i in the low half
 #pragma unroll
-      for (int c = 0; c < kKeys / 8; ++c) {
-        float p[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          p[i] = ex2_approx(fmaf(s[8 * c + i], sl2, neg_ref));
-          part[i & 3] += p[i];
-        }
-        const uint32_t addr = pbase + (c >> 3) * (kRows * 128) + ((((c & 7) ^ swz)) << 4);
-        st_shared_v4(addr, pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]), pack_bf16x2(p[4], p[5]),
-                     pack_bf16x2(p[6], p[7]));
+      for (int i = 0; i < kKeys / 2; ++i) {
+        const float2 x = ffma2(make_float2(s[2 * i], s[2 * i + 1]), sl2v, negv);
+        const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+        part[i & 1] = fadd2(part[i & 1], p);
+        pk[i] = pack_bf16x2(p.x, p.y);
       }
-      l_sum += (part[0] + part[1]) + (part[2] + part[3]);
-      fence_proxy_async_smem();
+      l_sum += (part[0].x + part[0].y) + (part[1].x + part[1].y);
+      tmem_st64(tS, pk);  // P overwrites the S columns this thread has read
+      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(BAR_P_FULL + t));
