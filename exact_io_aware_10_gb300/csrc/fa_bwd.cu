@@ -8,23 +8,27 @@
 // Three launches on one stream:
 //  1. bwd_pre_kernel   D_i = sum_c dO_ic O_ic and LSE_i * log2(e) into padded
 //                      fp32 rows (+inf / 0 past N), and dQacc <- 0.
-//  2. bwd_main_kernel  one CTA per (batch*head, 128-key tile j).  K_j and V_j
-//                      stay in shared memory; the CTA streams the query tiles
-//                      i that see tile j and, per tile, runs five tcgen05 MMAs
-//                      with fp32 accumulators in TMEM:
-//                        S^T = K_j Q_i^T          (TMEM cols   0..127)
-//                        dP^T = V_j dO_i^T        (TMEM cols 128..255)
-//                        dV_j += P^T dO_i         (TMEM cols 256..256+d)
-//                        dK_j += dS^T Q_i         (TMEM cols 256+d..256+2d)
-//                        dQ_i  = dS K_j           (TMEM cols   0..d, reusing S^T)
-//                      P^T and dS^T (bf16) go through one shared-memory tile;
-//                      dQ_i is added into the fp32 accumulator with vector
-//                      reductions (red.global.add.v4.f32).
+//  2. bwd_main_kernel  one CTA per (128-key tile j, batch*head); the grid runs
+//                      head by head so the CTAs in flight share one head's Q,
+//                      dO and dQ accumulator in L2.  K_j and V_j stay in shared
+//                      memory; the CTA streams the query tiles i that see
+//                      tile j and, per tile, runs five tcgen05 MMAs with fp32
+//                      accumulators in TMEM:
+//                        S^T  = K_j Q_i^T          (TMEM cols   0..127)
+//                        dP^T = V_j dO_i^T         (TMEM cols 128..255)
+//                        dV_j += P^T dO_i          (A = P^T, bf16 in TMEM over S^T)
+//                        dK_j += dS^T Q_i          (A = dS^T from shared memory)
+//                        dQ_i^T = K_j^T dS^T       (d = 128; TMEM cols 0..127, lanes = head dim)
+//                        dQ_i   = dS K_j           (d = 64;  TMEM cols 0..63, lanes = queries)
+//                      dQ_i is added into the fp32 accumulator with reductions;
+//                      at d = 128 a warp's reduction covers 32 consecutive
+//                      floats of one row (one 128-byte line).
 //  3. bwd_dq_kernel    dQ = bf16(dQacc).
 //
-// Roles of the main kernel (10 warps): warps 0-7 compute (thread = key row of
-// S^T / dP^T / dK / dV and query row of dQ; warps 0-3 take the first half of
-// the columns, 4-7 the second), warp 8 loads (TMA), warp 9 issues the MMAs.
+// Roles of the main kernel (12 warps = 3 warpgroups): warps 0-7 compute
+// (thread = key row of S^T / dP^T / dK / dV; warps 0-3 take query columns
+// 0-63, warps 4-7 columns 64-127), warp 8 loads (TMA), warp 9 issues the MMAs,
+// warps 10-11 idle; the third warpgroup hands registers to the compute warps.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -35,7 +39,9 @@
 namespace fa {
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;
+constexpr uint32_t kRegsCompute = 216;  // 2 x 128 x 216 + 128 x 72 = 384 x 168 (the launch pool)
+constexpr uint32_t kRegsOther = 72;
 constexpr int kTile = 128;  // keys per CTA and queries per step
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -48,7 +54,7 @@ struct BwdCfg {
   static constexpr int kSlots = 3;  // Q / dO ring
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kTileBytes;
-  static constexpr int kOffP = kOffV + kTileBytes;  // P^T, then dS^T
+  static constexpr int kOffP = kOffV + kTileBytes;  // dS^T (bf16, 128 x 128)
   static constexpr int kOffRing = kOffP + kPBytes;
   static constexpr int kOffSide = kOffRing + kSlots * kTileBytes;  // 2 x (LSE2[128], D[128])
   static constexpr int kOffBar = kOffSide + 2 * 1024;
@@ -65,7 +71,6 @@ enum : int {
   BAR_SIDE_EMPTY = 9,  // + 2
   BAR_SDP = 11,
   BAR_P = 12,
-  BAR_DV = 13,
   BAR_DS = 14,
   BAR_DQ_FULL = 15,
   BAR_DQ_READ = 16,
@@ -102,6 +107,10 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
                : "memory");
+}
+
+__device__ __forceinline__ void red_add_f32(float* addr, float v) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
 }
 
 __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
@@ -188,9 +197,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int bh = blockIdx.x;
+  const int bh = blockIdx.y;
   const int b = bh / a.H;
-  const int j = gridDim.y - 1 - blockIdx.y;  // key tile; causal: most query tiles first
+  const int j = blockIdx.x;  // key tile; causal: the tiles with most query tiles start first
   const int N = a.N;
   int kv_len = N;
   if (a.kv_lens != nullptr) kv_len = min(max(a.kv_lens[b], 0), N);
@@ -210,7 +219,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar(BAR_SDP), 1);
     mbar_init(bar(BAR_P), kComputeWarps);
-    mbar_init(bar(BAR_DV), 1);
     mbar_init(bar(BAR_DS), kComputeWarps);
     mbar_init(bar(BAR_DQ_FULL), 1);
     mbar_init(bar(BAR_DQ_READ), kComputeWarps);
@@ -230,124 +238,138 @@ __global__ void __launch_bounds__(kThreads, 1)
   const WaitCtx wc{abort_flag, a.status};
   const size_t side_row = static_cast<size_t>(bh) * a.Npad;
 
-  if (warp == 8) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0 && nt > 0) {
-      tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmdO);
-      mbar_arrive_expect_tx(bar(BAR_KV), 2 * C::kTileBytes);
-      for (int s = 0; s < C::kSub; ++s) {
-        tma_load_3d(sbase + C::kOffK + s * C::kSubBytes, &tmK, bar(BAR_KV), s * 64, j * kTile, bh);
-        tma_load_3d(sbase + C::kOffV + s * C::kSubBytes, &tmV, bar(BAR_KV), s * 64, j * kTile, bh);
-      }
-      int issued = 0, side_issued = 0;
-      bool ok = true;
-      for (int it = 0; ok && it < nt; ++it) {
-        const int i = i0 + it;
-        const int sd = it & 1;
-        if (!mbar_wait(bar(BAR_SIDE_EMPTY + sd), ((it >> 1) & 1) ^ 1, wc)) break;
-        mbar_arrive_expect_tx(bar(BAR_SIDE_FULL + sd), 1024);
-        bulk_load(sbase + C::kOffSide + sd * 1024, a.Lpad + side_row + i * kTile, 512, bar(BAR_SIDE_FULL + sd));
-        bulk_load(sbase + C::kOffSide + sd * 1024 + 512, a.Dpad + side_row + i * kTile, 512,
-                  bar(BAR_SIDE_FULL + sd));
-        side_issued = it + 1;
-        for (int w = 0; w < 2; ++w) {  // Q_i then dO_i
-          const int u = 2 * it + w;
-          const int slot = u % C::kSlots;
-          if (!mbar_wait(bar(BAR_RING_EMPTY + slot), ((u / C::kSlots) & 1) ^ 1, wc)) {
-            ok = false;
-            break;
+  if (warp >= 8) {
+    regs_dealloc<kRegsOther>();
+    if (warp == 8) {
+      // ---------------------------------------------------------- producer
+      if (lane == 0 && nt > 0) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmdO);
+        mbar_arrive_expect_tx(bar(BAR_KV), 2 * C::kTileBytes);
+        for (int s = 0; s < C::kSub; ++s) {
+          tma_load_3d(sbase + C::kOffK + s * C::kSubBytes, &tmK, bar(BAR_KV), s * 64, j * kTile, bh);
+          tma_load_3d(sbase + C::kOffV + s * C::kSubBytes, &tmV, bar(BAR_KV), s * 64, j * kTile, bh);
+        }
+        int issued = 0, side_issued = 0;
+        bool ok = true;
+        for (int it = 0; ok && it < nt; ++it) {
+          const int i = i0 + it;
+          const int sd = it & 1;
+          if (!mbar_wait(bar(BAR_SIDE_EMPTY + sd), ((it >> 1) & 1) ^ 1, wc)) break;
+          mbar_arrive_expect_tx(bar(BAR_SIDE_FULL + sd), 1024);
+          bulk_load(sbase + C::kOffSide + sd * 1024, a.Lpad + side_row + i * kTile, 512, bar(BAR_SIDE_FULL + sd));
+          bulk_load(sbase + C::kOffSide + sd * 1024 + 512, a.Dpad + side_row + i * kTile, 512,
+                    bar(BAR_SIDE_FULL + sd));
+          side_issued = it + 1;
+          for (int w = 0; w < 2; ++w) {  // Q_i then dO_i
+            const int u = 2 * it + w;
+            const int slot = u % C::kSlots;
+            if (!mbar_wait(bar(BAR_RING_EMPTY + slot), ((u / C::kSlots) & 1) ^ 1, wc)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(bar(BAR_RING_FULL + slot), C::kTileBytes);
+            const CUtensorMap* tm = w ? &tmdO : &tmQ;
+            for (int s = 0; s < C::kSub; ++s)
+              tma_load_3d(sbase + C::kOffRing + slot * C::kTileBytes + s * C::kSubBytes, tm,
+                          bar(BAR_RING_FULL + slot), s * 64, i * kTile, bh);
+            issued = u + 1;
           }
-          mbar_arrive_expect_tx(bar(BAR_RING_FULL + slot), C::kTileBytes);
-          const CUtensorMap* tm = w ? &tmdO : &tmQ;
-          for (int s = 0; s < C::kSub; ++s)
-            tma_load_3d(sbase + C::kOffRing + slot * C::kTileBytes + s * C::kSubBytes, tm, bar(BAR_RING_FULL + slot),
-                        s * 64, i * kTile, bh);
-          issued = u + 1;
+        }
+        drain_wait(bar(BAR_KV), 0);
+        for (int s = 0; s < C::kSlots && s < issued; ++s) {
+          const int u_last = s + C::kSlots * ((issued - 1 - s) / C::kSlots);
+          drain_wait(bar(BAR_RING_FULL + s), (u_last / C::kSlots) & 1);
+        }
+        for (int s = 0; s < 2 && s < side_issued; ++s) {
+          const int it_last = s + 2 * ((side_issued - 1 - s) / 2);
+          drain_wait(bar(BAR_SIDE_FULL + s), (it_last >> 1) & 1);
         }
       }
-      drain_wait(bar(BAR_KV), 0);
-      for (int s = 0; s < C::kSlots && s < issued; ++s) {
-        const int u_last = s + C::kSlots * ((issued - 1 - s) / C::kSlots);
-        drain_wait(bar(BAR_RING_FULL + s), (u_last / C::kSlots) & 1);
-      }
-      for (int s = 0; s < 2 && s < side_issued; ++s) {
-        const int it_last = s + 2 * ((side_issued - 1 - s) / 2);
-        drain_wait(bar(BAR_SIDE_FULL + s), (it_last >> 1) & 1);
-      }
-    }
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && nt > 0) {
-      constexpr uint32_t idSS = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
-      constexpr uint32_t idKN = idesc_bf16_f32(128, D, false, true);     // dV, dK
-      constexpr uint32_t idNN = idesc_bf16_f32(128, D, true, true);      // dQ
-      const uint32_t sK = sbase + C::kOffK, sV = sbase + C::kOffV, sP = sbase + C::kOffP;
-      // A and B both K-major, K extent = D (head dim)
-      auto mma_kmajor_d = [&](uint32_t dcol, uint32_t a0, uint32_t b0) {
+    } else if (warp == 9) {
+      // ---------------------------------------------------------- MMA issuer
+      if (lane == 0 && nt > 0) {
+        constexpr uint32_t idSS = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
+        constexpr uint32_t idKN = idesc_bf16_f32(128, D, false, true);     // dV (TS), dK
+        const uint32_t sK = sbase + C::kOffK, sV = sbase + C::kOffV, sP = sbase + C::kOffP;
+        // A and B both K-major, K extent = D (head dim)
+        auto mma_kmajor_d = [&](uint32_t dcol, uint32_t a0, uint32_t b0) {
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * C::kSubBytes + (k & 3) * 32;
-          mma_ss(tmem + dcol, sdesc_sw128(a0 + off, 16, 1024), sdesc_sw128(b0 + off, 16, 1024), idSS, k > 0 ? 1u : 0u);
+          for (int k = 0; k < D / 16; ++k) {
+            const uint32_t off = (k >> 2) * C::kSubBytes + (k & 3) * 32;
+            mma_ss(tmem + dcol, sdesc_sw128(a0 + off, 16, 1024), sdesc_sw128(b0 + off, 16, 1024), idSS,
+                   k > 0 ? 1u : 0u);
+          }
+        };
+        bool ok = mbar_wait(bar(BAR_KV), 0, wc);
+        for (int it = 0; ok && it < nt; ++it) {
+          const int uQ = 2 * it, uO = 2 * it + 1;
+          const int sQ = uQ % C::kSlots, sO = uO % C::kSlots;
+          const uint32_t aQ = sbase + C::kOffRing + sQ * C::kTileBytes;
+          const uint32_t aO = sbase + C::kOffRing + sO * C::kTileBytes;
+          // dP^T = V_j dO_i^T
+          if (!(ok = mbar_wait(bar(BAR_RING_FULL + sO), (uO / C::kSlots) & 1, wc))) break;
+          tc_fence_after();
+          mma_kmajor_d(C::kColDP, sV, aO);
+          // S^T = K_j Q_i^T  (its columns hold dQ of the previous tile until that has been read)
+          if (it > 0 && !(ok = mbar_wait(bar(BAR_DQ_READ), (it - 1) & 1, wc))) break;
+          if (!(ok = mbar_wait(bar(BAR_RING_FULL + sQ), (uQ / C::kSlots) & 1, wc))) break;
+          tc_fence_after();
+          mma_kmajor_d(C::kColS, sK, aQ);
+          mma_commit(bar(BAR_SDP));
+          // dV_j += P^T dO_i   (P^T packed bf16 in TMEM: queries 0-63 in cols 0-31, 64-127 in cols 64-95)
+          if (!(ok = mbar_wait(bar(BAR_P), it & 1, wc))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < kTile / 16; ++k) {
+            const uint32_t acol = (k < 4) ? 8 * k : 64 + 8 * (k - 4);
+            mma_ts(tmem + C::kColDV, tmem + C::kColS + acol, sdesc_sw128(aO + k * 2048, C::kSubBytes, 1024), idKN,
+                   (it > 0 || k > 0) ? 1u : 0u);
+          }
+          mma_commit(bar(BAR_RING_EMPTY + sO));
+          // dK_j += dS^T Q_i  and  dQ_i (see the header)
+          if (!(ok = mbar_wait(bar(BAR_DS), it & 1, wc))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < kTile / 16; ++k) {
+            const uint32_t aoff = (k >> 2) * C::kSubBytes + (k & 3) * 32;
+            mma_ss(tmem + C::kColDK, sdesc_sw128(sP + aoff, 16, 1024), sdesc_sw128(aQ + k * 2048, C::kSubBytes, 1024),
+                   idKN, (it > 0 || k > 0) ? 1u : 0u);
+          }
+          if constexpr (D == 128) {
+            constexpr uint32_t idQT = idesc_bf16_f32(128, 128, true, true);  // A = K^T, B = dS^T
+#pragma unroll
+            for (int k = 0; k < kTile / 16; ++k)
+              mma_ss(tmem + C::kColDQ, sdesc_sw128(sK + k * 2048, C::kSubBytes, 1024),
+                     sdesc_sw128(sP + k * 2048, C::kSubBytes, 1024), idQT, k > 0 ? 1u : 0u);
+          } else {
+            constexpr uint32_t idNN = idesc_bf16_f32(128, D, true, true);  // A = dS, B = K
+#pragma unroll
+            for (int k = 0; k < kTile / 16; ++k)
+              mma_ss(tmem + C::kColDQ, sdesc_sw128(sP + k * 2048, C::kSubBytes, 1024),
+                     sdesc_sw128(sK + k * 2048, C::kSubBytes, 1024), idNN, k > 0 ? 1u : 0u);
+          }
+          mma_commit(bar(BAR_DQ_FULL));
+          mma_commit(bar(BAR_RING_EMPTY + sQ));
         }
-      };
-      // A = P^T / dS^T (K-major over 128 queries), B MN-major (rows = queries)
-      auto mma_p_b = [&](uint32_t dcol, uint32_t b0, bool acc) {
-#pragma unroll
-        for (int k = 0; k < kTile / 16; ++k) {
-          const uint32_t aoff = (k >> 2) * C::kSubBytes + (k & 3) * 32;
-          mma_ss(tmem + dcol, sdesc_sw128(sP + aoff, 16, 1024), sdesc_sw128(b0 + k * 2048, C::kSubBytes, 1024), idKN,
-                 (acc || k > 0) ? 1u : 0u);
-        }
-      };
-      bool ok = mbar_wait(bar(BAR_KV), 0, wc);
-      for (int it = 0; ok && it < nt; ++it) {
-        const int uQ = 2 * it, uO = 2 * it + 1;
-        const int sQ = uQ % C::kSlots, sO = uO % C::kSlots;
-        const uint32_t aQ = sbase + C::kOffRing + sQ * C::kTileBytes;
-        const uint32_t aO = sbase + C::kOffRing + sO * C::kTileBytes;
-        // dP^T = V_j dO_i^T
-        if (!(ok = mbar_wait(bar(BAR_RING_FULL + sO), (uO / C::kSlots) & 1, wc))) break;
-        tc_fence_after();
-        mma_kmajor_d(C::kColDP, sV, aO);
-        // S^T = K_j Q_i^T  (its columns hold dQ_{i-1} until that has been read)
-        if (it > 0 && !(ok = mbar_wait(bar(BAR_DQ_READ), (it - 1) & 1, wc))) break;
-        if (!(ok = mbar_wait(bar(BAR_RING_FULL + sQ), (uQ / C::kSlots) & 1, wc))) break;
-        tc_fence_after();
-        mma_kmajor_d(C::kColS, sK, aQ);
-        mma_commit(bar(BAR_SDP));
-        // dV_j += P^T dO_i
-        if (!(ok = mbar_wait(bar(BAR_P), it & 1, wc))) break;
-        tc_fence_after();
-        mma_p_b(C::kColDV, aO, it > 0);
-        mma_commit(bar(BAR_DV));
-        mma_commit(bar(BAR_RING_EMPTY + sO));
-        // dK_j += dS^T Q_i ;  dQ_i = dS K_j
-        if (!(ok = mbar_wait(bar(BAR_DS), it & 1, wc))) break;
-        tc_fence_after();
-        mma_p_b(C::kColDK, aQ, it > 0);
-#pragma unroll
-        for (int k = 0; k < kTile / 16; ++k)
-          mma_ss(tmem + C::kColDQ, sdesc_sw128(sP + k * 2048, C::kSubBytes, 1024),
-                 sdesc_sw128(sK + k * 2048, C::kSubBytes, 1024), idNN, k > 0 ? 1u : 0u);
-        mma_commit(bar(BAR_DQ_FULL));
-        mma_commit(bar(BAR_RING_EMPTY + sQ));
+        if (ok) mma_commit(bar(BAR_FINAL));
+        mma_commit(bar(BAR_DRAIN));
+        drain_wait(bar(BAR_DRAIN), 0);
       }
-      if (ok) mma_commit(bar(BAR_FINAL));
-      mma_commit(bar(BAR_DRAIN));
-      drain_wait(bar(BAR_DRAIN), 0);
     }
   } else {
+    regs_alloc<kRegsCompute>();
     // ------------------------------------------------------------ compute warps
-    const int half = warp >> 2;  // column half
+    const int half = warp >> 2;  // query-column half
     const int q4 = warp & 3;
-    const int r = q4 * 32 + lane;  // key row (S^T, dP^T, dK, dV) / query row (dQ)
+    const int r = q4 * 32 + lane;  // key row (S^T, dP^T, dK, dV); head-dim row of dQ^T (d = 128)
     const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
     const int key = j * kTile + r;
     const bool key_ok = key < kv_len;
-    const uint32_t prow = sbase + C::kOffP + half * C::kSubBytes + r * 128;
+    const uint32_t dsrow = sbase + C::kOffP + half * C::kSubBytes + r * 128;
     const int swz = r & 7;
-    const float sl2 = a.scale_log2;
+    const float2 sl2v = make_float2(a.scale_log2, a.scale_log2);
+    const float2 scv = make_float2(a.scale, a.scale);
     bool aborted = false;
     for (int it = 0; it < nt; ++it) {
       const int i = i0 + it;
@@ -362,71 +384,82 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- P^T = exp2(S^T * scale * log2e - LSE2[q]) on this thread's 64 query columns
       float p[64];
       {
-        uint32_t rr[64];
-        tmem_ld64(tmem + lane_off + C::kColS + half * 64, rr);
-        // causal: key > query is masked; queries past N have LSE2 = +inf -> 0
-        const int qlo = i * kTile + half * 64;
-        const int first_vis = a.causal ? (key - qlo) : 0;  // columns c >= first_vis are visible
+        float sv[64];
+        tmem_ld64(tmem + lane_off + C::kColS + half * 64, *reinterpret_cast<uint32_t(*)[64]>(sv));
 #pragma unroll
         for (int c = 0; c < 64; c += 4) {
           const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c);
-          p[c + 0] = ex2_approx(fmaf(__uint_as_float(rr[c + 0]), sl2, -l4.x));
-          p[c + 1] = ex2_approx(fmaf(__uint_as_float(rr[c + 1]), sl2, -l4.y));
-          p[c + 2] = ex2_approx(fmaf(__uint_as_float(rr[c + 2]), sl2, -l4.z));
-          p[c + 3] = ex2_approx(fmaf(__uint_as_float(rr[c + 3]), sl2, -l4.w));
+          const float2 x0 = ffma2(make_float2(sv[c], sv[c + 1]), sl2v, make_float2(-l4.x, -l4.y));
+          const float2 x1 = ffma2(make_float2(sv[c + 2], sv[c + 3]), sl2v, make_float2(-l4.z, -l4.w));
+          p[c + 0] = ex2_approx(x0.x);
+          p[c + 1] = ex2_approx(x0.y);
+          p[c + 2] = ex2_approx(x1.x);
+          p[c + 3] = ex2_approx(x1.y);
         }
+        // causal: key > query is masked; queries past N have LSE2 = +inf -> 0
+        const int qlo = i * kTile + half * 64;
+        const int first_vis = a.causal ? (key - qlo) : 0;  // columns c >= first_vis are visible
         if (!key_ok || first_vis > 0) {
 #pragma unroll
           for (int c = 0; c < 64; ++c)
             if (!key_ok || c < first_vis) p[c] = 0.f;
         }
       }
+      {
+        uint32_t pk[32];
 #pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8) {
-        st_shared_v4(prow + (((c8 ^ swz)) << 4), pack_bf16x2(p[8 * c8 + 0], p[8 * c8 + 1]),
-                     pack_bf16x2(p[8 * c8 + 2], p[8 * c8 + 3]), pack_bf16x2(p[8 * c8 + 4], p[8 * c8 + 5]),
-                     pack_bf16x2(p[8 * c8 + 6], p[8 * c8 + 7]));
+        for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(p[2 * c], p[2 * c + 1]);
+        tmem_st32(tmem + lane_off + C::kColS + half * 64, pk);  // over this thread's own S^T columns
+        tmem_st_wait();
       }
-      fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(BAR_P));
-      // ---- dS^T = scale * P^T * (dP^T - D[q])
+      // ---- dS^T = scale * P^T * (dP^T - D[q])  -> shared memory (bf16, K-major for dK, MN-major for dQ)
       {
-        uint32_t rr[64];
-        tmem_ld64(tmem + lane_off + C::kColDP + half * 64, rr);
+        float dv[64];
+        tmem_ld64(tmem + lane_off + C::kColDP + half * 64, *reinterpret_cast<uint32_t(*)[64]>(dv));
 #pragma unroll
-        for (int c = 0; c < 64; c += 4) {
-          const float4 d4 = *reinterpret_cast<const float4*>(dsum + c);
-          p[c + 0] = a.scale * p[c + 0] * (__uint_as_float(rr[c + 0]) - d4.x);
-          p[c + 1] = a.scale * p[c + 1] * (__uint_as_float(rr[c + 1]) - d4.y);
-          p[c + 2] = a.scale * p[c + 2] * (__uint_as_float(rr[c + 2]) - d4.z);
-          p[c + 3] = a.scale * p[c + 3] * (__uint_as_float(rr[c + 3]) - d4.w);
+        for (int c = 0; c < 64; c += 2) {
+          const float2 d2 = *reinterpret_cast<const float2*>(dsum + c);
+          const float2 ps = fmul2(make_float2(p[c], p[c + 1]), scv);
+          const float2 g = fadd2(make_float2(dv[c], dv[c + 1]), make_float2(-d2.x, -d2.y));
+          const float2 ds = fmul2(ps, g);
+          p[c] = ds.x;
+          p[c + 1] = ds.y;
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(BAR_SIDE_EMPTY + sd));
-      if (!mbar_wait(bar(BAR_DV), it & 1, wc)) {  // P^T no longer read by the dV MMA
-        aborted = true;
-        break;
-      }
 #pragma unroll
       for (int c8 = 0; c8 < 8; ++c8) {
-        st_shared_v4(prow + (((c8 ^ swz)) << 4), pack_bf16x2(p[8 * c8 + 0], p[8 * c8 + 1]),
+        st_shared_v4(dsrow + (((c8 ^ swz)) << 4), pack_bf16x2(p[8 * c8 + 0], p[8 * c8 + 1]),
                      pack_bf16x2(p[8 * c8 + 2], p[8 * c8 + 3]), pack_bf16x2(p[8 * c8 + 4], p[8 * c8 + 5]),
                      pack_bf16x2(p[8 * c8 + 6], p[8 * c8 + 7]));
       }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(BAR_DS));
-      // ---- dQ_i rows (thread = query row r) += this tile's dS K_j
+      // ---- dQ_i += this tile's contribution
       if (!mbar_wait(bar(BAR_DQ_FULL), it & 1, wc)) {
         aborted = true;
         break;
       }
       tc_fence_after();
-      {
+      if constexpr (D == 128) {
+        // dQ^T: lane = head-dim index r, columns = this half's 64 queries; a warp
+        // reduces 32 consecutive floats of one dQ row per instruction
+        uint32_t rr[64];
+        tmem_ld64(tmem + lane_off + C::kColDQ + half * 64, rr);
+        const int q0 = i * kTile + half * 64;
+        float* col = a.dQacc + (static_cast<size_t>(bh) * N + q0) * D + r;
+        const int nrow = min(64, N - q0);
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (c < nrow) red_add_f32(col + static_cast<size_t>(c) * D, __uint_as_float(rr[c]));
+      } else {
+        // dQ: lane = query row r, columns = this half's D/2 head-dim entries
         const int qrow = i * kTile + r;
         float* dst = a.dQacc + (static_cast<size_t>(bh) * N + qrow) * D + half * (D / 2);
 #pragma unroll
@@ -533,7 +566,7 @@ fa_status bwd_launch_d(const void* Q, const void* K, const void* V, const void* 
   bwd_pre_kernel<D><<<static_cast<unsigned>((pre_rows + 7) / 8), 256, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), LSE, a, BH);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
-  bwd_main_kernel<D><<<dim3(BH, nq), kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, a);
+  bwd_main_kernel<D><<<dim3(nq, BH), kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, a);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   const long long n4 = static_cast<long long>(BH) * N * D / 4;
   bwd_dq_kernel<<<static_cast<unsigned>((n4 + 255) / 256), 256, 0, stream>>>(a.dQacc,
