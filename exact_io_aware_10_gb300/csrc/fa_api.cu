@@ -41,8 +41,26 @@ unsigned* device_status_ptr() {
   return g_status_ptr[dev];
 }
 
+namespace {
+bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, CUtensorMapSwizzle swizzle, const void* base, int rank,
+                 const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box);
+}  // namespace
+
 bool encode_bf16_tmap(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
                       const uint64_t* strides_bytes, const uint32_t* box) {
+  return encode_tmap(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, CU_TENSOR_MAP_SWIZZLE_128B, base, rank, dims,
+                     strides_bytes, box);
+}
+
+bool encode_f32_tmap(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                     const uint64_t* strides_bytes, const uint32_t* box) {
+  return encode_tmap(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, CU_TENSOR_MAP_SWIZZLE_NONE, base, rank, dims,
+                     strides_bytes, box);
+}
+
+namespace {
+bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, CUtensorMapSwizzle swizzle, const void* base, int rank,
+                 const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box) {
   {
     std::lock_guard<std::mutex> lk(g_mu);
     if (g_encode == nullptr) {
@@ -65,11 +83,12 @@ bool encode_bf16_tmap(CUtensorMap* map, const void* base, int rank, const uint64
     estr[i] = 1;
     if (i + 1 < rank) gstr[i] = strides_bytes[i];
   }
-  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank), const_cast<void*>(base),
-                        gdim, gstr, bdim, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = g_encode(map, dtype, static_cast<cuuint32_t>(rank), const_cast<void*>(base), gdim, gstr, bdim, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
+}  // namespace
 
 }  // namespace fa
 

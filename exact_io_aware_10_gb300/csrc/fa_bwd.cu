@@ -6,8 +6,8 @@
 //     dK = scale dS^T Q,  dQ = scale dS K.
 //
 // Three launches on one stream:
-//  1. bwd_pre_kernel   D_i = sum_c dO_ic O_ic and LSE_i * log2(e) into padded
-//                      fp32 rows (+inf / 0 past N), and dQacc <- 0.
+//  1. bwd_pre_kernel   -D_i = -sum_c dO_ic O_ic and -LSE_i * log2(e) into padded
+//                      fp32 rows (0 / -inf past N), and dQacc <- 0.
 //  2. bwd_main_kernel  one CTA per (128-key tile j, batch*head); the grid runs
 //                      head by head so the CTAs in flight share one head's Q,
 //                      dO and dQ accumulator in L2.  K_j and V_j stay in shared
@@ -18,17 +18,20 @@
 //                        dP^T = V_j dO_i^T         (TMEM cols 128..255)
 //                        dV_j += P^T dO_i          (A = P^T, bf16 in TMEM over S^T)
 //                        dK_j += dS^T Q_i          (A = dS^T from shared memory)
-//                        dQ_i^T = K_j^T dS^T       (d = 128; TMEM cols 0..127, lanes = head dim)
-//                        dQ_i   = dS K_j           (d = 64;  TMEM cols 0..63, lanes = queries)
-//                      dQ_i is added into the fp32 accumulator with reductions;
-//                      at d = 128 a warp's reduction covers 32 consecutive
-//                      floats of one row (one 128-byte line).
+//                        dQ_i^T = K_j^T dS^T       (d = 128: lanes = head dim, over dP^T)
+//                        dQ_i   = dS K_j           (d = 64: lanes = queries, over dP^T)
+//                      MMA order per tile: dV_i, S_{i+1}, dK_i, dQ_i, dP_{i+1}, so
+//                      the next tile's scores are ready while dS_i is formed.
+//                      dQ_i is added into the fp32 accumulator with reductions
+//                      in L2; at d = 128 one warp instruction covers 32
+//                      consecutive floats of a dQ row.
 //  3. bwd_dq_kernel    dQ = bf16(dQacc).
 //
-// Roles of the main kernel (12 warps = 3 warpgroups): warps 0-7 compute
-// (thread = key row of S^T / dP^T / dK / dV; warps 0-3 take query columns
-// 0-63, warps 4-7 columns 64-127), warp 8 loads (TMA), warp 9 issues the MMAs,
-// warps 10-11 idle; the third warpgroup hands registers to the compute warps.
+// Roles of the main kernel (20 warps = 5 warpgroups): warps 0-15 compute
+// (thread = key row of S^T / dP^T / dK / dV; warpgroup h takes query columns
+// 32h..32h+31 and head-dim columns h*d/4.. of dK/dV), warp 16 loads (TMA),
+// warp 17 issues the MMAs, warps 18-19 idle; the fifth warpgroup hands
+// registers to the compute warps.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -39,9 +42,9 @@
 namespace fa {
 namespace {
 
-constexpr int kThreads = 384;
-constexpr uint32_t kRegsCompute = 216;  // 2 x 128 x 216 + 128 x 72 = 384 x 168 (the launch pool)
-constexpr uint32_t kRegsOther = 72;
+constexpr int kThreads = 640;
+constexpr uint32_t kRegsCompute = 104;  // 4 x 128 x 104 + 128 x 64 = 640 x 96 (the launch pool)
+constexpr uint32_t kRegsOther = 64;
 constexpr int kTile = 128;  // keys per CTA and queries per step
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -51,26 +54,29 @@ struct BwdCfg {
   static constexpr int kSubBytes = kTile * 128;
   static constexpr int kTileBytes = kTile * D * 2;
   static constexpr int kPBytes = kTile * kTile * 2;
-  static constexpr int kSlots = 3;  // Q / dO ring
+  static constexpr int kSlots = 3;  // Q_i, Q_{i+1} and dO_i tiles
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kTileBytes;
   static constexpr int kOffP = kOffV + kTileBytes;  // dS^T (bf16, 128 x 128)
-  static constexpr int kOffRing = kOffP + kPBytes;
+  static constexpr int kOffRing = kOffP + kPBytes;  // Q slots 0-1, then the dO slot
   static constexpr int kOffSide = kOffRing + kSlots * kTileBytes;  // 2 x (LSE2[128], D[128])
   static constexpr int kOffBar = kOffSide + 2 * 1024;
   static constexpr int kSmemBytes = kOffBar + 256 + 1024;
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D, kColDQ = 0;
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D, kColDQ = 128;
 };
 
 enum : int {
   BAR_KV = 0,
-  BAR_RING_FULL = 1,   // + slot (3)
-  BAR_RING_EMPTY = 4,  // + slot (3)
+  BAR_Q_FULL = 1,   // + slot (2)
+  BAR_DO_FULL = 3,
+  BAR_Q_EMPTY = 4,  // + slot (2)
+  BAR_DO_EMPTY = 6,
   BAR_SIDE_FULL = 7,   // + 2
   BAR_SIDE_EMPTY = 9,  // + 2
-  BAR_SDP = 11,
+  BAR_S = 11,
   BAR_P = 12,
+  BAR_DP = 13,
   BAR_DS = 14,
   BAR_DQ_FULL = 15,
   BAR_DQ_READ = 16,
@@ -80,11 +86,11 @@ enum : int {
 };
 constexpr int kOffTmemSlot = kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 4;
-constexpr int kComputeWarps = 8;
+constexpr int kComputeWarps = 16;
 
 struct BwdArgs {
-  float* Dpad;      // [BH, Npad]
-  float* Lpad;      // [BH, Npad] LSE * log2(e), +inf past N
+  float* Dpad;      // [BH, Npad] -D, 0 past N
+  float* Lpad;      // [BH, Npad] -LSE * log2(e), -inf past N
   float* dQacc;     // [BH, N, D] fp32
   void* dK;         // [BH, N, D] bf16
   void* dV;
@@ -119,7 +125,7 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
 }
 
 // --------------------------------------------------------------------------- 1. preprocess
-// One warp per row: D = rowsum(dO * O) in fp32, LSE in log2 units, dQacc row = 0.
+// One warp per row: -D = -rowsum(dO * O) in fp32, -LSE in log2 units, dQacc row = 0.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ O,
                                                       const __nv_bfloat16* __restrict__ dO,
@@ -133,7 +139,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
   if (r >= a.N) {
     if (lane == 0) {
       a.Dpad[gw] = 0.f;
-      a.Lpad[gw] = INFINITY;
+      a.Lpad[gw] = -INFINITY;
     }
     return;
   }
@@ -163,8 +169,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   if (lane == 0) {
-    a.Dpad[gw] = acc;
-    a.Lpad[gw] = LSE[row] * kLog2e;
+    a.Dpad[gw] = -acc;
+    a.Lpad[gw] = -LSE[row] * kLog2e;
   }
 }
 
@@ -209,16 +215,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar(BAR_KV), 1);
-    for (int s = 0; s < C::kSlots; ++s) {
-      mbar_init(bar(BAR_RING_FULL + s), 1);
-      mbar_init(bar(BAR_RING_EMPTY + s), 1);
-    }
     for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(BAR_Q_FULL + s), 1);
+      mbar_init(bar(BAR_Q_EMPTY + s), 1);
       mbar_init(bar(BAR_SIDE_FULL + s), 1);
       mbar_init(bar(BAR_SIDE_EMPTY + s), kComputeWarps);
     }
-    mbar_init(bar(BAR_SDP), 1);
+    mbar_init(bar(BAR_DO_FULL), 1);
+    mbar_init(bar(BAR_DO_EMPTY), 1);
+    mbar_init(bar(BAR_S), 1);
     mbar_init(bar(BAR_P), kComputeWarps);
+    mbar_init(bar(BAR_DP), 1);
     mbar_init(bar(BAR_DS), kComputeWarps);
     mbar_init(bar(BAR_DQ_FULL), 1);
     mbar_init(bar(BAR_DQ_READ), kComputeWarps);
@@ -238,9 +245,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const WaitCtx wc{abort_flag, a.status};
   const size_t side_row = static_cast<size_t>(bh) * a.Npad;
 
-  if (warp >= 8) {
+  if (warp >= kComputeWarps) {
     regs_dealloc<kRegsOther>();
-    if (warp == 8) {
+    if (warp == kComputeWarps) {
       // ---------------------------------------------------------- producer
       if (lane == 0 && nt > 0) {
         tma_prefetch_desc(&tmQ);
@@ -250,9 +257,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(sbase + C::kOffK + s * C::kSubBytes, &tmK, bar(BAR_KV), s * 64, j * kTile, bh);
           tma_load_3d(sbase + C::kOffV + s * C::kSubBytes, &tmV, bar(BAR_KV), s * 64, j * kTile, bh);
         }
-        int issued = 0, side_issued = 0;
-        bool ok = true;
-        for (int it = 0; ok && it < nt; ++it) {
+        int side_issued = 0, q_issued = 0, o_issued = 0;
+        for (int it = 0; it < nt; ++it) {
           const int i = i0 + it;
           const int sd = it & 1;
           if (!mbar_wait(bar(BAR_SIDE_EMPTY + sd), ((it >> 1) & 1) ^ 1, wc)) break;
@@ -261,37 +267,40 @@ __global__ void __launch_bounds__(kThreads, 1)
           bulk_load(sbase + C::kOffSide + sd * 1024 + 512, a.Dpad + side_row + i * kTile, 512,
                     bar(BAR_SIDE_FULL + sd));
           side_issued = it + 1;
-          for (int w = 0; w < 2; ++w) {  // Q_i then dO_i
-            const int u = 2 * it + w;
-            const int slot = u % C::kSlots;
-            if (!mbar_wait(bar(BAR_RING_EMPTY + slot), ((u / C::kSlots) & 1) ^ 1, wc)) {
-              ok = false;
-              break;
-            }
-            mbar_arrive_expect_tx(bar(BAR_RING_FULL + slot), C::kTileBytes);
-            const CUtensorMap* tm = w ? &tmdO : &tmQ;
-            for (int s = 0; s < C::kSub; ++s)
-              tma_load_3d(sbase + C::kOffRing + slot * C::kTileBytes + s * C::kSubBytes, tm,
-                          bar(BAR_RING_FULL + slot), s * 64, i * kTile, bh);
-            issued = u + 1;
-          }
+          // Q_i into Q slot it % 2 (free once dK of tile it-2 is done)
+          if (!mbar_wait(bar(BAR_Q_EMPTY + sd), ((it >> 1) & 1) ^ 1, wc)) break;
+          mbar_arrive_expect_tx(bar(BAR_Q_FULL + sd), C::kTileBytes);
+          for (int s = 0; s < C::kSub; ++s)
+            tma_load_3d(sbase + C::kOffRing + sd * C::kTileBytes + s * C::kSubBytes, &tmQ, bar(BAR_Q_FULL + sd),
+                        s * 64, i * kTile, bh);
+          q_issued = it + 1;
+          // dO_i into the dO slot (free once dV of tile it-1 is done)
+          if (!mbar_wait(bar(BAR_DO_EMPTY), (it & 1) ^ 1, wc)) break;
+          mbar_arrive_expect_tx(bar(BAR_DO_FULL), C::kTileBytes);
+          for (int s = 0; s < C::kSub; ++s)
+            tma_load_3d(sbase + C::kOffRing + 2 * C::kTileBytes + s * C::kSubBytes, &tmdO, bar(BAR_DO_FULL), s * 64,
+                        i * kTile, bh);
+          o_issued = it + 1;
         }
         drain_wait(bar(BAR_KV), 0);
-        for (int s = 0; s < C::kSlots && s < issued; ++s) {
-          const int u_last = s + C::kSlots * ((issued - 1 - s) / C::kSlots);
-          drain_wait(bar(BAR_RING_FULL + s), (u_last / C::kSlots) & 1);
+        for (int s = 0; s < 2 && s < q_issued; ++s) {
+          const int it_last = s + 2 * ((q_issued - 1 - s) / 2);
+          drain_wait(bar(BAR_Q_FULL + s), (it_last >> 1) & 1);
         }
         for (int s = 0; s < 2 && s < side_issued; ++s) {
           const int it_last = s + 2 * ((side_issued - 1 - s) / 2);
           drain_wait(bar(BAR_SIDE_FULL + s), (it_last >> 1) & 1);
         }
+        if (o_issued > 0) drain_wait(bar(BAR_DO_FULL), (o_issued - 1) & 1);
       }
-    } else if (warp == 9) {
+    } else if (warp == kComputeWarps + 1) {
       // ---------------------------------------------------------- MMA issuer
       if (lane == 0 && nt > 0) {
         constexpr uint32_t idSS = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
         constexpr uint32_t idKN = idesc_bf16_f32(128, D, false, true);     // dV (TS), dK
         const uint32_t sK = sbase + C::kOffK, sV = sbase + C::kOffV, sP = sbase + C::kOffP;
+        auto q_addr = [&](int it) { return sbase + C::kOffRing + (it & 1) * C::kTileBytes; };
+        const uint32_t aO = sbase + C::kOffRing + 2 * C::kTileBytes;
         // A and B both K-major, K extent = D (head dim)
         auto mma_kmajor_d = [&](uint32_t dcol, uint32_t a0, uint32_t b0) {
 #pragma unroll
@@ -302,32 +311,40 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         };
         bool ok = mbar_wait(bar(BAR_KV), 0, wc);
-        for (int it = 0; ok && it < nt; ++it) {
-          const int uQ = 2 * it, uO = 2 * it + 1;
-          const int sQ = uQ % C::kSlots, sO = uO % C::kSlots;
-          const uint32_t aQ = sbase + C::kOffRing + sQ * C::kTileBytes;
-          const uint32_t aO = sbase + C::kOffRing + sO * C::kTileBytes;
-          // dP^T = V_j dO_i^T
-          if (!(ok = mbar_wait(bar(BAR_RING_FULL + sO), (uO / C::kSlots) & 1, wc))) break;
+        // prologue: S_0 and dP_0
+        if (ok) ok = mbar_wait(bar(BAR_Q_FULL + 0), 0, wc);
+        if (ok) {
+          tc_fence_after();
+          mma_kmajor_d(C::kColS, sK, q_addr(0));
+          mma_commit(bar(BAR_S));
+          ok = mbar_wait(bar(BAR_DO_FULL), 0, wc);
+        }
+        if (ok) {
           tc_fence_after();
           mma_kmajor_d(C::kColDP, sV, aO);
-          // S^T = K_j Q_i^T  (its columns hold dQ of the previous tile until that has been read)
-          if (it > 0 && !(ok = mbar_wait(bar(BAR_DQ_READ), (it - 1) & 1, wc))) break;
-          if (!(ok = mbar_wait(bar(BAR_RING_FULL + sQ), (uQ / C::kSlots) & 1, wc))) break;
-          tc_fence_after();
-          mma_kmajor_d(C::kColS, sK, aQ);
-          mma_commit(bar(BAR_SDP));
-          // dV_j += P^T dO_i   (P^T packed bf16 in TMEM: queries 0-63 in cols 0-31, 64-127 in cols 64-95)
+          mma_commit(bar(BAR_DP));
+        }
+        for (int it = 0; ok && it < nt; ++it) {
+          const uint32_t aQ = q_addr(it);
+          const bool next = it + 1 < nt;
+          // dV_j += P^T dO_i  (P^T packed bf16 in TMEM: warpgroup h's 32 queries in cols 32h..32h+15)
           if (!(ok = mbar_wait(bar(BAR_P), it & 1, wc))) break;
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < kTile / 16; ++k) {
-            const uint32_t acol = (k < 4) ? 8 * k : 64 + 8 * (k - 4);
+            const uint32_t acol = 32 * (k >> 1) + 8 * (k & 1);
             mma_ts(tmem + C::kColDV, tmem + C::kColS + acol, sdesc_sw128(aO + k * 2048, C::kSubBytes, 1024), idKN,
                    (it > 0 || k > 0) ? 1u : 0u);
           }
-          mma_commit(bar(BAR_RING_EMPTY + sO));
-          // dK_j += dS^T Q_i  and  dQ_i (see the header)
+          mma_commit(bar(BAR_DO_EMPTY));
+          // S_{i+1} = K_j Q_{i+1}^T over the S^T columns (after dV has read P^T)
+          if (next) {
+            if (!(ok = mbar_wait(bar(BAR_Q_FULL + ((it + 1) & 1)), ((it + 1) >> 1) & 1, wc))) break;
+            tc_fence_after();
+            mma_kmajor_d(C::kColS, sK, q_addr(it + 1));
+            mma_commit(bar(BAR_S));
+          }
+          // dK_j += dS^T Q_i  and  dQ_i over the dP^T columns
           if (!(ok = mbar_wait(bar(BAR_DS), it & 1, wc))) break;
           tc_fence_after();
 #pragma unroll
@@ -350,7 +367,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                      sdesc_sw128(sK + k * 2048, C::kSubBytes, 1024), idNN, k > 0 ? 1u : 0u);
           }
           mma_commit(bar(BAR_DQ_FULL));
-          mma_commit(bar(BAR_RING_EMPTY + sQ));
+          mma_commit(bar(BAR_Q_EMPTY + (it & 1)));
+          // dP_{i+1} = V_j dO_{i+1}^T over the dP^T columns (after dQ_i has been read out)
+          if (next) {
+            if (!(ok = mbar_wait(bar(BAR_DO_FULL), (it + 1) & 1, wc))) break;
+            if (!(ok = mbar_wait(bar(BAR_DQ_READ), it & 1, wc))) break;
+            tc_fence_after();
+            mma_kmajor_d(C::kColDP, sV, aO);
+            mma_commit(bar(BAR_DP));
+          }
         }
         if (ok) mma_commit(bar(BAR_FINAL));
         mma_commit(bar(BAR_DRAIN));
@@ -360,13 +385,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     regs_alloc<kRegsCompute>();
     // ------------------------------------------------------------ compute warps
-    const int half = warp >> 2;  // query-column half
+    const int grp = warp >> 2;  // warpgroup: query columns 32 grp .. 32 grp + 31
     const int q4 = warp & 3;
     const int r = q4 * 32 + lane;  // key row (S^T, dP^T, dK, dV); head-dim row of dQ^T (d = 128)
     const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
     const int key = j * kTile + r;
     const bool key_ok = key < kv_len;
-    const uint32_t dsrow = sbase + C::kOffP + half * C::kSubBytes + r * 128;
+    // this thread's 32 query columns of dS^T: sub-tile grp / 2, 16-byte chunks 4 (grp & 1) .. +3
+    const uint32_t dsrow = sbase + C::kOffP + (grp >> 1) * C::kSubBytes + r * 128;
     const int swz = r & 7;
     const float2 sl2v = make_float2(a.scale_log2, a.scale_log2);
     const float2 scv = make_float2(a.scale, a.scale);
@@ -374,67 +400,79 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int it = 0; it < nt; ++it) {
       const int i = i0 + it;
       const int sd = it & 1;
-      if (!mbar_wait(bar(BAR_SIDE_FULL + sd), (it >> 1) & 1, wc) || !mbar_wait(bar(BAR_SDP), it & 1, wc)) {
+      if (!mbar_wait(bar(BAR_SIDE_FULL + sd), (it >> 1) & 1, wc) || !mbar_wait(bar(BAR_S), it & 1, wc)) {
         aborted = true;
         break;
       }
       tc_fence_after();
-      const float* lse2 = reinterpret_cast<const float*>(smem + C::kOffSide + sd * 1024) + half * 64;
-      const float* dsum = lse2 + 128;
-      // ---- P^T = exp2(S^T * scale * log2e - LSE2[q]) on this thread's 64 query columns
-      float p[64];
+      const float* nlse2 = reinterpret_cast<const float*>(smem + C::kOffSide + sd * 1024) + grp * 32;  // -LSE2
+      const float* ndsum = nlse2 + 128;                                                                // -D
+      // ---- P^T = exp2(S^T * scale * log2e - LSE2[q]) on this thread's 32 query columns
+      float p[32];
       {
-        float sv[64];
-        tmem_ld64(tmem + lane_off + C::kColS + half * 64, *reinterpret_cast<uint32_t(*)[64]>(sv));
+        uint32_t sv[32];
+        tmem_ld32(tmem + lane_off + C::kColS + grp * 32, sv);
 #pragma unroll
-        for (int c = 0; c < 64; c += 4) {
-          const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c);
-          const float2 x0 = ffma2(make_float2(sv[c], sv[c + 1]), sl2v, make_float2(-l4.x, -l4.y));
-          const float2 x1 = ffma2(make_float2(sv[c + 2], sv[c + 3]), sl2v, make_float2(-l4.z, -l4.w));
+        for (int c = 0; c < 32; c += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(nlse2 + c);
+          const float2 x0 = ffma2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sl2v,
+                                  make_float2(l4.x, l4.y));
+          const float2 x1 = ffma2(make_float2(__uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3])), sl2v,
+                                  make_float2(l4.z, l4.w));
           p[c + 0] = ex2_approx(x0.x);
           p[c + 1] = ex2_approx(x0.y);
           p[c + 2] = ex2_approx(x1.x);
           p[c + 3] = ex2_approx(x1.y);
         }
-        // causal: key > query is masked; queries past N have LSE2 = +inf -> 0
-        const int qlo = i * kTile + half * 64;
+        // causal: key > query is masked; queries past N have -LSE2 = -inf -> 0
+        const int qlo = i * kTile + grp * 32;
         const int first_vis = a.causal ? (key - qlo) : 0;  // columns c >= first_vis are visible
         if (!key_ok || first_vis > 0) {
 #pragma unroll
-          for (int c = 0; c < 64; ++c)
+          for (int c = 0; c < 32; ++c)
             if (!key_ok || c < first_vis) p[c] = 0.f;
         }
       }
       {
-        uint32_t pk[32];
+        uint32_t pk[16];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(p[2 * c], p[2 * c + 1]);
-        tmem_st32(tmem + lane_off + C::kColS + half * 64, pk);  // over this thread's own S^T columns
+        for (int c = 0; c < 16; ++c) pk[c] = pack_bf16x2(p[2 * c], p[2 * c + 1]);
+        tmem_st16(tmem + lane_off + C::kColS + grp * 32, pk);  // over this thread's own S^T columns
         tmem_st_wait();
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(BAR_P));
-      // ---- dS^T = scale * P^T * (dP^T - D[q])  -> shared memory (bf16, K-major for dK, MN-major for dQ)
+      // ---- dS^T = scale * P^T * (dP^T - D[q])  -> shared memory (bf16)
+      if (!mbar_wait(bar(BAR_DP), it & 1, wc)) {
+        aborted = true;
+        break;
+      }
+      tc_fence_after();
       {
-        float dv[64];
-        tmem_ld64(tmem + lane_off + C::kColDP + half * 64, *reinterpret_cast<uint32_t(*)[64]>(dv));
+        uint32_t dv[32];
+        tmem_ld32(tmem + lane_off + C::kColDP + grp * 32, dv);
 #pragma unroll
-        for (int c = 0; c < 64; c += 2) {
-          const float2 d2 = *reinterpret_cast<const float2*>(dsum + c);
-          const float2 ps = fmul2(make_float2(p[c], p[c + 1]), scv);
-          const float2 g = fadd2(make_float2(dv[c], dv[c + 1]), make_float2(-d2.x, -d2.y));
-          const float2 ds = fmul2(ps, g);
-          p[c] = ds.x;
-          p[c + 1] = ds.y;
+        for (int c = 0; c < 32; c += 4) {
+          const float4 d4 = *reinterpret_cast<const float4*>(ndsum + c);
+          const float2 g0 = fadd2(make_float2(__uint_as_float(dv[c]), __uint_as_float(dv[c + 1])), make_float2(d4.x, d4.y));
+          const float2 g1 =
+              fadd2(make_float2(__uint_as_float(dv[c + 2]), __uint_as_float(dv[c + 3])), make_float2(d4.z, d4.w));
+          const float2 ds0 = fmul2(fmul2(make_float2(p[c], p[c + 1]), scv), g0);
+          const float2 ds1 = fmul2(fmul2(make_float2(p[c + 2], p[c + 3]), scv), g1);
+          p[c] = ds0.x;
+          p[c + 1] = ds0.y;
+          p[c + 2] = ds1.x;
+          p[c + 3] = ds1.y;
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(BAR_SIDE_EMPTY + sd));
 #pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8) {
-        st_shared_v4(dsrow + (((c8 ^ swz)) << 4), pack_bf16x2(p[8 * c8 + 0], p[8 * c8 + 1]),
+      for (int c8 = 0; c8 < 4; ++c8) {
+        const int chunk = 4 * (grp & 1) + c8;
+        st_shared_v4(dsrow + (((chunk ^ swz)) << 4), pack_bf16x2(p[8 * c8 + 0], p[8 * c8 + 1]),
                      pack_bf16x2(p[8 * c8 + 2], p[8 * c8 + 3]), pack_bf16x2(p[8 * c8 + 4], p[8 * c8 + 5]),
                      pack_bf16x2(p[8 * c8 + 6], p[8 * c8 + 7]));
       }
@@ -448,66 +486,69 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       if constexpr (D == 128) {
-        // dQ^T: lane = head-dim index r, columns = this half's 64 queries; a warp
-        // reduces 32 consecutive floats of one dQ row per instruction
-        uint32_t rr[64];
-        tmem_ld64(tmem + lane_off + C::kColDQ + half * 64, rr);
-        const int q0 = i * kTile + half * 64;
+        // dQ^T: lane = head-dim index r, columns = this warpgroup's 32 queries;
+        // each reduction instruction of the warp covers 32 consecutive floats of one row
+        uint32_t rr[32];
+        tmem_ld32(tmem + lane_off + C::kColDQ + grp * 32, rr);
+        const int q0 = i * kTile + grp * 32;
         float* col = a.dQacc + (static_cast<size_t>(bh) * N + q0) * D + r;
-        const int nrow = min(64, N - q0);
+        if (q0 + 32 <= N) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c)
-          if (c < nrow) red_add_f32(col + static_cast<size_t>(c) * D, __uint_as_float(rr[c]));
+          for (int c = 0; c < 32; ++c) red_add_f32(col + c * D, __uint_as_float(rr[c]));
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (q0 + c < N) red_add_f32(col + c * D, __uint_as_float(rr[c]));
+        }
       } else {
-        // dQ: lane = query row r, columns = this half's D/2 head-dim entries
+        // dQ: lane = query row r, columns = this warpgroup's 16 head-dim entries
         const int qrow = i * kTile + r;
-        float* dst = a.dQacc + (static_cast<size_t>(bh) * N + qrow) * D + half * (D / 2);
+        uint32_t rr[16];
+        tmem_ld16(tmem + lane_off + C::kColDQ + grp * 16, rr);
+        if (qrow < N) {
+          float* dst = a.dQacc + (static_cast<size_t>(bh) * N + qrow) * D + grp * 16;
 #pragma unroll
-        for (int c0 = 0; c0 < D / 2; c0 += 32) {
-          uint32_t rr[32];
-          tmem_ld32(tmem + lane_off + C::kColDQ + half * (D / 2) + c0, rr);
-          if (qrow < N) {
-#pragma unroll
-            for (int c = 0; c < 32; c += 4)
-              red_add_v4(dst + c0 + c, __uint_as_float(rr[c]), __uint_as_float(rr[c + 1]), __uint_as_float(rr[c + 2]),
-                         __uint_as_float(rr[c + 3]));
-          }
+          for (int c = 0; c < 16; c += 4)
+            red_add_v4(dst + c, __uint_as_float(rr[c]), __uint_as_float(rr[c + 1]), __uint_as_float(rr[c + 2]),
+                       __uint_as_float(rr[c + 3]));
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(BAR_DQ_READ));
     }
-    // ---- epilogue: dV_j, dK_j rows (thread = key row r), this warp's column half
+    // ---- epilogue: dV_j, dK_j rows (thread = key row r), head-dim columns of this warpgroup
     if (!aborted) {
       const bool have = nt > 0;
       if (have && !mbar_wait(bar(BAR_FINAL), 0, wc)) aborted = true;
       if (!aborted) {
         tc_fence_after();
+        constexpr int kCols = D / 4;
         const bool in_range = key < N;
-        const size_t rowoff = (static_cast<size_t>(bh) * N + key) * D + half * (D / 2);
+        const size_t rowoff = (static_cast<size_t>(bh) * N + key) * D + grp * kCols;
 #pragma unroll
         for (int which = 0; which < 2; ++which) {
           uint8_t* out = static_cast<uint8_t*>(which ? a.dK : a.dV) + rowoff * 2;
-          const uint32_t col = (which ? C::kColDK : C::kColDV) + half * (D / 2);
-#pragma unroll
-          for (int c0 = 0; c0 < D / 2; c0 += 32) {
-            uint32_t rr[32];
-            if (have) {
-              tmem_ld32(tmem + lane_off + col + c0, rr);
+          const uint32_t col = (which ? C::kColDK : C::kColDV) + grp * kCols;
+          uint32_t rr[kCols];
+          if (have) {
+            if constexpr (kCols == 32) {
+              tmem_ld32(tmem + lane_off + col, rr);
             } else {
-#pragma unroll
-              for (int c = 0; c < 32; ++c) rr[c] = 0u;
+              tmem_ld16(tmem + lane_off + col, rr);
             }
-            if (in_range) {
-              uint4* dst = reinterpret_cast<uint4*>(out + c0 * 2);
+          } else {
 #pragma unroll
-              for (int q = 0; q < 4; ++q)
-                dst[q] = make_uint4(pack_bf16x2(__uint_as_float(rr[8 * q + 0]), __uint_as_float(rr[8 * q + 1])),
-                                    pack_bf16x2(__uint_as_float(rr[8 * q + 2]), __uint_as_float(rr[8 * q + 3])),
-                                    pack_bf16x2(__uint_as_float(rr[8 * q + 4]), __uint_as_float(rr[8 * q + 5])),
-                                    pack_bf16x2(__uint_as_float(rr[8 * q + 6]), __uint_as_float(rr[8 * q + 7])));
-            }
+            for (int c = 0; c < kCols; ++c) rr[c] = 0u;
+          }
+          if (in_range) {
+            uint4* dst = reinterpret_cast<uint4*>(out);
+#pragma unroll
+            for (int q = 0; q < kCols / 8; ++q)
+              dst[q] = make_uint4(pack_bf16x2(__uint_as_float(rr[8 * q + 0]), __uint_as_float(rr[8 * q + 1])),
+                                  pack_bf16x2(__uint_as_float(rr[8 * q + 2]), __uint_as_float(rr[8 * q + 3])),
+                                  pack_bf16x2(__uint_as_float(rr[8 * q + 4]), __uint_as_float(rr[8 * q + 5])),
+                                  pack_bf16x2(__uint_as_float(rr[8 * q + 6]), __uint_as_float(rr[8 * q + 7])));
           }
         }
       }

@@ -23,6 +23,10 @@ unsigned* device_status_ptr();
 bool encode_bf16_tmap(CUtensorMap* map, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
                       const uint32_t* box);
 
+// Encode a tiled fp32 tensor map without swizzle (row-major boxes in shared memory).
+bool encode_f32_tmap(CUtensorMap* map, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
+                     const uint32_t* box);
+
 inline int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
 
 inline fa_status launch_status() {
