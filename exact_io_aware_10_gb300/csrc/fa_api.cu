@@ -197,6 +197,7 @@ int fa_get_device_status(void* stream) {
     const unsigned zero = 0;
     if (cudaMemcpyToSymbol(fa::g_fa_status, &zero, sizeof(zero)) != cudaSuccess) return FA_ERR_CUDA;
   }
+  if (v & fa::kStatusLaunchBit) return FA_ERR_CUDA;
   if (v & fa::kStatusTimeoutBit) return FA_ERR_TIMEOUT;
   if (v & fa::kStatusBadTableBit) return FA_ERR_BAD_BLOCK_TABLE;
   return FA_OK;

@@ -22,9 +22,10 @@
 //                        dQ_i   = dS K_j           (d = 64: lanes = queries, over dP^T)
 //                      MMA order per tile: dV_i, S_{i+1}, dK_i, dQ_i, dP_{i+1}, so
 //                      the next tile's scores are ready while dS_i is formed.
-//                      dQ_i is added into the fp32 accumulator with reductions
-//                      in L2; at d = 128 one warp instruction covers 32
-//                      consecutive floats of a dQ row.
+//                      dQ_i is added into the fp32 accumulator in L2: at
+//                      d = 128 by one TMA bulk reduction of a 128 x 32 box per
+//                      compute warpgroup, staged in shared memory, at d = 64 by
+//                      vector reductions.
 //  3. bwd_dq_kernel    dQ = bf16(dQacc).
 //
 // Roles of the main kernel (20 warps = 5 warpgroups): warps 0-15 compute
@@ -59,9 +60,16 @@ struct BwdCfg {
   static constexpr int kOffV = kOffK + kTileBytes;
   static constexpr int kOffP = kOffV + kTileBytes;  // dS^T (bf16, 128 x 128)
   static constexpr int kOffRing = kOffP + kPBytes;  // Q slots 0-1, then the dO slot
-  static constexpr int kOffSide = kOffRing + kSlots * kTileBytes;  // 2 x (LSE2[128], D[128])
+  // dQ staging for the TMA reductions, 16 KB (32 queries x 128 fp32) per compute
+  // warpgroup: warpgroups 0-1 here, 2-3 in the dS^T buffer (idle while dQ is
+  // read out)
+  static constexpr int kOffStage = kOffRing + kSlots * kTileBytes;
+  static constexpr int kStageBytes = (D == 128) ? 2 * 16384 : 0;
+  static constexpr int kOffSide = kOffStage + kStageBytes;  // 2 x (-LSE2[128], -D[128])
   static constexpr int kOffBar = kOffSide + 2 * 1024;
-  static constexpr int kSmemBytes = kOffBar + 256 + 1024;
+  static constexpr int kUsedBytes = kOffBar + 256;
+  static constexpr int kSmemBytes = (kUsedBytes + 1024 <= 232448) ? kUsedBytes + 1024 : 232448;
+  static constexpr int kMaxPad = kSmemBytes - kUsedBytes;  // alignment padding the allocation can absorb
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D, kColDQ = 128;
 };
@@ -113,10 +121,6 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
                : "memory");
-}
-
-__device__ __forceinline__ void red_add_f32(float* addr, float v) {
-  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
 }
 
 __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
@@ -191,9 +195,17 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                    const BwdArgs a) {
+                    const __grid_constant__ CUtensorMap tmdQ, const BwdArgs a) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
+  {
+    // the tiles need a 1024-byte aligned base; refuse (and report) rather than overrun
+    const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+    if (pad > static_cast<uint32_t>(C::kMaxPad)) {
+      if (threadIdx.x == 0) atomicOr(a.status, kStatusLaunchBit);
+      return;
+    }
+  }
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   const uint32_t barbase = sbase + C::kOffBar;
@@ -469,6 +481,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(BAR_SIDE_EMPTY + sd));
+      if constexpr (D == 128) {
+        // the previous tile's dQ reductions of warpgroups 2-3 read staging inside
+        // the dS^T buffer: their reads must be done before any warp overwrites it
+        if (it > 0) {
+          if (grp >= 2 && q4 == 0 && lane == 0) bulk_wait_read_all();
+          named_barrier_sync(1, 32 * kComputeWarps);
+        }
+      }
 #pragma unroll
       for (int c8 = 0; c8 < 4; ++c8) {
         const int chunk = 4 * (grp & 1) + c8;
@@ -486,20 +506,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       if constexpr (D == 128) {
-        // dQ^T: lane = head-dim index r, columns = this warpgroup's 32 queries;
-        // each reduction instruction of the warp covers 32 consecutive floats of one row
+        // dQ^T: lane = head-dim index r, columns = this warpgroup's 32 queries.
+        // The TMEM columns are released as soon as the values are in registers;
+        // the warpgroup then stages its 32 x 128 fp32 box (row-major) and one
+        // thread adds it into dQacc with a TMA reduction in L2.
         uint32_t rr[32];
         tmem_ld32(tmem + lane_off + C::kColDQ + grp * 32, rr);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(BAR_DQ_READ));
         const int q0 = i * kTile + grp * 32;
-        float* col = a.dQacc + (static_cast<size_t>(bh) * N + q0) * D + r;
-        if (q0 + 32 <= N) {
+        const uint32_t stg = (grp < 2) ? sbase + C::kOffStage + grp * 16384 : sbase + C::kOffP + (grp - 2) * 16384;
+        const bool leader = (q4 == 0 && lane == 0);
+        if (grp < 2 && it > 0 && leader) bulk_wait_read_all();  // this staging slot's previous reduction
+        named_barrier_sync(2 + grp, 128);
 #pragma unroll
-          for (int c = 0; c < 32; ++c) red_add_f32(col + c * D, __uint_as_float(rr[c]));
-        } else {
-#pragma unroll
-          for (int c = 0; c < 32; ++c)
-            if (q0 + c < N) red_add_f32(col + c * D, __uint_as_float(rr[c]));
+        for (int q = 0; q < 32; ++q) st_shared_f32(stg + q * 512 + r * 4, __uint_as_float(rr[q]));
+        fence_proxy_async_smem();
+        named_barrier_sync(2 + grp, 128);
+        if (leader && q0 < N) {
+          tma_reduce_add_3d(&tmdQ, stg, 0, q0, bh);
+          bulk_commit();
         }
+        continue;  // DQ_READ already signalled
       } else {
         // dQ: lane = query row r, columns = this warpgroup's 16 head-dim entries
         const int qrow = i * kTile + r;
@@ -517,6 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(BAR_DQ_READ));
     }
+    if (lane == 0) bulk_wait_read_all();  // staging must outlive the reductions' reads
     // ---- epilogue: dV_j, dK_j rows (thread = key row r), head-dim columns of this warpgroup
     if (!aborted) {
       const bool have = nt > 0;
@@ -592,10 +622,14 @@ fa_status bwd_launch_d(const void* Q, const void* K, const void* V, const void* 
   const uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(N), static_cast<uint64_t>(BH)};
   const uint64_t strides[2] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(N) * D * 2};
   const uint32_t box[3] = {64, kTile, 1};
-  CUtensorMap tq, tk, tv, tdo;
+  CUtensorMap tq, tk, tv, tdo, tdq;
   if (!encode_bf16_tmap(&tq, Q, 3, dims, strides, box) || !encode_bf16_tmap(&tk, K, 3, dims, strides, box) ||
       !encode_bf16_tmap(&tv, V, 3, dims, strides, box) || !encode_bf16_tmap(&tdo, dO, 3, dims, strides, box))
     return FA_ERR_CUDA;
+  // fp32 dQ accumulator as D (head dim) x 32 (queries) boxes for the TMA reductions
+  const uint64_t qstrides[2] = {static_cast<uint64_t>(D) * 4, static_cast<uint64_t>(N) * D * 4};
+  const uint32_t qbox[3] = {static_cast<uint32_t>(D), 32, 1};
+  if (!encode_f32_tmap(&tdq, a.dQacc, 3, dims, qstrides, qbox)) return FA_ERR_CUDA;
   static bool attr_set = false;
   if (!attr_set) {
     if (cudaFuncSetAttribute(bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
@@ -607,7 +641,7 @@ fa_status bwd_launch_d(const void* Q, const void* K, const void* V, const void* 
   bwd_pre_kernel<D><<<static_cast<unsigned>((pre_rows + 7) / 8), 256, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), LSE, a, BH);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
-  bwd_main_kernel<D><<<dim3(nq, BH), kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, a);
+  bwd_main_kernel<D><<<dim3(nq, BH), kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, a);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   const long long n4 = static_cast<long long>(BH) * N * D / 4;
   bwd_dq_kernel<<<static_cast<unsigned>((n4 + 255) / 256), 256, 0, stream>>>(a.dQacc,

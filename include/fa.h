@@ -168,8 +168,9 @@ int fa_paged_decode_noalloc(const void* q, const void* k_cache, const void* v_ca
 
 /*
  * Synchronises `stream`, then returns and clears the device status word of
- * the current device: FA_OK, FA_ERR_TIMEOUT or FA_ERR_BAD_BLOCK_TABLE (the
- * first two bits latched since the last call, timeout first), or FA_ERR_CUDA.
+ * the current device: FA_OK, or the most severe condition latched since the
+ * last call -- FA_ERR_CUDA (a kernel could not set up its shared memory, or the
+ * query itself failed), FA_ERR_TIMEOUT, FA_ERR_BAD_BLOCK_TABLE.
  */
 int fa_get_device_status(void* stream);
 
