@@ -49,6 +49,8 @@ DECODE = dict(B=64, Hq=32, Hkv=8, d=128, L_lo=512, L_hi=32768, block=16, max_blo
 WORKLOAD = ("long-context causal prefill B1 H16 d128 (fwd+bwd N=16384, fwd N=65536) + paged GQA decode "
             "B64 Hq32 Hkv8 d128 L~U[512,32768] block16 splits16")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# GB300 nominal dense figures, the denominators the targets are also stated in
+NOMINAL = {"bf16_tflops": 2250.0, "hbm_gbs": 8000.0}
 # ncu dram bytes (read + write) per launch of the dominant kernel, with the
 # hash of the kernel source they were taken on (null once the source changes)
 TRAFFIC_RECORD = {"kernel": "fwd_kernel<128>", "source": "exact_io_aware_10_gb300/csrc/fa_fwd.cu",
@@ -299,11 +301,20 @@ def run_ours(args):
     def tf(p):
         return K * flops[p] / (part_ms[p] * 1e-3) / 1e12
 
+    def tf_part(p):
+        v = tf(p)
+        return {"TFLOP/s": v, "frac": v / peak_tf, "frac_of_nominal": v / NOMINAL["bf16_tflops"],
+                "ms": part_ms[p] / K}
+
     parts = {
-        "fwd_N16384": {"TFLOP/s": tf("fwd16"), "frac": tf("fwd16") / peak_tf, "ms": part_ms["fwd16"] / K},
-        "bwd_N16384": {"TFLOP/s": tf("bwd16"), "frac": tf("bwd16") / peak_tf, "ms": part_ms["bwd16"] / K},
-        "fwd_N65536": {"TFLOP/s": tf("fwd64"), "frac": tf("fwd64") / peak_tf, "ms": part_ms["fwd64"] / K},
-        "decode": {"GB/s": dec_gbs / world, "frac": dec_gbs / world / peak_hbm, "ms": part_ms["decode"] / K},
+        "fwd_N16384": tf_part("fwd16"),
+        "bwd_N16384": tf_part("bwd16"),
+        "fwd_N65536": tf_part("fwd64"),
+        "decode": {"GB/s": dec_gbs / world, "frac": dec_gbs / world / peak_hbm,
+                   "frac_of_nominal": dec_gbs / world / NOMINAL["hbm_gbs"], "ms": part_ms["decode"] / K},
+        "denominators": {"measured_bf16_tflops": peak_tf, "measured_hbm_gbs": peak_hbm,
+                         "nominal_bf16_tflops": NOMINAL["bf16_tflops"], "nominal_hbm_gbs": NOMINAL["hbm_gbs"],
+                         "source": peak_src},
     }
 
     # roofline of the dominant kernel: the forward kernel (one launch per fa_fwd call)
@@ -322,6 +333,7 @@ def run_ours(args):
                 "unit": "TFLOP/s", "frac": achieved / peak_tf, "traffic": traffic,
                 "peak_source": f"{peak_src} bf16_tflops (burst)",
                 "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
+                "frac_of_nominal": achieved / NOMINAL["bf16_tflops"],
                 "launches_per_step": 2, "flops_per_step": fwd_flops_step}
 
     # end to end: the same parts through the C ABI with pinned host buffers,

@@ -9,8 +9,8 @@
 //  1. bwd_pre_kernel   -D_i = -sum_c dO_ic O_ic and -LSE_i * log2(e) into padded
 //                      fp32 rows (0 / -inf past N), and dQacc <- 0.
 //  2. bwd_main_kernel  one CTA per (128-key tile j, batch*head); the grid runs
-//                      head by head so the CTAs in flight share one head's Q,
-//                      dO and dQ accumulator in L2.  K_j and V_j stay in shared
+//                      over groups of four heads so the CTAs in flight share a
+//                      few heads' Q, dO and dQ accumulator in L2.  K_j and V_j stay in shared
 //                      memory; the CTA streams the query tiles i that see
 //                      tile j and, per tile, runs five tcgen05 MMAs with fp32
 //                      accumulators in TMEM:
@@ -95,6 +95,7 @@ enum : int {
 constexpr int kOffTmemSlot = kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 4;
 constexpr int kComputeWarps = 16;
+constexpr int kHeadGroup = 4;  // heads whose CTAs are interleaved in the grid
 
 struct BwdArgs {
   float* Dpad;      // [BH, Npad] -D, 0 past N
@@ -103,7 +104,7 @@ struct BwdArgs {
   void* dK;         // [BH, N, D] bf16
   void* dV;
   const int32_t* kv_lens;
-  int H, N, Npad, nq;
+  int H, BH, N, Npad, nq;
   int causal;
   float scale;
   float scale_log2;
@@ -215,9 +216,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int bh = blockIdx.y;
+  // grid: y = group of kHeadGroup heads, x = key tile * kHeadGroup + head in
+  // group: the CTAs in flight share a few heads' Q, dO and dQ accumulator in L2,
+  // and within a group the key tiles with most query tiles (causal) start first
+  const int bh = blockIdx.y * kHeadGroup + static_cast<int>(blockIdx.x % kHeadGroup);
+  if (bh >= a.BH) return;
   const int b = bh / a.H;
-  const int j = blockIdx.x;  // key tile; causal: the tiles with most query tiles start first
+  const int j = static_cast<int>(blockIdx.x / kHeadGroup);
   const int N = a.N;
   int kv_len = N;
   if (a.kv_lens != nullptr) kv_len = min(max(a.kv_lens[b], 0), N);
@@ -610,6 +615,7 @@ fa_status bwd_launch_d(const void* Q, const void* K, const void* V, const void* 
   a.dV = dV;
   a.kv_lens = kv_lens;
   a.H = H;
+  a.BH = BH;
   a.N = N;
   a.Npad = Npad;
   a.nq = nq;
@@ -641,7 +647,8 @@ fa_status bwd_launch_d(const void* Q, const void* K, const void* V, const void* 
   bwd_pre_kernel<D><<<static_cast<unsigned>((pre_rows + 7) / 8), 256, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), LSE, a, BH);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
-  bwd_main_kernel<D><<<dim3(nq, BH), kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, a);
+  const dim3 grid(nq * kHeadGroup, ceil_div(BH, kHeadGroup));
+  bwd_main_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, a);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   const long long n4 = static_cast<long long>(BH) * N * D / 4;
   bwd_dq_kernel<<<static_cast<unsigned>((n4 + 255) / 256), 256, 0, stream>>>(a.dQacc,
