@@ -54,8 +54,9 @@ NOMINAL = {"bf16_tflops": 2250.0, "hbm_gbs": 8000.0}
 # ncu dram bytes (read + write) per launch of the dominant kernel, with the
 # hash of the kernel source they were taken on (null once the source changes)
 TRAFFIC_RECORD = {"kernel": "fwd_kernel<128>", "source": "exact_io_aware_10_gb300/csrc/fa_fwd.cu",
-                  "sha256": "931fd1edebd5850635034c29d844fcad7d0ea307b9c17336c0f86681ab749ba9",
-                  "bytes_per_launch_N16384": 554.180096e6 + 60.245248e6, "bytes_per_launch_N65536": None}
+                  "sha256": "d1437597a63a3a755449c92bdebb8a39a44893d7551b18c8aa4bf9e50cfac9d5",
+                  "bytes_per_launch_N16384": 546389504 + 49661952,
+                  "bytes_per_launch_N65536": 7735814656 + 270459136}
 
 
 def load_peaks():
@@ -329,8 +330,16 @@ def run_ours(args):
             traffic = sum(per) / 2.0
         elif per:
             traffic = {"N16384_only": per[0]}
+    P = PREFILL
     roofline = {"kernel": "fwd_kernel<128> (fa_fwd)", "bound": "tensor", "achieved": achieved, "peak": peak_tf,
                 "unit": "TFLOP/s", "frac": achieved / peak_tf, "traffic": traffic,
+                "traffic_detail": None if traffic is None else {
+                    "dram_bytes_N16384": rec["bytes_per_launch_N16384"],
+                    "dram_bytes_N65536": rec["bytes_per_launch_N65536"],
+                    "compulsory_bytes_N16384": acc.fwd_bytes(P["B"], P["H"], P["N_fb"], P["d"]),
+                    "compulsory_bytes_N65536": acc.fwd_bytes(P["B"], P["H"], P["N_f"], P["d"]),
+                    "source": "ncu dram__bytes_read.sum + dram__bytes_write.sum, one launch each "
+                              "(profiles/fwd_kernel_d128_N16384_causal.md)"},
                 "peak_source": f"{peak_src} bf16_tflops (burst)",
                 "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
                 "frac_of_nominal": achieved / NOMINAL["bf16_tflops"],
