@@ -10,6 +10,7 @@
 #include <mutex>
 
 #include "fa_internal.h"
+#include "sm103.cuh"
 
 namespace fa {
 
@@ -89,6 +90,21 @@ bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, CUtensorMapSwizzle
   return r == CUDA_SUCCESS;
 }
 }  // namespace
+
+// One CTA waits on an mbarrier that nothing ever completes; the bounded wait
+// must give up after `timeout_ns`, latch the timeout bit and let the kernel end.
+__global__ void selftest_wait_kernel(unsigned* status, unsigned long long timeout_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  WaitCtx wc{&abort_flag, status, timeout_ns};
+  (void)mbar_wait(smem_u32(&bar), 0, wc);
+}
 
 }  // namespace fa
 
@@ -187,6 +203,15 @@ int fa_paged_decode(const void* q, const void* k_cache, const void* v_cache, con
   if (ws_bytes < fa_paged_decode_workspace_size(B, Hq, d, S)) return FA_ERR_INVALID_ARG;
   return fa::decode_launch(q, k_cache, v_cache, block_table, seq_lens, o, lse, B, Hq, Hkv, d, block_size, max_blocks,
                            num_blocks, S, scale, workspace, static_cast<cudaStream_t>(stream));
+}
+
+int fa_selftest_wait_timeout(unsigned timeout_us, void* stream) {
+  if (timeout_us == 0 || timeout_us > 1000000u) return FA_ERR_INVALID_ARG;
+  unsigned* status = fa::device_status_ptr();
+  if (status == nullptr) return FA_ERR_CUDA;
+  fa::selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      status, static_cast<unsigned long long>(timeout_us) * 1000ull);
+  return fa::launch_status();
 }
 
 int fa_get_device_status(void* stream) {

@@ -63,6 +63,7 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
 struct WaitCtx {
   volatile int* abort_flag;  // shared memory
   unsigned* status;          // global device status word
+  unsigned long long timeout_ns = kWaitTimeoutNs;
 };
 
 static __device__ __forceinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, WaitCtx ctx) {
@@ -71,7 +72,7 @@ static __device__ __forceinline__ bool mbar_wait_slow(uint32_t bar, uint32_t par
     if (mbar_test(bar, parity)) return true;
     if ((i & 63u) == 0) {
       if (*ctx.abort_flag) return false;
-      if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+      if (global_timer_ns() - t0 > ctx.timeout_ns) {
         *ctx.abort_flag = 1;
         atomicOr(ctx.status, kStatusTimeoutBit);
         return false;

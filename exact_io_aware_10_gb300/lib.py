@@ -36,6 +36,7 @@ SIGNATURES = {
     "fa_paged_decode_workspace_size": (_sz, [_i, _i, _i, _i]),
     "fa_paged_decode": (_i, [_vp] * 7 + [_i] * 8 + [_f, _vp, _sz, _vp]),
     "fa_get_device_status": (_i, [_vp]),
+    "fa_selftest_wait_timeout": (_i, [ctypes.c_uint, _vp]),
     "fa_paged_decode_noalloc": (_i, [_vp] * 7 + [_i] * 8 + [_f, _vp]),
 }
 
@@ -222,6 +223,12 @@ def fa_paged_decode_noalloc(q, k_cache, v_cache, block_table, seq_lens, scale=No
                                      _stream(stream))
     _check(st, "fa_paged_decode_noalloc")
     return o, lse
+
+
+def fa_selftest_wait_timeout(timeout_us=20000, stream=None) -> int:
+    """Launch the bounded-wait self-test; returns the launch status (the
+    device result is read with fa_get_device_status)."""
+    return int(load().fa_selftest_wait_timeout(int(timeout_us), _stream(stream)))
 
 
 def fa_get_device_status(stream=None) -> int:

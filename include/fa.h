@@ -167,6 +167,16 @@ int fa_paged_decode_noalloc(const void* q, const void* k_cache, const void* v_ca
                             void* stream);
 
 /*
+ * Self-test of the library's failure detection: launches one CTA that waits on
+ * a pipeline barrier nothing ever completes.  The bounded wait used by every
+ * kernel gives up after `timeout_us` microseconds (1 .. 1,000,000), latches
+ * FA_ERR_TIMEOUT in the device status word and the kernel ends normally; the
+ * CUDA context stays usable.  Read the result with fa_get_device_status().
+ * (Not an operation of the pages; it checks this library's error path.)
+ */
+int fa_selftest_wait_timeout(unsigned timeout_us, void* stream);
+
+/*
  * Synchronises `stream`, then returns and clears the device status word of
  * the current device: FA_OK, or the most severe condition latched since the
  * last call -- FA_ERR_CUDA (a kernel could not set up its shared memory, or the

@@ -96,3 +96,9 @@ def test_decode_argument_validation(so):
     assert call(bs=32) == fl.FA_ERR_UNSUPPORTED
     assert call(S=17) == fl.FA_ERR_UNSUPPORTED
     assert call(nb=0) == fl.FA_ERR_INVALID_ARG
+
+
+def test_selftest_argument_validation(so):
+    s = ctypes.c_void_p(0)
+    assert so.fa_selftest_wait_timeout(0, s) == fl.FA_ERR_INVALID_ARG
+    assert so.fa_selftest_wait_timeout(2000000, s) == fl.FA_ERR_INVALID_ARG
