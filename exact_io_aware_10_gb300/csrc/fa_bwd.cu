@@ -318,13 +318,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t sK = sbase + C::kOffK, sV = sbase + C::kOffV, sP = sbase + C::kOffP;
         auto q_addr = [&](int it) { return sbase + C::kOffRing + (it & 1) * C::kTileBytes; };
         const uint32_t aO = sbase + C::kOffRing + 2 * C::kTileBytes;
+        // Descriptors are built once per operand tile (K-major and MN-major views)
+        // and advanced by immediates, so the issuing thread keeps the tensor pipe fed.
+        const uint64_t kK = sdesc_sw128(sK, 16, 1024), kV = sdesc_sw128(sV, 16, 1024);
+        const uint64_t kP = sdesc_sw128(sP, 16, 1024), kO = sdesc_sw128(aO, 16, 1024);
+        const uint64_t mK = sdesc_sw128(sK, C::kSubBytes, 1024), mP = sdesc_sw128(sP, C::kSubBytes, 1024);
+        const uint64_t mO = sdesc_sw128(aO, C::kSubBytes, 1024);
+        const uint64_t kQ0 = sdesc_sw128(q_addr(0), 16, 1024), mQ0 = sdesc_sw128(q_addr(0), C::kSubBytes, 1024);
+        auto kq = [&](int it) { return sdesc_advance(kQ0, (it & 1) * C::kTileBytes); };
+        auto mq = [&](int it) { return sdesc_advance(mQ0, (it & 1) * C::kTileBytes); };
         // A and B both K-major, K extent = D (head dim)
-        auto mma_kmajor_d = [&](uint32_t dcol, uint32_t a0, uint32_t b0) {
+        auto mma_kmajor_d = [&](uint32_t dcol, uint64_t da, uint64_t db) {
 #pragma unroll
           for (int k = 0; k < D / 16; ++k) {
             const uint32_t off = (k >> 2) * C::kSubBytes + (k & 3) * 32;
-            mma_ss(tmem + dcol, sdesc_sw128(a0 + off, 16, 1024), sdesc_sw128(b0 + off, 16, 1024), idSS,
-                   k > 0 ? 1u : 0u);
+            mma_ss(tmem + dcol, sdesc_advance(da, off), sdesc_advance(db, off), idSS, k > 0 ? 1u : 0u);
           }
         };
         bool ok = mbar_wait(bar(BAR_KV), 0, wc);
@@ -332,17 +340,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) ok = mbar_wait(bar(BAR_Q_FULL + 0), 0, wc);
         if (ok) {
           tc_fence_after();
-          mma_kmajor_d(C::kColS, sK, q_addr(0));
+          mma_kmajor_d(C::kColS, kK, kq(0));
           mma_commit(bar(BAR_S));
           ok = mbar_wait(bar(BAR_DO_FULL), 0, wc);
         }
         if (ok) {
           tc_fence_after();
-          mma_kmajor_d(C::kColDP, sV, aO);
+          mma_kmajor_d(C::kColDP, kV, kO);
           mma_commit(bar(BAR_DP));
         }
         for (int it = 0; ok && it < nt; ++it) {
-          const uint32_t aQ = q_addr(it);
           const bool next = it + 1 < nt;
           // dV_j += P^T dO_i  (P^T packed bf16 in TMEM: warpgroup h's 32 queries in cols 32h..32h+15)
           if (!(ok = mbar_wait(bar(BAR_P), it & 1, wc))) break;
@@ -350,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int k = 0; k < kTile / 16; ++k) {
             const uint32_t acol = 32 * (k >> 1) + 8 * (k & 1);
-            mma_ts(tmem + C::kColDV, tmem + C::kColS + acol, sdesc_sw128(aO + k * 2048, C::kSubBytes, 1024), idKN,
+            mma_ts(tmem + C::kColDV, tmem + C::kColS + acol, sdesc_advance(mO, k * 2048), idKN,
                    (it > 0 || k > 0) ? 1u : 0u);
           }
           mma_commit(bar(BAR_DO_EMPTY));
@@ -358,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (next) {
             if (!(ok = mbar_wait(bar(BAR_Q_FULL + ((it + 1) & 1)), ((it + 1) >> 1) & 1, wc))) break;
             tc_fence_after();
-            mma_kmajor_d(C::kColS, sK, q_addr(it + 1));
+            mma_kmajor_d(C::kColS, kK, kq(it + 1));
             mma_commit(bar(BAR_S));
           }
           // dK_j += dS^T Q_i  and  dQ_i over the dP^T columns
@@ -367,21 +374,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int k = 0; k < kTile / 16; ++k) {
             const uint32_t aoff = (k >> 2) * C::kSubBytes + (k & 3) * 32;
-            mma_ss(tmem + C::kColDK, sdesc_sw128(sP + aoff, 16, 1024), sdesc_sw128(aQ + k * 2048, C::kSubBytes, 1024),
-                   idKN, (it > 0 || k > 0) ? 1u : 0u);
+            mma_ss(tmem + C::kColDK, sdesc_advance(kP, aoff), sdesc_advance(mq(it), k * 2048), idKN,
+                   (it > 0 || k > 0) ? 1u : 0u);
           }
           if constexpr (D == 128) {
             constexpr uint32_t idQT = idesc_bf16_f32(128, 128, true, true);  // A = K^T, B = dS^T
 #pragma unroll
             for (int k = 0; k < kTile / 16; ++k)
-              mma_ss(tmem + C::kColDQ, sdesc_sw128(sK + k * 2048, C::kSubBytes, 1024),
-                     sdesc_sw128(sP + k * 2048, C::kSubBytes, 1024), idQT, k > 0 ? 1u : 0u);
+              mma_ss(tmem + C::kColDQ, sdesc_advance(mK, k * 2048), sdesc_advance(mP, k * 2048), idQT,
+                     k > 0 ? 1u : 0u);
           } else {
             constexpr uint32_t idNN = idesc_bf16_f32(128, D, true, true);  // A = dS, B = K
 #pragma unroll
             for (int k = 0; k < kTile / 16; ++k)
-              mma_ss(tmem + C::kColDQ, sdesc_sw128(sP + k * 2048, C::kSubBytes, 1024),
-                     sdesc_sw128(sK + k * 2048, C::kSubBytes, 1024), idNN, k > 0 ? 1u : 0u);
+              mma_ss(tmem + C::kColDQ, sdesc_advance(mP, k * 2048), sdesc_advance(mK, k * 2048), idNN,
+                     k > 0 ? 1u : 0u);
           }
           mma_commit(bar(BAR_DQ_FULL));
           mma_commit(bar(BAR_Q_EMPTY + (it & 1)));
@@ -390,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(ok = mbar_wait(bar(BAR_DO_FULL), (it + 1) & 1, wc))) break;
             if (!(ok = mbar_wait(bar(BAR_DQ_READ), it & 1, wc))) break;
             tc_fence_after();
-            mma_kmajor_d(C::kColDP, sV, aO);
+            mma_kmajor_d(C::kColDP, kV, kO);
             mma_commit(bar(BAR_DP));
           }
         }

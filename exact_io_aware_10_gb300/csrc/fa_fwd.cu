@@ -198,25 +198,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && nmax > 0) {
       constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idPV = idesc_bf16_f32(128, D, false, true);
+      // Descriptors are built once per operand tile and advanced by immediates,
+      // so the single issuing thread keeps the tensor pipe fed.
+      const uint64_t dQ0 = sdesc_sw128(sbase + C::kOffQ, 16, 1024);
+      const uint64_t dKV0 = sdesc_sw128(sbase + C::kOffKV, 16, 1024);            // K-major view of slot 0
+      const uint64_t dV0 = sdesc_sw128(sbase + C::kOffKV, C::kSubBytes, 1024);  // MN-major view of slot 0
       auto issue_S = [&](int t, int slot) {
-        const uint32_t a0 = sbase + C::kOffQ + t * C::kTileBytes;
-        const uint32_t b0 = sbase + C::kOffKV + slot * C::kTileBytes;
+        const uint64_t da = sdesc_advance(dQ0, t * C::kTileBytes);
+        const uint64_t db = sdesc_advance(dKV0, slot * C::kTileBytes);
+        const uint32_t dcol = tmem + C::col_s(t);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k >> 2) * C::kSubBytes + (k & 3) * 32;
-          mma_ss(tmem + C::col_s(t), sdesc_sw128(a0 + off, 16, 1024), sdesc_sw128(b0 + off, 16, 1024), idS,
-                 k > 0 ? 1u : 0u);
+          mma_ss(dcol, sdesc_advance(da, off), sdesc_advance(db, off), idS, k > 0 ? 1u : 0u);
         }
       };
       // A = P in TMEM: row = lane, 16 keys per MMA = 8 columns of packed bf16 pairs
       auto issue_PV = [&](int t, int slot, bool acc) {
-        const uint32_t b0 = sbase + C::kOffKV + slot * C::kTileBytes;
+        const uint64_t db = sdesc_advance(dV0, slot * C::kTileBytes);
+        const uint32_t dcol = tmem + C::col_o(t), acol = tmem + C::col_s(t);
 #pragma unroll
-        for (int k = 0; k < kKeys / 16; ++k) {
-          const uint32_t boff = k * 16 * 128;
-          mma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + 8 * k, sdesc_sw128(b0 + boff, C::kSubBytes, 1024), idPV,
-                 (acc || k > 0) ? 1u : 0u);
-        }
+        for (int k = 0; k < kKeys / 16; ++k)
+          mma_ts(dcol, acol + 8 * k, sdesc_advance(db, k * 16 * 128), idPV, (acc || k > 0) ? 1u : 0u);
       };
       bool ok = mbar_wait(bar(BAR_Q), 0, wc);
       if (ok) ok = mbar_wait(bar(BAR_KV_FULL + 0), 0, wc);

@@ -195,6 +195,13 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
   return d;
 }
 
+// A descriptor for `base + off` equals the descriptor for `base` plus off >> 4:
+// the start-address field holds address >> 4 in 14 bits, and shared-memory
+// addresses stay below 256 KB, so the addition never carries out of it.
+__device__ __forceinline__ uint64_t sdesc_advance(uint64_t desc, uint32_t off_bytes) {
+  return desc + static_cast<uint64_t>(off_bytes >> 4);
+}
+
 // TMEM loads: 32 lanes x 32-bit, one lane (row) per thread, consecutive
 // columns per register.  The wait is part of the same statement so no use of
 // the destination registers can be scheduled before the data has arrived.
