@@ -30,6 +30,7 @@ from .attention import (  # noqa: F401
     attention_probs,
     attention_forward,
     attention_forward_rows,
+    attention_forward_varlen,
     attention_backward,
     streaming_row_forward,
     algorithm1_forward,

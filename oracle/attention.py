@@ -265,3 +265,26 @@ def merge_states(ms, ls, os_):
     l = (w * ls).sum()
     o = (w[:, None] * os_).sum(axis=0)
     return o / l, m, l
+
+
+def attention_forward_varlen(Q, K, V, cu_seqlens, causal=False, scale=None):
+    """Attention over a packed ragged batch: Q, K, V are [total, H, d] with
+    sequence s occupying rows cu_seqlens[s] .. cu_seqlens[s+1]-1; every
+    sequence is an independent attention problem ([FA-notes] §2.1 applied per
+    sequence; causal masking is top-left within each sequence).
+    Returns O [total, H, d] and LSE [H, total]."""
+    Q, K, V = to_f64(Q), to_f64(K), to_f64(V)
+    cu = np.asarray(cu_seqlens.cpu().numpy() if hasattr(cu_seqlens, "cpu") else cu_seqlens, dtype=np.int64)
+    total, H, d = Q.shape
+    O = np.zeros((total, H, V.shape[2]))
+    LSE = np.full((H, total), NEG_INF)
+    for s in range(len(cu) - 1):
+        a, b = int(cu[s]), int(cu[s + 1])
+        if b <= a:
+            continue
+        # [L, H, d] -> [1, H, L, d]
+        q, k, v = (x[a:b].transpose(1, 0, 2)[None] for x in (Q, K, V))
+        o, lse = attention_forward(q, k, v, causal=causal, scale=scale)
+        O[a:b] = o[0].transpose(1, 0, 2)
+        LSE[:, a:b] = lse[0]
+    return O, LSE

@@ -368,3 +368,30 @@ def test_materialised_memory_numbers():
     g = json.load(open(os.path.join(GOLDEN, "materialized_memory.json")))
     for c in g["cases"]:
         assert oracle.materialized_matrix_bytes(c["N"], c["bytes_per_elem"], c["n_matrices"], c["heads"]) == c["bytes"]
+
+
+def test_varlen_oracle_is_per_sequence_attention_and_ignores_neighbours():
+    # each packed sequence equals an isolated problem; changing another
+    # sequence's tokens does not change it (independence of sequences)
+    H, d = 3, 8
+    lens = [5, 1, 17, 9]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    total = int(cu[-1])
+    Q, K, V = (_rand((total, H, d), s) for s in (60, 61, 62))
+    for causal in (False, True):
+        O, L = oracle.attention_forward_varlen(Q, K, V, cu, causal=causal)
+        for s, n in enumerate(lens):
+            a = int(cu[s])
+            # single-sequence closed checks: causal row 0 returns V[0]
+            if causal:
+                np.testing.assert_allclose(O[a], V[a], atol=1e-15)
+            P = oracle.attention_probs(Q[a:a + n].transpose(1, 0, 2)[None], K[a:a + n].transpose(1, 0, 2)[None],
+                                       causal=causal)
+            np.testing.assert_allclose(O[a:a + n].transpose(1, 0, 2), (P[0] @ V[a:a + n].transpose(1, 0, 2)),
+                                       atol=1e-13)
+        K2 = K.copy()
+        K2[int(cu[2]):int(cu[3])] += _rand((lens[2], H, d), 63)  # perturb sequence 2 only
+        O2, _ = oracle.attention_forward_varlen(Q, K2, V, cu, causal=causal)
+        keep = np.r_[0:int(cu[2]), int(cu[3]):total]
+        np.testing.assert_array_equal(O2[keep], O[keep])
+        assert not np.allclose(O2[int(cu[2]):int(cu[3])], O[int(cu[2]):int(cu[3])])
