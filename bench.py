@@ -46,6 +46,13 @@ from exact_io_aware_10_gb300 import workloads as wl  # noqa: E402
 METRIC = "attention fwd/bwd TFLOP/s (% of BF16 peak); paged-decode HBM GB/s (% of peak)"
 PREFILL = dict(B=1, H=16, d=128, N_fb=16384, N_f=65536)
 DECODE = dict(B=64, Hq=32, Hkv=8, d=128, L_lo=512, L_hi=32768, block=16, max_blocks=2048, splits=16)
+# packed ragged-batch forward workloads, timed after the step: the BERT-large-
+# shaped padded configuration's lengths packed without padding, and a long-
+# context causal prefill mix; lengths are uniform integers in [lo, hi]
+VARLEN = {
+    "bert": dict(num_seqs=16, lo=128, hi=512, H=16, d=64, causal=False, config_id=2, padded_N=512),
+    "long": dict(num_seqs=16, lo=512, hi=16384, H=16, d=128, causal=True, config_id=6, padded_N=None),
+}
 WORKLOAD = ("long-context causal prefill B1 H16 d128 (fwd+bwd N=16384, fwd N=65536) + paged GQA decode "
             "B64 Hq32 Hkv8 d128 L~U[512,32768] block16 splits16")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -207,6 +214,73 @@ class Workload:
         return acc.decode_bytes(self.seq_lens_host.tolist(), D["Hq"], D["Hkv"], D["d"], D["block"])
 
 
+class VarlenWorkload:
+    """Device-resident packed inputs of one ragged-batch forward (and, where
+    the mix has a padded form, the same tokens padded for fa_fwd_ex)."""
+
+    def __init__(self, dev, name, seed=0):
+        from exact_io_aware_10_gb300 import lib
+
+        self.lib = lib
+        c = VARLEN[name]
+        self.c = c
+        sd = wl.config_seed(seed, c["config_id"])
+        if c["padded_N"] is not None:
+            lens = wl.padded_lengths(c["num_seqs"], c["lo"], c["hi"], seed=sd).tolist()
+        else:
+            lens = wl.varlen_lengths(c["num_seqs"], c["lo"], c["hi"], seed=sd)
+        self.lengths = lens
+        total = sum(lens)
+        cu = [0]
+        for n in lens:
+            cu.append(cu[-1] + n)
+        self.cu = torch.tensor(cu, dtype=torch.int32, device=dev)
+        shp = (total, c["H"], c["d"])
+        self.Q, self.K, self.V = (wl.device_normal_bf16(shp, sd + 20 + i, dev) for i in range(3))
+        self.O = torch.empty_like(self.Q)
+        self.L = torch.empty((c["H"], total), dtype=torch.float32, device=dev)
+        self.flops = acc.varlen_fwd_flops(lens, c["H"], c["d"], c["causal"])
+        self.padded = None
+        if c["padded_N"] is not None:
+            B, N = len(lens), c["padded_N"]
+            pshp = (B, c["H"], N, c["d"])
+            self.padded = [wl.device_normal_bf16(pshp, sd + 30 + i, dev) for i in range(3)]
+            self.Op = torch.empty_like(self.padded[0])
+            self.Lp = torch.empty(pshp[:3], dtype=torch.float32, device=dev)
+            self.kv = torch.tensor(lens, dtype=torch.int32, device=dev)
+
+    def packed(self):
+        self.lib.fa_fwd_varlen(self.Q, self.K, self.V, self.cu, max(self.lengths), causal=self.c["causal"],
+                               O=self.O, LSE=self.L)
+
+    def padded_fwd(self):
+        self.lib.fa_fwd(*self.padded, causal=self.c["causal"], kv_lens=self.kv, O=self.Op, LSE=self.Lp)
+
+
+def time_varlen(dev, seed, steps, warmup, barrier, max_over_ranks, world, peak_tf):
+    """TFLOP/s of the packed ragged-batch forward on each VARLEN mix (useful
+    FLOPs of the sequences), and of the padded equivalent where there is one."""
+    out = {}
+    for name in VARLEN:
+        v = VarlenWorkload(dev, name, seed)
+        parts = ("packed",) if v.padded is None else ("packed", "padded_fwd")
+        _, ms = time_parts(lambda p: getattr(v, p)(), parts, steps, warmup, barrier)
+        assert v.lib.fa_get_device_status() == v.lib.FA_OK, "device status word reported an error"
+        c = v.c
+        r = {"H": c["H"], "d": c["d"], "causal": c["causal"], "num_seqs": c["num_seqs"],
+             "lengths": f"U[{c['lo']},{c['hi']}]", "total_tokens": sum(v.lengths), "flops": v.flops}
+        for p in parts:
+            t = max_over_ranks(ms[p])
+            tf = world * steps * v.flops / (t * 1e-3) / 1e12
+            key = "packed" if p == "packed" else f"padded_to_{c['padded_N']}"
+            r[key] = {"TFLOP/s": tf, "frac": tf / world / peak_tf, "frac_of_nominal": tf / world / NOMINAL["bf16_tflops"],
+                      "ms": t / steps}
+        out[f"varlen_{name}"] = r
+        del v
+        torch.cuda.empty_cache()
+    return out
+
+
 class HostBuffers:
     """Pinned host copies of a step's inputs and outputs for the end-to-end run."""
 
@@ -359,6 +433,11 @@ def run_ours(args):
            "decode_GB/s": world * e2e_steps * dbytes / (e2e_part["decode"] * 1e-3) / 1e9,
            "ms_per_step": max_over_ranks(e2e_total) / e2e_steps}
 
+    next_rows = None
+    if not args.skip_next_rows:
+        next_rows = time_varlen(dev, args.seed, args.steps, args.warmup, barrier, max_over_ranks, world, peak_tf)
+        next_rows["note"] = "timed after the step, outside value and ms_per_step; TFLOP/s count useful FLOPs only"
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline_sample(args.cpu_seconds)
@@ -374,7 +453,7 @@ def run_ours(args):
             "decode": {"value": dec_gbs, "unit": "GB/s", "frac": dec_gbs / world / peak_hbm,
                        "peak": peak_hbm, "peak_source": f"{peak_src} hbm_gbs", "bytes_per_step": dbytes},
             "parts": parts, "roofline": roofline, "e2e": e2e, "cpu_baseline": cpu,
-            "gpu_launches": K * sum(Workload.LAUNCHES.values()), "clocks": clocks,
+            "gpu_launches": K * sum(Workload.LAUNCHES.values()), "clocks": clocks, "next_rows": next_rows,
         }
         print(json.dumps(line))
     if dist is not None:
@@ -462,6 +541,7 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--skip-next-rows", action="store_true", help="skip the ragged-batch forward timings")
     ap.add_argument("--ref-prefix", type=int, default=2048)
     args = ap.parse_args()
     if args.warmup < 3:

@@ -4,6 +4,8 @@ Conventions (matmul work only; exp, masking and reductions are not counted):
   forward   4 * B * H * N^2 * d     (QK^T and PV, 2 N^2 d each), halved when causal
   backward  2.5 x the forward       (five N^2 d products instead of two)
   key padding: the effective forward count is 4 * H * N * d * sum_b L_b
+  packed ragged batch: the sum of the forward count of every sequence,
+            4 * H * d * sum_s L_s^2, halved when causal
   decode    bytes = K and V of every visible key, read once per KV head
             (sum_b L_b * Hkv * d * 2 B * 2) + q + o + lse + the block-table
             entries and sequence lengths read.
@@ -23,6 +25,10 @@ def bwd_flops(B, H, N, d, causal=False):
 
 def fwd_flops_padded(H, N, d, kv_lens):
     return 4.0 * H * N * d * float(sum(int(x) for x in kv_lens))
+
+
+def varlen_fwd_flops(lengths, H, d, causal=False):
+    return sum(fwd_flops(1, H, int(n), d, causal) for n in lengths)
 
 
 def fwd_bytes(B, H, N, d):

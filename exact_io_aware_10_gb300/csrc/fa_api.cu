@@ -145,7 +145,7 @@ const char* fa_status_string(int status) {
   }
 }
 
-int fa_version(void) { return 100; }
+int fa_version(void) { return 101; }
 
 int fa_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d, int causal,
               float scale, const int32_t* kv_lens, void* stream) {
@@ -157,6 +157,20 @@ int fa_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* LSE, 
 int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d, int causal,
            float scale, void* stream) {
   return fa_fwd_ex(Q, K, V, O, LSE, B, H, N, d, causal, scale, nullptr, stream);
+}
+
+int fa_fwd_varlen(const void* Q, const void* K, const void* V, void* O, float* LSE, const int32_t* cu_seqlens,
+                  int num_seqs, int total, int max_seqlen, int H, int d, int causal, float scale, void* stream) {
+  if (num_seqs < 1 || total < 0 || max_seqlen < 0 || H < 1) return FA_ERR_INVALID_ARG;
+  if (bad_scale(scale)) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (total == 0 || max_seqlen == 0) return FA_OK;
+  if (!Q || !K || !V || !O || !LSE || !cu_seqlens) return FA_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(LSE)) return FA_ERR_INVALID_ARG;
+  if (static_cast<long long>(num_seqs) * H > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  if ((static_cast<long long>(max_seqlen) + 255) / 256 > 65535) return FA_ERR_UNSUPPORTED;
+  return fa::fwd_varlen_launch(Q, K, V, O, LSE, cu_seqlens, num_seqs, total, max_seqlen, H, d, causal, scale,
+                               static_cast<cudaStream_t>(stream));
 }
 
 size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
@@ -223,6 +237,7 @@ int fa_get_device_status(void* stream) {
     if (cudaMemcpyToSymbol(fa::g_fa_status, &zero, sizeof(zero)) != cudaSuccess) return FA_ERR_CUDA;
   }
   if (v & fa::kStatusLaunchBit) return FA_ERR_CUDA;
+  if (v & fa::kStatusBadArgBit) return FA_ERR_INVALID_ARG;
   if (v & fa::kStatusTimeoutBit) return FA_ERR_TIMEOUT;
   if (v & fa::kStatusBadTableBit) return FA_ERR_BAD_BLOCK_TABLE;
   return FA_OK;

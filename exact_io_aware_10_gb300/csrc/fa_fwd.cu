@@ -78,6 +78,10 @@ struct FwdArgs {
   void* O;
   float* LSE;
   const int32_t* kv_lens;
+  // packed ragged batch: Q/K/V/O are [total, H, D], LSE is [H, total] and
+  // sequence s owns tokens cu_seqlens[s] .. cu_seqlens[s+1]-1 (nullptr: dense)
+  const int32_t* cu_seqlens;
+  int total;
   int H, N;
   int causal;
   float scale_log2;  // scale * log2(e)
@@ -108,19 +112,38 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int bh = blockIdx.x;
+  const int bh = blockIdx.x;  // dense: batch * H + head; packed: sequence * H + head
   const int b = bh / args.H;
   const int mblk = gridDim.y - 1 - blockIdx.y;  // longest causal work first
   const int N = args.N;
+  const bool packed = args.cu_seqlens != nullptr;
+  const int head = bh % args.H;
 
-  int kv_len = N;
-  if (args.kv_lens != nullptr) kv_len = min(max(args.kv_lens[b], 0), N);
+  // rows of this (sequence, head): Lq query rows; keys are the same rows, the
+  // first kv_len of them visible; tok0 = first token of the sequence (packed)
+  int Lq = N, kv_len = N, tok0 = 0;
+  if (packed) {
+    tok0 = args.cu_seqlens[b];
+    const int tok1 = args.cu_seqlens[b + 1];
+    // offsets must be non-decreasing within [0, total], and no sequence may be
+    // longer than the max_seqlen the grid covers; otherwise nothing is written
+    // for this sequence and the status word records the bad argument
+    if (tok0 < 0 || tok1 < tok0 || tok1 > args.total || tok1 - tok0 > static_cast<int>(gridDim.y) * 2 * kRows) {
+      if (blockIdx.y == 0 && threadIdx.x == 0) atomicOr(args.status, kStatusBadArgBit);
+      return;
+    }
+    Lq = tok1 - tok0;
+    kv_len = Lq;
+  } else if (args.kv_lens != nullptr) {
+    kv_len = min(max(args.kv_lens[b], 0), N);
+  }
+  if (packed && 2 * mblk * kRows >= Lq) return;  // whole CTA past this sequence's end
   int n_t[2];
   bool valid_t[2];
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
     const int qt = 2 * mblk + t;
-    valid_t[t] = qt * kRows < N;
+    valid_t[t] = qt * kRows < Lq;
     int end = kv_len;
     if (args.causal) end = min(end, qt * kRows + kRows);
     n_t[t] = valid_t[t] ? (end + kKeys - 1) / kKeys : 0;
@@ -161,6 +184,14 @@ __global__ void __launch_bounds__(kThreads, 1)
    regs_dealloc<kRegsOther>();
    if (warp == 8) {
     // ------------------------------------------------------------ producer
+    // TMA coordinates of 128 rows starting at `row`: dense maps are (d, N, B*H),
+    // packed maps are (d, H, total)
+    auto load_rows = [&](uint32_t dst, const CUtensorMap* tm, uint32_t mb, int x, int row) {
+      if (packed)
+        tma_load_3d(dst, tm, mb, x, head, tok0 + row);
+      else
+        tma_load_3d(dst, tm, mb, x, row, bh);
+    };
     if (lane == 0) {
       uint32_t qbytes = 0;
       for (int t = 0; t < 2; ++t)
@@ -170,8 +201,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < 2; ++t) {
           if (!valid_t[t]) continue;
           for (int s = 0; s < C::kSub; ++s)
-            tma_load_3d(sbase + C::kOffQ + t * C::kTileBytes + s * C::kSubBytes, &tmQ, bar(BAR_Q), s * 64,
-                        (2 * mblk + t) * kRows, bh);
+            load_rows(sbase + C::kOffQ + t * C::kTileBytes + s * C::kSubBytes, &tmQ, bar(BAR_Q), s * 64,
+                      (2 * mblk + t) * kRows);
         }
       }
       int issued = 0;
@@ -182,8 +213,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(bar(BAR_KV_FULL + slot), C::kTileBytes);
         const CUtensorMap* tm = (u & 1) ? &tmV : &tmK;
         for (int s = 0; s < C::kSub; ++s)
-          tma_load_3d(sbase + C::kOffKV + slot * C::kTileBytes + s * C::kSubBytes, tm, bar(BAR_KV_FULL + slot), s * 64,
-                      (u >> 1) * kKeys, bh);
+          load_rows(sbase + C::kOffKV + slot * C::kTileBytes + s * C::kSubBytes, tm, bar(BAR_KV_FULL + slot), s * 64,
+                    (u >> 1) * kKeys);
         issued = u + 1;
       }
       // let every issued copy land before the CTA can exit
@@ -353,8 +384,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const bool empty = !(l_sum > 0.f);
         const float inv = empty ? 0.f : 1.f / l_sum;
-        const bool in_range = row < N;
-        uint8_t* orow = static_cast<uint8_t*>(args.O) + (static_cast<size_t>(bh) * N + row) * (D * 2);
+        const bool in_range = row < Lq;
+        const size_t orow_idx = packed ? static_cast<size_t>(tok0 + row) * args.H + head
+                                       : static_cast<size_t>(bh) * N + row;
+        uint8_t* orow = static_cast<uint8_t*>(args.O) + orow_idx * (D * 2);
 #pragma unroll 1
         for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t r[32];
@@ -376,7 +409,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (in_range) {
           const float lse = empty ? -INFINITY : (m_ref + lg2_approx(l_sum)) * 0.69314718055994531f;
-          args.LSE[static_cast<size_t>(bh) * N + row] = lse;
+          const size_t lidx = packed ? static_cast<size_t>(head) * args.total + tok0 + row
+                                     : static_cast<size_t>(bh) * N + row;
+          args.LSE[lidx] = lse;
         }
       }
     }
@@ -413,6 +448,8 @@ fa_status fwd_launch_d(const void* Q, const void* K, const void* V, void* O, flo
   a.O = O;
   a.LSE = LSE;
   a.kv_lens = kv_lens;
+  a.cu_seqlens = nullptr;
+  a.total = 0;
   a.H = H;
   a.N = N;
   a.causal = causal ? 1 : 0;
@@ -423,7 +460,54 @@ fa_status fwd_launch_d(const void* Q, const void* K, const void* V, void* O, flo
   return launch_status();
 }
 
+template <int D>
+fa_status fwd_varlen_launch_d(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                              const int32_t* cu_seqlens, int num_seqs, int total, int max_seqlen, int H, int causal,
+                              float scale, cudaStream_t stream) {
+  using C = FwdCfg<D>;
+  // packed [total, H, D]: TMA dims (D, H, total), a box of 128 consecutive tokens of one head
+  const uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(H), static_cast<uint64_t>(total)};
+  const uint64_t strides[2] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(H) * D * 2};
+  const uint32_t box[3] = {64, 1, kRows};
+  CUtensorMap tq, tk, tv;
+  if (!encode_bf16_tmap(&tq, Q, 3, dims, strides, box) || !encode_bf16_tmap(&tk, K, 3, dims, strides, box) ||
+      !encode_bf16_tmap(&tv, V, 3, dims, strides, box))
+    return FA_ERR_CUDA;
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
+      return FA_ERR_CUDA;
+    attr_set = true;
+  }
+  unsigned* status = device_status_ptr();
+  if (status == nullptr) return FA_ERR_CUDA;
+  FwdArgs a;
+  a.O = O;
+  a.LSE = LSE;
+  a.kv_lens = nullptr;
+  a.cu_seqlens = cu_seqlens;
+  a.total = total;
+  a.H = H;
+  a.N = max_seqlen;
+  a.causal = causal ? 1 : 0;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.status = status;
+  dim3 grid(num_seqs * H, ceil_div(max_seqlen, 2 * kRows));
+  fwd_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, a);
+  return launch_status();
+}
+
 }  // namespace
+
+fa_status fwd_varlen_launch(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                            const int32_t* cu_seqlens, int num_seqs, int total, int max_seqlen, int H, int d,
+                            int causal, float scale, cudaStream_t stream) {
+  if (d == 64)
+    return fwd_varlen_launch_d<64>(Q, K, V, O, LSE, cu_seqlens, num_seqs, total, max_seqlen, H, causal, scale, stream);
+  if (d == 128)
+    return fwd_varlen_launch_d<128>(Q, K, V, O, LSE, cu_seqlens, num_seqs, total, max_seqlen, H, causal, scale, stream);
+  return FA_ERR_UNSUPPORTED;
+}
 
 fa_status fwd_launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d,
                      int causal, float scale, const int32_t* kv_lens, cudaStream_t stream) {

@@ -38,6 +38,9 @@ inline fa_status launch_status() {
 // validated by the public entry points before these are called.
 fa_status fwd_launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d,
                      int causal, float scale, const int32_t* kv_lens, cudaStream_t stream);
+fa_status fwd_varlen_launch(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                            const int32_t* cu_seqlens, int num_seqs, int total, int max_seqlen, int H, int d,
+                            int causal, float scale, cudaStream_t stream);
 fa_status bwd_launch(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
                      void* dQ, void* dK, void* dV, int B, int H, int N, int d, int causal, float scale,
                      const int32_t* kv_lens, void* workspace, cudaStream_t stream);

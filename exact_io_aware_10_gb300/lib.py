@@ -31,6 +31,7 @@ SIGNATURES = {
     "fa_version": (_i, []),
     "fa_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp]),
     "fa_fwd_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp, _vp]),
+    "fa_fwd_varlen": (_i, [_vp] * 6 + [_i, _i, _i, _i, _i, _i, _f, _vp]),
     "fa_bwd_workspace_size": (_sz, [_i, _i, _i, _i]),
     "fa_bwd": (_i, [_vp] * 9 + [_i, _i, _i, _i, _i, _f, _vp, _vp, _sz, _vp]),
     "fa_paged_decode_workspace_size": (_sz, [_i, _i, _i, _i]),
@@ -124,6 +125,33 @@ def fa_fwd(Q, K, V, causal=False, scale=None, kv_lens=None, O=None, LSE=None, st
     st = lib.fa_fwd_ex(_p(Q), _p(K), _p(V), _p(O), _p(LSE), B, H, N, d, int(bool(causal)), scale, _p(kv_lens),
                        _stream(stream))
     _check(st, "fa_fwd")
+    return O, LSE
+
+
+def fa_fwd_varlen(Q, K, V, cu_seqlens, max_seqlen, causal=False, scale=None, O=None, LSE=None, stream=None):
+    """O [total, H, d], LSE [H, total] for a packed ragged batch.
+
+    cu_seqlens is a CUDA int32 tensor [num_seqs + 1] of sequence offsets;
+    max_seqlen (a Python int) bounds the longest sequence.
+    """
+    lib = load()
+    total, H, d = Q.shape
+    for t, n in ((Q, "Q"), (K, "K"), (V, "V")):
+        _need(t, torch.bfloat16, (total, H, d), n)
+    _need(cu_seqlens, torch.int32, None, "cu_seqlens")
+    if cu_seqlens.dim() != 1 or cu_seqlens.numel() < 2:
+        raise ValueError("cu_seqlens must be 1-D with num_seqs + 1 >= 2 entries")
+    num_seqs = cu_seqlens.numel() - 1
+    if O is None:
+        O = torch.empty_like(Q)
+    if LSE is None:
+        LSE = torch.empty((H, total), dtype=torch.float32, device=Q.device)
+    _need(O, torch.bfloat16, (total, H, d), "O")
+    _need(LSE, torch.float32, (H, total), "LSE")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    st = lib.fa_fwd_varlen(_p(Q), _p(K), _p(V), _p(O), _p(LSE), _p(cu_seqlens), num_seqs, total, int(max_seqlen),
+                           H, d, int(bool(causal)), scale, _stream(stream))
+    _check(st, "fa_fwd_varlen")
     return O, LSE
 
 

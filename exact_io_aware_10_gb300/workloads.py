@@ -15,6 +15,9 @@ Long Range Arena -- are stood in for by these synthetic tensors):
                  random unit direction u; each Q row and each K row is picked
                  with probability 0.1 and gets c*u added, c = sqrt(8*sqrt(d)),
                  so about 1% of (query, key) pairs gain ~+8 in scaled logit.
+* ``varlen``     a packed ragged batch: sequence lengths L_s ~ U{lo..hi}
+                 (or given), Q, K, V, dO ~ N(0, std^2) in layout [total, H, d]
+                 with sequence s in rows cu_seqlens[s] .. cu_seqlens[s+1]-1.
 * ``paged``      decode queries [B, Hq, d], a paged KV cache
                  [num_blocks, block_size, Hkv, d], context lengths
                  L_b ~ U{lo..hi}, and a block table whose physical ids are a
@@ -34,6 +37,9 @@ __all__ = [
     "padded_lengths",
     "boosted_inputs",
     "paged_inputs",
+    "VarlenInputs",
+    "varlen_lengths",
+    "varlen_inputs",
     "paged_layout",
     "device_normal_bf16",
     "config_seed",
@@ -85,6 +91,42 @@ def padded_lengths(B, lo, hi, seed=0) -> torch.Tensor:
     """Per-sequence valid key lengths, uniform integers in [lo, hi], int32 [B]."""
     g = _gen(seed + 101)
     return torch.randint(lo, hi + 1, (B,), generator=g, dtype=torch.int64).to(torch.int32)
+
+
+@dataclass
+class VarlenInputs:
+    Q: torch.Tensor  # [total, H, d] bf16 (CPU)
+    K: torch.Tensor
+    V: torch.Tensor
+    dO: torch.Tensor
+    cu_seqlens: torch.Tensor  # int32 [num_seqs + 1], starts at 0, ends at total
+    max_seqlen: int
+
+    @property
+    def lengths(self):
+        return (self.cu_seqlens[1:] - self.cu_seqlens[:-1]).tolist()
+
+
+def varlen_lengths(num_seqs, lo, hi, seed=0) -> list:
+    """Sequence lengths of a ragged batch, uniform integers in [lo, hi]."""
+    g = _gen(seed + 211)
+    return torch.randint(lo, hi + 1, (num_seqs,), generator=g, dtype=torch.int64).tolist()
+
+
+def varlen_inputs(lengths, H, d, seed=0, std=1.0) -> VarlenInputs:
+    """Packed [total, H, d] Q, K, V, dO for sequences of the given lengths."""
+    lengths = [int(x) for x in lengths]
+    if any(x < 0 for x in lengths) or not lengths:
+        raise ValueError("lengths must be a non-empty list of non-negative ints")
+    cu = torch.zeros(len(lengths) + 1, dtype=torch.int64)
+    cu[1:] = torch.cumsum(torch.tensor(lengths, dtype=torch.int64), 0)
+    total = int(cu[-1])
+    g = _gen(seed)
+    Q = _normal_bf16((total, H, d), g, std)
+    K = _normal_bf16((total, H, d), g, std)
+    V = _normal_bf16((total, H, d), g, std)
+    dO = _normal_bf16((total, H, d), g, 1.0)
+    return VarlenInputs(Q, K, V, dO, cu.to(torch.int32), max(lengths))
 
 
 def boosted_inputs(B, H, N, d, seed=0, std=0.5, pick_prob=0.1, boost=8.0) -> AttentionInputs:

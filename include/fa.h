@@ -76,6 +76,29 @@ int fa_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* LSE, 
               int causal, float scale, const int32_t* kv_lens, void* stream);
 
 /*
+ * Forward attention over a packed ragged batch: num_seqs sequences of
+ * different lengths laid end to end, each attending only to itself (with
+ * per-sequence causal masking).  This is the irregular-batch case of the
+ * S12 chapter's "exp(-inf - -inf) is NaN" passage, where whole key tiles
+ * are masked, and the no-padding form of fa_fwd_ex's key-padding mask.
+ *   Q, K, V    : [total, H, d] bf16, read only; token t of every head is row t.
+ *   O          : [total, H, d] bf16, written for every token of every sequence.
+ *   LSE        : [H, total] fp32, written (natural log, as fa_fwd).
+ *   cu_seqlens : device int32 [num_seqs + 1]; sequence s owns tokens
+ *                cu_seqlens[s] .. cu_seqlens[s+1]-1.  It must start at 0,
+ *                be non-decreasing and end at total.  Empty sequences are
+ *                allowed.  Query i and key j of a sequence are positions
+ *                within that sequence; causal masks j > i (square, top-left).
+ *   max_seqlen : an upper bound of the longest sequence (it sizes the grid).
+ * Errors: FA_ERR_INVALID_ARG / FA_ERR_UNSUPPORTED / FA_ERR_CUDA for the
+ * host-visible arguments.  cu_seqlens lives on the device, so a sequence with
+ * bad offsets or longer than max_seqlen is found there: nothing is written for
+ * it and fa_get_device_status() then returns FA_ERR_INVALID_ARG.
+ */
+int fa_fwd_varlen(const void* Q, const void* K, const void* V, void* O, float* LSE, const int32_t* cu_seqlens,
+                  int num_seqs, int total, int max_seqlen, int H, int d, int causal, float scale, void* stream);
+
+/*
  * Bytes of device workspace fa_bwd needs: two fp32 [B, H, Npad] row buffers
  * (D = rowsum(dO * O) and LSE in log2 units; Npad = N rounded up to 128) and
  * an fp32 [B, H, N, d] dQ accumulator, each rounded up to 256 bytes.

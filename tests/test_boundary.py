@@ -43,7 +43,7 @@ def test_status_strings(so):
                        (4, "FA_ERR_TIMEOUT"), (5, "FA_ERR_BAD_BLOCK_TABLE")]:
         assert so.fa_status_string(code).decode() == name
     assert so.fa_status_string(99).decode() == "FA_ERR_UNKNOWN"
-    assert so.fa_version() == 100
+    assert so.fa_version() == 101
 
 
 def _fake(n=1):
@@ -63,6 +63,26 @@ def test_forward_argument_validation(so):
     assert so.fa_fwd(ctypes.c_void_p(0x10000008), K, V, O, L, 1, 1, 16, 64, 0, 0.1, s) == fl.FA_ERR_INVALID_ARG
     # N = 0 is a valid no-op and launches nothing
     assert so.fa_fwd(Q, K, V, O, L, 1, 1, 0, 64, 0, 0.1, s) == fl.FA_OK
+
+
+def test_varlen_forward_argument_validation(so):
+    Q, K, V, O, L, cu = _fake(6)
+    s = ctypes.c_void_p(0)
+    f = so.fa_fwd_varlen
+    # (Q, K, V, O, LSE, cu_seqlens, num_seqs, total, max_seqlen, H, d, causal, scale, stream)
+    assert f(Q, K, V, O, L, cu, 2, 100, 64, 4, 96, 0, 0.1, s) == fl.FA_ERR_UNSUPPORTED
+    assert f(Q, K, V, O, L, cu, 0, 100, 64, 4, 64, 0, 0.1, s) == fl.FA_ERR_INVALID_ARG
+    assert f(Q, K, V, O, L, cu, 2, -1, 64, 4, 64, 0, 0.1, s) == fl.FA_ERR_INVALID_ARG
+    assert f(Q, K, V, O, L, cu, 2, 100, -1, 4, 64, 0, 0.1, s) == fl.FA_ERR_INVALID_ARG
+    assert f(Q, K, V, O, L, cu, 2, 100, 64, 0, 64, 0, 0.1, s) == fl.FA_ERR_INVALID_ARG
+    assert f(Q, K, V, O, L, None, 2, 100, 64, 4, 64, 0, 0.1, s) == fl.FA_ERR_INVALID_ARG
+    assert f(Q, K, V, O, None, cu, 2, 100, 64, 4, 64, 0, 0.1, s) == fl.FA_ERR_INVALID_ARG
+    assert f(Q, K, V, O, L, cu, 2, 100, 64, 4, 64, 0, float("inf"), s) == fl.FA_ERR_INVALID_ARG
+    assert f(Q, ctypes.c_void_p(0x10000004), V, O, L, cu, 2, 100, 64, 4, 64, 0, 0.1, s) == fl.FA_ERR_INVALID_ARG
+    # a max_seqlen needing more than 65535 grid rows is outside the kernel's grid
+    assert f(Q, K, V, O, L, cu, 2, 100, 256 * 65536, 4, 64, 0, 0.1, s) == fl.FA_ERR_UNSUPPORTED
+    # an empty batch is a valid no-op and launches nothing
+    assert f(Q, K, V, O, L, cu, 2, 0, 0, 4, 64, 0, 0.1, s) == fl.FA_OK
 
 
 def test_backward_argument_validation(so):
