@@ -1,7 +1,8 @@
 """Run one attention entry point on seeded synthetic inputs, e.g. for a
 profiler:  python -m exact_io_aware_10_gb300.cli fwd --N 16384 --iters 2
 
-Subcommands: fwd, bwd (runs fwd once to produce O/LSE, then bwd), decode.
+Subcommands: fwd, bwd (runs fwd once to produce O/LSE, then bwd), decode,
+varlen (packed ragged batch of --num-seqs sequences, lengths U[--seq-lo, --seq-hi]).
 Prints the CUDA-event time of the last iteration.
 """
 from __future__ import annotations
@@ -20,7 +21,7 @@ from exact_io_aware_10_gb300 import workloads as wl  # noqa: E402
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("op", choices=["fwd", "bwd", "decode"])
+    ap.add_argument("op", choices=["fwd", "bwd", "decode", "varlen"])
     ap.add_argument("--B", type=int, default=1)
     ap.add_argument("--H", type=int, default=16)
     ap.add_argument("--N", type=int, default=16384)
@@ -33,6 +34,9 @@ def main(argv=None):
     ap.add_argument("--L-hi", type=int, default=32768)
     ap.add_argument("--splits", type=int, default=16)
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--num-seqs", type=int, default=16)
+    ap.add_argument("--seq-lo", type=int, default=512)
+    ap.add_argument("--seq-hi", type=int, default=16384)
     a = ap.parse_args(argv)
     dev = torch.device("cuda")
     lib.load()
@@ -48,6 +52,19 @@ def main(argv=None):
                 lib.fa_fwd(Q, K, V, causal=causal, O=O, LSE=L)
             else:
                 lib.fa_bwd(Q, K, V, O, dO, L, causal=causal)
+            end.record()
+    elif a.op == "varlen":
+        lens = wl.varlen_lengths(a.num_seqs, a.seq_lo, a.seq_hi, seed=a.seed)
+        cu = [0]
+        for n in lens:
+            cu.append(cu[-1] + n)
+        shp = (cu[-1], a.H, a.d)
+        Q, K, V = (wl.device_normal_bf16(shp, a.seed + i, dev) for i in range(3))
+        cu = torch.tensor(cu, dtype=torch.int32, device=dev)
+        O, L = lib.fa_fwd_varlen(Q, K, V, cu, max(lens), causal=causal)
+        for _ in range(a.iters):
+            start.record()
+            lib.fa_fwd_varlen(Q, K, V, cu, max(lens), causal=causal, O=O, LSE=L)
             end.record()
     else:
         sl, table, NB, _ = wl.paged_layout(a.B, a.L_lo, a.L_hi, 16, a.seed, None)

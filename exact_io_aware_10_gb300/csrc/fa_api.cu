@@ -151,6 +151,7 @@ int fa_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* LSE, 
               float scale, const int32_t* kv_lens, void* stream) {
   int st = check_attn(Q, K, V, O, LSE, B, H, N, d, scale);
   if (st != FA_OK || N == 0) return st;
+  if (B > 65535) return FA_ERR_UNSUPPORTED;  // batch entries are the grid's z dimension
   return fa::fwd_launch(Q, K, V, O, LSE, B, H, N, d, causal, scale, kv_lens, static_cast<cudaStream_t>(stream));
 }
 
@@ -167,6 +168,7 @@ int fa_fwd_varlen(const void* Q, const void* K, const void* V, void* O, float* L
   if (total == 0 || max_seqlen == 0) return FA_OK;
   if (!Q || !K || !V || !O || !LSE || !cu_seqlens) return FA_ERR_INVALID_ARG;
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(LSE)) return FA_ERR_INVALID_ARG;
+  if (num_seqs > 65535) return FA_ERR_UNSUPPORTED;  // sequences are the grid's z dimension
   if (static_cast<long long>(num_seqs) * H > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
   if ((static_cast<long long>(max_seqlen) + 255) / 256 > 65535) return FA_ERR_UNSUPPORTED;
   return fa::fwd_varlen_launch(Q, K, V, O, LSE, cu_seqlens, num_seqs, total, max_seqlen, H, d, causal, scale,

@@ -112,7 +112,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int bh = blockIdx.x;  // dense: batch * H + head; packed: sequence * H + head
+  // grid (H, query-tile pairs, B or num_seqs): the heads of one batch entry
+  // (sequence) run side by side, so concurrent CTAs share its K/V in L2
+  const int bh = blockIdx.z * gridDim.x + blockIdx.x;  // dense: batch * H + head; packed: sequence * H + head
   const int b = bh / args.H;
   const int mblk = gridDim.y - 1 - blockIdx.y;  // longest causal work first
   const int N = args.N;
@@ -455,7 +457,7 @@ fa_status fwd_launch_d(const void* Q, const void* K, const void* V, void* O, flo
   a.causal = causal ? 1 : 0;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.status = status;
-  dim3 grid(B * H, ceil_div(N, 2 * kRows));
+  dim3 grid(H, ceil_div(N, 2 * kRows), B);
   fwd_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, a);
   return launch_status();
 }
@@ -492,7 +494,7 @@ fa_status fwd_varlen_launch_d(const void* Q, const void* K, const void* V, void*
   a.causal = causal ? 1 : 0;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.status = status;
-  dim3 grid(num_seqs * H, ceil_div(max_seqlen, 2 * kRows));
+  dim3 grid(H, ceil_div(max_seqlen, 2 * kRows), num_seqs);
   fwd_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, a);
   return launch_status();
 }

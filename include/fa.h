@@ -60,7 +60,7 @@ int fa_version(void);
  *             that replaces the notes' (m, l) pair, §3.3).
  *   causal  : non-zero masks key j > query i (top-left aligned, square).
  *   scale   : logit scale, typically 1/sqrt(d); must be finite and > 0.
- * B, H >= 1, N >= 0 (N = 0 is a no-op).  Errors: FA_ERR_INVALID_ARG,
+ * B, H >= 1, N >= 0 (N = 0 is a no-op); B <= 65535.  Errors: FA_ERR_INVALID_ARG,
  * FA_ERR_UNSUPPORTED, FA_ERR_CUDA.
  */
 int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d, int causal,
@@ -90,6 +90,7 @@ int fa_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* LSE, 
  *                allowed.  Query i and key j of a sequence are positions
  *                within that sequence; causal masks j > i (square, top-left).
  *   max_seqlen : an upper bound of the longest sequence (it sizes the grid).
+ * num_seqs in [1, 65535], H >= 1, total >= 0 (total = 0 is a no-op).
  * Errors: FA_ERR_INVALID_ARG / FA_ERR_UNSUPPORTED / FA_ERR_CUDA for the
  * host-visible arguments.  cu_seqlens lives on the device, so a sequence with
  * bad offsets or longer than max_seqlen is found there: nothing is written for

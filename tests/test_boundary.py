@@ -61,6 +61,8 @@ def test_forward_argument_validation(so):
     assert so.fa_fwd(Q, K, V, O, L, 1, 1, 16, 64, 0, 0.0, s) == fl.FA_ERR_INVALID_ARG
     assert so.fa_fwd(Q, K, V, O, L, 1, 1, 16, 64, 0, float("nan"), s) == fl.FA_ERR_INVALID_ARG
     assert so.fa_fwd(ctypes.c_void_p(0x10000008), K, V, O, L, 1, 1, 16, 64, 0, 0.1, s) == fl.FA_ERR_INVALID_ARG
+    # more batch entries than the grid's z dimension holds
+    assert so.fa_fwd(Q, K, V, O, L, 65536, 1, 16, 64, 0, 0.1, s) == fl.FA_ERR_UNSUPPORTED
     # N = 0 is a valid no-op and launches nothing
     assert so.fa_fwd(Q, K, V, O, L, 1, 1, 0, 64, 0, 0.1, s) == fl.FA_OK
 
@@ -81,6 +83,8 @@ def test_varlen_forward_argument_validation(so):
     assert f(Q, ctypes.c_void_p(0x10000004), V, O, L, cu, 2, 100, 64, 4, 64, 0, 0.1, s) == fl.FA_ERR_INVALID_ARG
     # a max_seqlen needing more than 65535 grid rows is outside the kernel's grid
     assert f(Q, K, V, O, L, cu, 2, 100, 256 * 65536, 4, 64, 0, 0.1, s) == fl.FA_ERR_UNSUPPORTED
+    # more sequences than the grid's z dimension holds
+    assert f(Q, K, V, O, L, cu, 65536, 100, 64, 4, 64, 0, 0.1, s) == fl.FA_ERR_UNSUPPORTED
     # an empty batch is a valid no-op and launches nothing
     assert f(Q, K, V, O, L, cu, 2, 0, 0, 4, 64, 0, 0.1, s) == fl.FA_OK
 
