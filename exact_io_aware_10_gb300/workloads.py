@@ -18,6 +18,9 @@ Long Range Arena -- are stood in for by these synthetic tensors):
 * ``varlen``     a packed ragged batch: sequence lengths L_s ~ U{lo..hi}
                  (or given), Q, K, V, dO ~ N(0, std^2) in layout [total, H, d]
                  with sequence s in rows cu_seqlens[s] .. cu_seqlens[s+1]-1.
+* ``paged_prefill``  query chunks of lengths q_len_b packed [total_q, Hq, d]
+                 (cu_seqlens_q) over a ``paged`` cache whose sequences hold
+                 kv_len_b >= q_len_b tokens (cached prefix + the chunk).
 * ``paged``      decode queries [B, Hq, d], a paged KV cache
                  [num_blocks, block_size, Hkv, d], context lengths
                  L_b ~ U{lo..hi}, and a block table whose physical ids are a
@@ -38,6 +41,8 @@ __all__ = [
     "boosted_inputs",
     "paged_inputs",
     "VarlenInputs",
+    "PagedPrefillInputs",
+    "paged_prefill_inputs",
     "varlen_lengths",
     "varlen_inputs",
     "paged_layout",
@@ -202,6 +207,42 @@ def paged_inputs(B, Hq, Hkv, d, L_lo, L_hi, block_size=16, seed=0, max_blocks=No
     k_cache = _normal_bf16((max(NB, 1), block_size, Hkv, d), g, std)
     v_cache = _normal_bf16((max(NB, 1), block_size, Hkv, d), g, std)
     return PagedInputs(q, k_cache, v_cache, table, seq_lens, block_size)
+
+
+@dataclass
+class PagedPrefillInputs:
+    q: torch.Tensor  # [total_q, Hq, d] bf16 (CPU)
+    k_cache: torch.Tensor  # [num_blocks, block_size, Hkv, d] bf16
+    v_cache: torch.Tensor
+    block_table: torch.Tensor  # int32 [B, max_blocks], -1 past a sequence's blocks
+    cu_seqlens_q: torch.Tensor  # int32 [B + 1]
+    seq_lens_k: torch.Tensor  # int32 [B]
+    block_size: int
+
+    @property
+    def q_lens(self):
+        return (self.cu_seqlens_q[1:] - self.cu_seqlens_q[:-1]).tolist()
+
+    @property
+    def max_seqlen_q(self):
+        return max(self.q_lens)
+
+
+def paged_prefill_inputs(q_lens, kv_lens, Hq, Hkv, d, block_size=16, seed=0, std=1.0, max_blocks=None,
+                         spare_blocks=0) -> PagedPrefillInputs:
+    """Chunked-prefill inputs on the CPU: a ``paged_layout`` cache for context
+    lengths kv_lens, and packed query chunks of lengths q_lens."""
+    q_lens = [int(x) for x in q_lens]
+    if len(q_lens) != len(kv_lens) or not q_lens or min(q_lens) < 0:
+        raise ValueError("q_lens and kv_lens must be equal-length lists of non-negative ints")
+    seq_lens, table, NB, g = paged_layout(len(q_lens), 0, 0, block_size, seed, max_blocks, list(kv_lens),
+                                          spare_blocks)
+    cu = torch.zeros(len(q_lens) + 1, dtype=torch.int64)
+    cu[1:] = torch.cumsum(torch.tensor(q_lens, dtype=torch.int64), 0)
+    q = _normal_bf16((int(cu[-1]), Hq, d), g, std)
+    k_cache = _normal_bf16((max(NB, 1), block_size, Hkv, d), g, std)
+    v_cache = _normal_bf16((max(NB, 1), block_size, Hkv, d), g, std)
+    return PagedPrefillInputs(q, k_cache, v_cache, table, cu.to(torch.int32), seq_lens, block_size)
 
 
 def device_normal_bf16(shape, seed, device, std=1.0):

@@ -42,6 +42,11 @@ from .decode import (  # noqa: F401
     paged_decode_streaming,
     split_paged_decode,
 )
+from .paged_prefill import (  # noqa: F401
+    chunk_key_mask,
+    paged_prefill,
+    paged_prefill_rows,
+)
 from .io_model import (  # noqa: F401
     standard_hbm_accesses,
     flash_hbm_accesses,
