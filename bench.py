@@ -53,6 +53,11 @@ VARLEN = {
     "bert": dict(num_seqs=16, lo=128, hi=512, H=16, d=64, causal=False, config_id=2, padded_N=512),
     "long": dict(num_seqs=16, lo=512, hi=16384, H=16, d=128, causal=True, config_id=6, padded_N=None),
 }
+# chunked prefill over a paged cache, timed after the step: every sequence
+# appends a q_len-token chunk to a cached prefix of U[prefix_lo, prefix_hi]
+# tokens (GQA heads, 16-token blocks, seeded random block placement)
+PAGED_PREFILL = dict(num_seqs=16, q_len=2048, prefix_lo=0, prefix_hi=30720, Hq=32, Hkv=8, d=128, block_size=16,
+                     config_id=7)
 WORKLOAD = ("long-context causal prefill B1 H16 d128 (fwd+bwd N=16384, fwd N=65536) + paged GQA decode "
             "B64 Hq32 Hkv8 d128 L~U[512,32768] block16 splits16")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -281,6 +286,54 @@ def time_varlen(dev, seed, steps, warmup, barrier, max_over_ranks, world, peak_t
     return out
 
 
+class PagedPrefillWorkload:
+    """Device-resident chunks, paged cache and block table of PAGED_PREFILL."""
+
+    def __init__(self, dev, seed=0):
+        from exact_io_aware_10_gb300 import lib
+
+        self.lib = lib
+        c = PAGED_PREFILL
+        sd = wl.config_seed(seed, c["config_id"])
+        g = torch.Generator().manual_seed(sd)
+        prefix = torch.randint(c["prefix_lo"], c["prefix_hi"] + 1, (c["num_seqs"],), generator=g).tolist()
+        self.q_lens = [c["q_len"]] * c["num_seqs"]
+        self.kv_lens = [p + c["q_len"] for p in prefix]
+        sl, table, NB, _ = wl.paged_layout(c["num_seqs"], 0, 0, c["block_size"], sd, None, self.kv_lens)
+        cu = [0]
+        for n in self.q_lens:
+            cu.append(cu[-1] + n)
+        self.cu = torch.tensor(cu, dtype=torch.int32, device=dev)
+        self.sl, self.table = sl.to(dev), table.to(dev)
+        self.q = wl.device_normal_bf16((cu[-1], c["Hq"], c["d"]), sd + 1, dev)
+        cshape = (NB, c["block_size"], c["Hkv"], c["d"])
+        self.kc = wl.device_normal_bf16(cshape, sd + 2, dev)
+        self.vc = wl.device_normal_bf16(cshape, sd + 3, dev)
+        self.o = torch.empty_like(self.q)
+        self.lse = torch.empty((c["Hq"], cu[-1]), dtype=torch.float32, device=dev)
+        self.flops = acc.paged_prefill_flops(self.q_lens, self.kv_lens, c["Hq"], c["d"], True)
+
+    def run(self):
+        self.lib.fa_paged_prefill(self.q, self.kc, self.vc, self.table, self.cu, self.sl, max(self.q_lens),
+                                  causal=True, o=self.o, lse=self.lse)
+
+
+def time_paged_prefill(dev, seed, steps, warmup, barrier, max_over_ranks, world, peak_tf):
+    w = PagedPrefillWorkload(dev, seed)
+    _, ms = time_parts(lambda p: w.run(), ("run",), steps, warmup, barrier)
+    assert w.lib.fa_get_device_status() == w.lib.FA_OK, "device status word reported an error"
+    t = max_over_ranks(ms["run"])
+    tf = world * steps * w.flops / (t * 1e-3) / 1e12
+    c = PAGED_PREFILL
+    out = {"num_seqs": c["num_seqs"], "q_len": c["q_len"], "prefix": f"U[{c['prefix_lo']},{c['prefix_hi']}]",
+           "Hq": c["Hq"], "Hkv": c["Hkv"], "d": c["d"], "block_size": c["block_size"], "causal": "bottom-right",
+           "flops": w.flops, "TFLOP/s": tf, "frac": tf / world / peak_tf,
+           "frac_of_nominal": tf / world / NOMINAL["bf16_tflops"], "ms": t / steps}
+    del w
+    torch.cuda.empty_cache()
+    return out
+
+
 class HostBuffers:
     """Pinned host copies of a step's inputs and outputs for the end-to-end run."""
 
@@ -436,6 +489,8 @@ def run_ours(args):
     next_rows = None
     if not args.skip_next_rows:
         next_rows = time_varlen(dev, args.seed, args.steps, args.warmup, barrier, max_over_ranks, world, peak_tf)
+        next_rows["paged_prefill"] = time_paged_prefill(dev, args.seed, args.steps, args.warmup, barrier,
+                                                        max_over_ranks, world, peak_tf)
         next_rows["note"] = "timed after the step, outside value and ms_per_step; TFLOP/s count useful FLOPs only"
 
     cpu = None
@@ -541,7 +596,8 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--skip-next-rows", action="store_true", help="skip the ragged-batch forward timings")
+    ap.add_argument("--skip-next-rows", action="store_true",
+                    help="skip the ragged-batch forward and paged-prefill timings")
     ap.add_argument("--ref-prefix", type=int, default=2048)
     args = ap.parse_args()
     if args.warmup < 3:

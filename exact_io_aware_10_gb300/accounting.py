@@ -6,6 +6,9 @@ Conventions (matmul work only; exp, masking and reductions are not counted):
   key padding: the effective forward count is 4 * H * N * d * sum_b L_b
   packed ragged batch: the sum of the forward count of every sequence,
             4 * H * d * sum_s L_s^2, halved when causal
+  paged chunked prefill: 4 * Hq * d per visible (query, key) pair, counted
+            exactly: a causal chunk of q rows after a prefix of p keys has
+            q * p + q (q + 1) / 2 pairs; non-causal q * (p + q)
   decode    bytes = K and V of every visible key, read once per KV head
             (sum_b L_b * Hkv * d * 2 B * 2) + q + o + lse + the block-table
             entries and sequence lengths read.
@@ -29,6 +32,24 @@ def fwd_flops_padded(H, N, d, kv_lens):
 
 def varlen_fwd_flops(lengths, H, d, causal=False):
     return sum(fwd_flops(1, H, int(n), d, causal) for n in lengths)
+
+
+def paged_prefill_flops(q_lens, kv_lens, Hq, d, causal=True):
+    pairs = 0
+    for q, k in zip(q_lens, kv_lens):
+        q, k = int(q), int(k)
+        if not causal:
+            pairs += q * k
+            continue
+        for_rows = 0
+        p = k - q  # keys before the chunk's first query (negative: rows with no key)
+        if p >= 0:
+            for_rows = q * p + q * (q + 1) // 2
+        else:
+            r = q + p  # rows that see at least one key: r rows seeing 1..r keys
+            for_rows = max(r, 0) * (max(r, 0) + 1) // 2
+        pairs += for_rows
+    return 4.0 * Hq * d * pairs
 
 
 def fwd_bytes(B, H, N, d):

@@ -2,7 +2,9 @@
 profiler:  python -m exact_io_aware_10_gb300.cli fwd --N 16384 --iters 2
 
 Subcommands: fwd, bwd (runs fwd once to produce O/LSE, then bwd), decode,
-varlen (packed ragged batch of --num-seqs sequences, lengths U[--seq-lo, --seq-hi]).
+varlen (packed ragged batch of --num-seqs sequences, lengths U[--seq-lo, --seq-hi]),
+prefill (paged chunked prefill: --num-seqs chunks of --chunk tokens after cached
+prefixes of U[0, --prefix-hi] tokens, --Hq/--Hkv heads, 16-token blocks).
 Prints the CUDA-event time of the last iteration.
 """
 from __future__ import annotations
@@ -21,7 +23,7 @@ from exact_io_aware_10_gb300 import workloads as wl  # noqa: E402
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("op", choices=["fwd", "bwd", "decode", "varlen"])
+    ap.add_argument("op", choices=["fwd", "bwd", "decode", "varlen", "prefill"])
     ap.add_argument("--B", type=int, default=1)
     ap.add_argument("--H", type=int, default=16)
     ap.add_argument("--N", type=int, default=16384)
@@ -37,6 +39,8 @@ def main(argv=None):
     ap.add_argument("--num-seqs", type=int, default=16)
     ap.add_argument("--seq-lo", type=int, default=512)
     ap.add_argument("--seq-hi", type=int, default=16384)
+    ap.add_argument("--chunk", type=int, default=2048)
+    ap.add_argument("--prefix-hi", type=int, default=30720)
     a = ap.parse_args(argv)
     dev = torch.device("cuda")
     lib.load()
@@ -65,6 +69,21 @@ def main(argv=None):
         for _ in range(a.iters):
             start.record()
             lib.fa_fwd_varlen(Q, K, V, cu, max(lens), causal=causal, O=O, LSE=L)
+            end.record()
+    elif a.op == "prefill":
+        g = torch.Generator().manual_seed(a.seed)
+        prefix = torch.randint(0, a.prefix_hi + 1, (a.num_seqs,), generator=g).tolist()
+        kv = [p + a.chunk for p in prefix]
+        sl, table, NB, _ = wl.paged_layout(a.num_seqs, 0, 0, 16, a.seed, None, kv)
+        cu = torch.arange(0, (a.num_seqs + 1) * a.chunk, a.chunk, dtype=torch.int32, device=dev)
+        q = wl.device_normal_bf16((a.num_seqs * a.chunk, a.Hq, a.d), a.seed + 1, dev)
+        kc = wl.device_normal_bf16((NB, 16, a.Hkv, a.d), a.seed + 2, dev)
+        vc = wl.device_normal_bf16((NB, 16, a.Hkv, a.d), a.seed + 3, dev)
+        sl, table = sl.to(dev), table.to(dev)
+        o, lse = lib.fa_paged_prefill(q, kc, vc, table, cu, sl, a.chunk, causal=causal)
+        for _ in range(a.iters):
+            start.record()
+            lib.fa_paged_prefill(q, kc, vc, table, cu, sl, a.chunk, causal=causal, o=o, lse=lse)
             end.record()
     else:
         sl, table, NB, _ = wl.paged_layout(a.B, a.L_lo, a.L_hi, 16, a.seed, None)

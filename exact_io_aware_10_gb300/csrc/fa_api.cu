@@ -145,7 +145,7 @@ const char* fa_status_string(int status) {
   }
 }
 
-int fa_version(void) { return 101; }
+int fa_version(void) { return 102; }
 
 int fa_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d, int causal,
               float scale, const int32_t* kv_lens, void* stream) {
@@ -173,6 +173,33 @@ int fa_fwd_varlen(const void* Q, const void* K, const void* V, void* O, float* L
   if ((static_cast<long long>(max_seqlen) + 255) / 256 > 65535) return FA_ERR_UNSUPPORTED;
   return fa::fwd_varlen_launch(Q, K, V, O, LSE, cu_seqlens, num_seqs, total, max_seqlen, H, d, causal, scale,
                                static_cast<cudaStream_t>(stream));
+}
+
+int fa_paged_prefill(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                     const int32_t* cu_seqlens_q, const int32_t* seq_lens_k, void* o, float* lse, int num_seqs,
+                     int total_q, int max_seqlen_q, int Hq, int Hkv, int d, int num_blocks, int block_size,
+                     int max_blocks, int causal, float scale, void* stream) {
+  if (num_seqs < 1 || total_q < 0 || max_seqlen_q < 0 || Hq < 1 || Hkv < 1 || num_blocks < 1 || max_blocks < 1 ||
+      block_size < 1)
+    return FA_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0 || bad_scale(scale)) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  // a 128-key tile is gathered as whole boxes of min(block_size, 128) rows,
+  // each a multiple of 8 rows (one 1024-byte swizzle period)
+  if (block_size % 8 != 0 || (128 % block_size != 0 && block_size % 128 != 0)) return FA_ERR_UNSUPPORTED;
+  if (num_seqs > 65535 || static_cast<long long>(num_seqs) * Hq > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(num_blocks) * block_size >= 0x7fffffffLL ||
+      static_cast<long long>(max_blocks) * block_size >= 0x7fffffffLL)
+    return FA_ERR_UNSUPPORTED;
+  if ((static_cast<long long>(max_seqlen_q) + 255) / 256 > 65535) return FA_ERR_UNSUPPORTED;
+  if (total_q == 0 || max_seqlen_q == 0) return FA_OK;
+  if (!q || !k_cache || !v_cache || !block_table || !cu_seqlens_q || !seq_lens_k || !o || !lse)
+    return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) || !aligned16(lse))
+    return FA_ERR_INVALID_ARG;
+  return fa::fwd_paged_launch(q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens_k, o, lse, num_seqs, total_q,
+                              max_seqlen_q, Hq, Hkv, d, num_blocks, block_size, max_blocks, causal, scale,
+                              static_cast<cudaStream_t>(stream));
 }
 
 size_t fa_bwd_workspace_size(int B, int H, int N, int d) {

@@ -77,8 +77,10 @@ constexpr int kOffAbort = kOffTmemSlot + 4;
 struct FwdArgs {
   void* O;
   float* LSE;
+  // dense: keys visible per batch entry (nullptr: all N); paged: kv_len of
+  // each sequence (cached prefix + its query chunk)
   const int32_t* kv_lens;
-  // packed ragged batch: Q/K/V/O are [total, H, D], LSE is [H, total] and
+  // packed ragged batch: Q/O are [total, H, D], LSE is [H, total] and
   // sequence s owns tokens cu_seqlens[s] .. cu_seqlens[s+1]-1 (nullptr: dense)
   const int32_t* cu_seqlens;
   int total;
@@ -86,6 +88,11 @@ struct FwdArgs {
   int causal;
   float scale_log2;  // scale * log2(e)
   unsigned* status;
+  // paged K/V (nullptr: K/V laid out like Q): key t of sequence s and KV head
+  // g is cache row block_table[s][t / block_size] * block_size + t % block_size
+  // of the (D, Hkv, num_rows) tensor maps; query head h reads KV head h / group
+  const int32_t* block_table;
+  int max_blocks, block_size, box_rows, num_rows, num_blocks, group;
 };
 
 // Wait for a barrier phase ignoring the abort flag, for at most ~50 ms; used
@@ -121,23 +128,33 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool packed = args.cu_seqlens != nullptr;
   const int head = bh % args.H;
 
-  // rows of this (sequence, head): Lq query rows; keys are the same rows, the
-  // first kv_len of them visible; tok0 = first token of the sequence (packed)
-  int Lq = N, kv_len = N, tok0 = 0;
+  const bool paged = args.block_table != nullptr;
+  const int kv_head = paged ? head / args.group : head;
+
+  // rows of this (sequence, head): Lq query rows; kv_len visible keys; query
+  // row r sits at key position qoff + r (causal masks keys past it: qoff = 0
+  // is the square top-left mask, qoff = kv_len - Lq the bottom-right one of a
+  // query chunk at the end of its context); tok0 = first query token (packed)
+  // kv_lens: the dense key-padding lengths or the paged context lengths
+  const int kv_given = (args.kv_lens != nullptr) ? args.kv_lens[b] : N;
+  int Lq = N, kv_len = N, tok0 = 0, qoff = 0;
   if (packed) {
     tok0 = args.cu_seqlens[b];
     const int tok1 = args.cu_seqlens[b + 1];
-    // offsets must be non-decreasing within [0, total], and no sequence may be
-    // longer than the max_seqlen the grid covers; otherwise nothing is written
-    // for this sequence and the status word records the bad argument
-    if (tok0 < 0 || tok1 < tok0 || tok1 > args.total || tok1 - tok0 > static_cast<int>(gridDim.y) * 2 * kRows) {
+    kv_len = paged ? kv_given : tok1 - tok0;
+    // offsets must be non-decreasing within [0, total], no sequence may be
+    // longer than the max_seqlen the grid covers, and a paged context must fit
+    // its block-table row; otherwise nothing is written for this sequence and
+    // the status word records the bad argument
+    if (tok0 < 0 || tok1 < tok0 || tok1 > args.total || tok1 - tok0 > static_cast<int>(gridDim.y) * 2 * kRows ||
+        (paged && (kv_len < 0 || kv_len > args.max_blocks * args.block_size))) {
       if (blockIdx.y == 0 && threadIdx.x == 0) atomicOr(args.status, kStatusBadArgBit);
       return;
     }
     Lq = tok1 - tok0;
-    kv_len = Lq;
-  } else if (args.kv_lens != nullptr) {
-    kv_len = min(max(args.kv_lens[b], 0), N);
+    qoff = kv_len - Lq;
+  } else {
+    kv_len = min(max(kv_given, 0), N);
   }
   if (packed && 2 * mblk * kRows >= Lq) return;  // whole CTA past this sequence's end
   int n_t[2];
@@ -147,8 +164,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int qt = 2 * mblk + t;
     valid_t[t] = qt * kRows < Lq;
     int end = kv_len;
-    if (args.causal) end = min(end, qt * kRows + kRows);
-    n_t[t] = valid_t[t] ? (end + kKeys - 1) / kKeys : 0;
+    if (args.causal) end = min(end, qoff + qt * kRows + kRows);
+    n_t[t] = (valid_t[t] && end > 0) ? (end + kKeys - 1) / kKeys : 0;
   }
   const int nmax = max(n_t[0], n_t[1]);
 
@@ -194,31 +211,85 @@ __global__ void __launch_bounds__(kThreads, 1)
       else
         tma_load_3d(dst, tm, mb, x, row, bh);
     };
-    if (lane == 0) {
-      uint32_t qbytes = 0;
-      for (int t = 0; t < 2; ++t)
-        if (valid_t[t]) qbytes += C::kTileBytes;
-      if (qbytes != 0 && nmax > 0) {
-        mbar_arrive_expect_tx(bar(BAR_Q), qbytes);
-        for (int t = 0; t < 2; ++t) {
-          if (!valid_t[t]) continue;
-          for (int s = 0; s < C::kSub; ++s)
-            load_rows(sbase + C::kOffQ + t * C::kTileBytes + s * C::kSubBytes, &tmQ, bar(BAR_Q), s * 64,
-                      (2 * mblk + t) * kRows);
-        }
-      }
-      int issued = 0;
-      for (int u = 0; u < 2 * nmax; ++u) {
-        const int slot = u % C::kSlots;
-        const uint32_t ph = static_cast<uint32_t>(u / C::kSlots) & 1u;
-        if (!mbar_wait(bar(BAR_KV_EMPTY + slot), ph ^ 1u, wc)) break;
-        mbar_arrive_expect_tx(bar(BAR_KV_FULL + slot), C::kTileBytes);
-        const CUtensorMap* tm = (u & 1) ? &tmV : &tmK;
+    uint32_t qbytes = 0;
+    for (int t = 0; t < 2; ++t)
+      if (valid_t[t]) qbytes += C::kTileBytes;
+    if (lane == 0 && qbytes != 0 && nmax > 0) {
+      mbar_arrive_expect_tx(bar(BAR_Q), qbytes);
+      for (int t = 0; t < 2; ++t) {
+        if (!valid_t[t]) continue;
         for (int s = 0; s < C::kSub; ++s)
-          load_rows(sbase + C::kOffKV + slot * C::kTileBytes + s * C::kSubBytes, tm, bar(BAR_KV_FULL + slot), s * 64,
-                    (u >> 1) * kKeys);
-        issued = u + 1;
+          load_rows(sbase + C::kOffQ + t * C::kTileBytes + s * C::kSubBytes, &tmQ, bar(BAR_Q), s * 64,
+                    (2 * mblk + t) * kRows);
       }
+    }
+    // Paged K/V: a 128-key tile is gathered as `boxes` boxes of box_rows cache
+    // rows, each inside one physical block (one block-table entry), and lane r
+    // issues box r.  The warp keeps the block-table row in registers, 32
+    // entries (one per lane) at a time: the window of the current tile and,
+    // loaded one window ahead, the next, so no table read sits on the issue
+    // path.  A tile's entries never straddle two windows (128 / block_size
+    // divides 32, or one entry per tile).  A box past kv_len, or whose entry is
+    // outside [0, num_blocks), reads the zero fill past the last cache row, so
+    // masked keys and values stay finite; a bad entry is also recorded in the
+    // status word.
+    const int32_t* trow = paged ? args.block_table + static_cast<size_t>(b) * args.max_blocks : nullptr;
+    const int n_entries = paged ? (kv_len + args.block_size - 1) / args.block_size : 0;
+    const int boxes = paged ? kKeys / args.box_rows : 0;
+    auto table_window = [&](int w) -> int {
+      const int e = 32 * w + lane;
+      return (e < n_entries) ? trow[e] : -1;
+    };
+    int win = 0, cur = -1, nxt = -1;
+    if (paged) {
+      cur = table_window(0);
+      nxt = table_window(1);
+    }
+    int crow = args.num_rows;  // cache row of this lane's box in the current key tile
+    bool bad_table = false;
+    int issued = 0;
+    for (int u = 0; u < 2 * nmax; ++u) {
+      const int slot = u % C::kSlots;
+      const uint32_t ph = static_cast<uint32_t>(u / C::kSlots) & 1u;
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(bar(BAR_KV_EMPTY + slot), ph ^ 1u, wc) ? 1 : 0;
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      const uint32_t dst = sbase + C::kOffKV + slot * C::kTileBytes;
+      const CUtensorMap* tm = (u & 1) ? &tmV : &tmK;
+      if (lane == 0) mbar_arrive_expect_tx(bar(BAR_KV_FULL + slot), C::kTileBytes);
+      if (paged) {
+        if ((u & 1) == 0) {  // K and V of a key tile share its boxes
+          const int key0 = (u >> 1) * kKeys;
+          const int e0 = key0 / args.block_size;
+          if ((e0 >> 5) != win) {
+            cur = ((e0 >> 5) == win + 1) ? nxt : table_window(e0 >> 5);
+            win = e0 >> 5;
+            nxt = table_window(win + 1);
+          }
+          const int entry = __shfl_sync(0xffffffffu, cur, ((e0 & 31) + lane) & 31);
+          crow = args.num_rows;
+          const int key = key0 + lane * args.box_rows;
+          if (lane < boxes && key < kv_len) {
+            if (entry >= 0 && entry < args.num_blocks)
+              crow = entry * args.block_size + key % args.block_size;
+            else
+              bad_table = true;
+          }
+        }
+        __syncwarp();  // the transaction count is armed before any box lands
+        if (lane < boxes) {
+          for (int s = 0; s < C::kSub; ++s)
+            tma_load_3d(dst + s * C::kSubBytes + lane * args.box_rows * 128, tm, bar(BAR_KV_FULL + slot), s * 64,
+                        kv_head, crow);
+        }
+      } else if (lane == 0) {
+        for (int s = 0; s < C::kSub; ++s)
+          load_rows(dst + s * C::kSubBytes, tm, bar(BAR_KV_FULL + slot), s * 64, (u >> 1) * kKeys);
+      }
+      issued = u + 1;
+    }
+    if (__any_sync(0xffffffffu, bad_table) && lane == 0) atomicOr(args.status, kStatusBadTableBit);
+    if (lane == 0) {
       // let every issued copy land before the CTA can exit
       if (qbytes != 0 && nmax > 0) drain_wait(bar(BAR_Q), 0);
       for (int s = 0; s < C::kSlots && s < issued; ++s) {
@@ -308,12 +379,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tO = tmem + lane_off + C::col_o(t);
     const float sl2 = args.scale_log2;
     int last_key = kv_len - 1;
-    if (args.causal) last_key = min(last_key, row);
+    if (args.causal) last_key = min(last_key, qoff + row);
 
     float m_ref = -INFINITY;
     float l_sum = 0.f;
     bool aborted = false;
-    const int n = n_t[t];
+    const int n = (t == 0) ? n_t[0] : n_t[1];  // selects, not a runtime-indexed (stack) array
+    const bool valid = (t == 0) ? valid_t[0] : valid_t[1];
     for (int j = 0; j < n; ++j) {
       if (!mbar_wait(bar(BAR_S_FULL + t), static_cast<uint32_t>(j) & 1u, wc)) {
         aborted = true;
@@ -376,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(bar(BAR_P_FULL + t));
     }
 
-    if (valid_t[t] && !aborted) {
+    if (valid && !aborted) {
       bool have_o = n > 0;
       if (have_o) {
         have_o = mbar_wait(bar(BAR_O_FINAL + t), 0, wc);
@@ -446,7 +518,7 @@ fa_status fwd_launch_d(const void* Q, const void* K, const void* V, void* O, flo
   }
   unsigned* status = device_status_ptr();
   if (status == nullptr) return FA_ERR_CUDA;
-  FwdArgs a;
+  FwdArgs a{};  // zero: no paged K/V
   a.O = O;
   a.LSE = LSE;
   a.kv_lens = kv_lens;
@@ -483,7 +555,7 @@ fa_status fwd_varlen_launch_d(const void* Q, const void* K, const void* V, void*
   }
   unsigned* status = device_status_ptr();
   if (status == nullptr) return FA_ERR_CUDA;
-  FwdArgs a;
+  FwdArgs a{};  // zero: no paged K/V
   a.O = O;
   a.LSE = LSE;
   a.kv_lens = nullptr;
@@ -499,7 +571,74 @@ fa_status fwd_varlen_launch_d(const void* Q, const void* K, const void* V, void*
   return launch_status();
 }
 
+template <int D>
+fa_status fwd_paged_launch_d(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                             const int32_t* cu_seqlens_q, const int32_t* seq_lens_k, void* o, float* lse,
+                             int num_seqs, int total_q, int max_seqlen_q, int Hq, int Hkv, int num_blocks,
+                             int block_size, int max_blocks, int causal, float scale, cudaStream_t stream) {
+  using C = FwdCfg<D>;
+  // queries packed [total_q, Hq, D] as in the ragged forward; the caches
+  // [num_blocks, block_size, Hkv, D] as TMA dims (D, Hkv, num_blocks * block_size),
+  // boxes of min(block_size, 128) rows of one KV head
+  const int box_rows = block_size < kKeys ? block_size : kKeys;
+  const uint64_t qdims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(Hq), static_cast<uint64_t>(total_q)};
+  const uint64_t qstrides[2] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(Hq) * D * 2};
+  const uint32_t qbox[3] = {64, 1, kRows};
+  const int num_rows = num_blocks * block_size;
+  const uint64_t kdims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(Hkv), static_cast<uint64_t>(num_rows)};
+  const uint64_t kstrides[2] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(Hkv) * D * 2};
+  const uint32_t kbox[3] = {64, 1, static_cast<uint32_t>(box_rows)};
+  CUtensorMap tq, tk, tv;
+  if (!encode_bf16_tmap(&tq, q, 3, qdims, qstrides, qbox) || !encode_bf16_tmap(&tk, k_cache, 3, kdims, kstrides, kbox) ||
+      !encode_bf16_tmap(&tv, v_cache, 3, kdims, kstrides, kbox))
+    return FA_ERR_CUDA;
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
+      return FA_ERR_CUDA;
+    attr_set = true;
+  }
+  unsigned* status = device_status_ptr();
+  if (status == nullptr) return FA_ERR_CUDA;
+  FwdArgs a{};
+  a.O = o;
+  a.LSE = lse;
+  a.kv_lens = seq_lens_k;
+  a.cu_seqlens = cu_seqlens_q;
+  a.total = total_q;
+  a.H = Hq;
+  a.N = max_seqlen_q;
+  a.causal = causal ? 1 : 0;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.status = status;
+  a.block_table = block_table;
+  a.max_blocks = max_blocks;
+  a.block_size = block_size;
+  a.box_rows = box_rows;
+  a.num_rows = num_rows;
+  a.num_blocks = num_blocks;
+  a.group = Hq / Hkv;
+  dim3 grid(Hq, ceil_div(max_seqlen_q, 2 * kRows), num_seqs);
+  fwd_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, a);
+  return launch_status();
+}
+
 }  // namespace
+
+fa_status fwd_paged_launch(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                           const int32_t* cu_seqlens_q, const int32_t* seq_lens_k, void* o, float* lse,
+                           int num_seqs, int total_q, int max_seqlen_q, int Hq, int Hkv, int d, int num_blocks,
+                           int block_size, int max_blocks, int causal, float scale, cudaStream_t stream) {
+  if (d == 64)
+    return fwd_paged_launch_d<64>(q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens_k, o, lse, num_seqs,
+                                  total_q, max_seqlen_q, Hq, Hkv, num_blocks, block_size, max_blocks, causal, scale,
+                                  stream);
+  if (d == 128)
+    return fwd_paged_launch_d<128>(q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens_k, o, lse, num_seqs,
+                                   total_q, max_seqlen_q, Hq, Hkv, num_blocks, block_size, max_blocks, causal, scale,
+                                   stream);
+  return FA_ERR_UNSUPPORTED;
+}
 
 fa_status fwd_varlen_launch(const void* Q, const void* K, const void* V, void* O, float* LSE,
                             const int32_t* cu_seqlens, int num_seqs, int total, int max_seqlen, int H, int d,

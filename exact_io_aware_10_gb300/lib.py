@@ -32,6 +32,7 @@ SIGNATURES = {
     "fa_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp]),
     "fa_fwd_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp, _vp]),
     "fa_fwd_varlen": (_i, [_vp] * 6 + [_i, _i, _i, _i, _i, _i, _f, _vp]),
+    "fa_paged_prefill": (_i, [_vp] * 8 + [_i] * 10 + [_f, _vp]),
     "fa_bwd_workspace_size": (_sz, [_i, _i, _i, _i]),
     "fa_bwd": (_i, [_vp] * 9 + [_i, _i, _i, _i, _i, _f, _vp, _vp, _sz, _vp]),
     "fa_paged_decode_workspace_size": (_sz, [_i, _i, _i, _i]),
@@ -219,6 +220,42 @@ def fa_paged_decode(q, k_cache, v_cache, block_table, seq_lens, scale=None, num_
                              B, Hq, Hkv, d, bs, max_blocks, NB, int(num_splits), scale, _p(workspace),
                              workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st, "fa_paged_decode")
+    return o, lse
+
+
+def fa_paged_prefill(q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens_k, max_seqlen_q, causal=True,
+                     scale=None, o=None, lse=None, stream=None):
+    """Chunked prefill over a paged KV cache: o [total_q, Hq, d] bf16 and
+    lse [Hq, total_q] fp32 for query chunks packed by cu_seqlens_q (CUDA int32
+    [num_seqs + 1]); chunk s is the last tokens of a context of
+    seq_lens_k[s] keys (bottom-right causal alignment)."""
+    lib = load()
+    total_q, Hq, d = q.shape
+    NB, bs, Hkv, d2 = k_cache.shape
+    _need(q, torch.bfloat16, None, "q")
+    _need(k_cache, torch.bfloat16, None, "k_cache")
+    _need(v_cache, torch.bfloat16, (NB, bs, Hkv, d2), "v_cache")
+    _need(block_table, torch.int32, None, "block_table")
+    _need(cu_seqlens_q, torch.int32, None, "cu_seqlens_q")
+    if d2 != d:
+        raise ValueError("k_cache head dimension must match q")
+    if cu_seqlens_q.dim() != 1 or cu_seqlens_q.numel() < 2:
+        raise ValueError("cu_seqlens_q must be 1-D with num_seqs + 1 >= 2 entries")
+    num_seqs = cu_seqlens_q.numel() - 1
+    _need(seq_lens_k, torch.int32, (num_seqs,), "seq_lens_k")
+    if block_table.dim() != 2 or block_table.shape[0] != num_seqs:
+        raise ValueError("block_table must be [num_seqs, max_blocks]")
+    max_blocks = int(block_table.shape[1])
+    o = torch.empty_like(q) if o is None else o
+    _need(o, torch.bfloat16, (total_q, Hq, d), "o")
+    if lse is None:
+        lse = torch.empty((Hq, total_q), dtype=torch.float32, device=q.device)
+    _need(lse, torch.float32, (Hq, total_q), "lse")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    st = lib.fa_paged_prefill(_p(q), _p(k_cache), _p(v_cache), _p(block_table), _p(cu_seqlens_q), _p(seq_lens_k),
+                              _p(o), _p(lse), num_seqs, total_q, int(max_seqlen_q), Hq, Hkv, d, NB, bs, max_blocks,
+                              int(bool(causal)), scale, _stream(stream))
+    _check(st, "fa_paged_prefill")
     return o, lse
 
 

@@ -100,6 +100,46 @@ int fa_fwd_varlen(const void* Q, const void* K, const void* V, void* O, float* L
                   int num_seqs, int total, int max_seqlen, int H, int d, int causal, float scale, void* stream);
 
 /*
+ * Paged (chunked) prefill: a packed batch of query chunks, each attending to
+ * its sequence's keys and values in a paged KV cache.  This is the tiled
+ * forward with its key tiles fetched through the block table, as the S12
+ * chapter's "除了快，它还解锁了什么" (PagedAttention bullet) and "实现"
+ * describe, with grouped-query heads.
+ *   q            : [total_q, Hq, d] bf16; chunk s is rows cu_seqlens_q[s] ..
+ *                  cu_seqlens_q[s+1]-1 (offsets as in fa_fwd_varlen).
+ *   k_cache,
+ *   v_cache      : [num_blocks, block_size, Hkv, d] bf16 (the decode layout).
+ *                  Cache rows of a sequence's blocks past seq_lens_k are read
+ *                  and masked, so they must hold finite values.
+ *   block_table  : [num_seqs, max_blocks] int32; entries past
+ *                  ceil(seq_lens_k[s] / block_size) are never read.  An entry
+ *                  outside [0, num_blocks) reads as zero keys and values and
+ *                  latches FA_ERR_BAD_BLOCK_TABLE (that sequence's results are
+ *                  then meaningless).
+ *   seq_lens_k   : [num_seqs] int32 context length kv_len of each sequence:
+ *                  its cached prefix plus the chunk, 0 <= kv_len <=
+ *                  max_blocks * block_size.  The chunk is the LAST q_len tokens
+ *                  of the context: query i sits at position kv_len - q_len + i
+ *                  and, when causal, sees keys j <= kv_len - q_len + i
+ *                  (bottom-right alignment; q_len = kv_len is fa_fwd_varlen's
+ *                  square mask, q_len = 1 is decode).  Rows that see no key
+ *                  (q_len > kv_len) get O = 0 and LSE = -inf.
+ *   o            : [total_q, Hq, d] bf16, written.   lse: [Hq, total_q] fp32.
+ *   Query head h reads KV head h / (Hq / Hkv); Hq % Hkv must be 0.
+ *   block_size   : a multiple of 8 that divides 128 or is a multiple of 128,
+ *                  else FA_ERR_UNSUPPORTED.
+ *   max_seqlen_q : an upper bound of the longest chunk (it sizes the grid).
+ * num_seqs in [1, 65535].  Errors: FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED,
+ * FA_ERR_CUDA; a chunk with bad offsets, longer than max_seqlen_q or with
+ * kv_len outside its table row is skipped on the device and
+ * fa_get_device_status() returns FA_ERR_INVALID_ARG.
+ */
+int fa_paged_prefill(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                     const int32_t* cu_seqlens_q, const int32_t* seq_lens_k, void* o, float* lse, int num_seqs,
+                     int total_q, int max_seqlen_q, int Hq, int Hkv, int d, int num_blocks, int block_size,
+                     int max_blocks, int causal, float scale, void* stream);
+
+/*
  * Bytes of device workspace fa_bwd needs: two fp32 [B, H, Npad] row buffers
  * (D = rowsum(dO * O) and LSE in log2 units; Npad = N rounded up to 128) and
  * an fp32 [B, H, N, d] dQ accumulator, each rounded up to 256 bytes.

@@ -92,22 +92,25 @@ def paged_prefill_rows(q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens_
     """O [len(heads), len(rows), d] and LSE [len(heads), len(rows)] of chunk
     b's query ``rows`` for the given query heads: the same definition as
     paged_prefill, evaluated only where the full problem is too large."""
-    kc, vc = to_f64(k_cache), to_f64(v_cache)
     bt, cu, sl = _np_int(block_table), _np_int(cu_seqlens_q), _np_int(seq_lens_k)
     a, e = int(cu[b]), int(cu[b + 1])
     q_len, kv_len = e - a, int(sl[b])
     d = q.shape[2]
-    Hq, Hkv = q.shape[1], kc.shape[2]
+    Hq, Hkv = q.shape[1], k_cache.shape[2]
     grp = Hq // Hkv
     scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
     rows = np.asarray(rows)
     mask = chunk_key_mask(q_len, kv_len, causal)[rows]
-    O = np.zeros((len(heads), len(rows), vc.shape[3]))
+    O = np.zeros((len(heads), len(rows), v_cache.shape[3]))
     LSE = np.full((len(heads), len(rows)), NEG_INF)
+    # the same block-table gather as gather_paged_keys, done before widening
+    # so that only this sequence's rows are converted to fp64
+    tok = np.arange(kv_len)
+    phys = bt[b][tok // block_size]
     for t, h in enumerate(heads):
         g = h // grp
-        Kb = gather_paged_keys(kc, bt[b], kv_len, block_size, g)
-        Vb = gather_paged_keys(vc, bt[b], kv_len, block_size, g)
+        Kb = to_f64(k_cache[phys, tok % block_size, g])
+        Vb = to_f64(v_cache[phys, tok % block_size, g])
         qh = to_f64(q[a:e, h])[rows]
         S = scale * (qh @ Kb.T)
         for r in range(len(rows)):

@@ -43,7 +43,7 @@ def test_status_strings(so):
                        (4, "FA_ERR_TIMEOUT"), (5, "FA_ERR_BAD_BLOCK_TABLE")]:
         assert so.fa_status_string(code).decode() == name
     assert so.fa_status_string(99).decode() == "FA_ERR_UNKNOWN"
-    assert so.fa_version() == 101
+    assert so.fa_version() == 102
 
 
 def _fake(n=1):
@@ -87,6 +87,37 @@ def test_varlen_forward_argument_validation(so):
     assert f(Q, K, V, O, L, cu, 65536, 100, 64, 4, 64, 0, 0.1, s) == fl.FA_ERR_UNSUPPORTED
     # an empty batch is a valid no-op and launches nothing
     assert f(Q, K, V, O, L, cu, 2, 0, 0, 4, 64, 0, 0.1, s) == fl.FA_OK
+
+
+def test_paged_prefill_argument_validation(so):
+    q, kc, vc, bt, cu, sl, o, lse = _fake(8)
+    s = ctypes.c_void_p(0)
+
+    def call(**kw):
+        a = dict(num_seqs=2, total_q=100, max_seqlen_q=64, Hq=8, Hkv=2, d=128, num_blocks=10, block_size=16,
+                 max_blocks=4, causal=1, scale=0.1)
+        a.update(kw)
+        return so.fa_paged_prefill(a.get("q", q), kc, vc, a.get("bt", bt), cu, sl, o, lse, a["num_seqs"],
+                                   a["total_q"], a["max_seqlen_q"], a["Hq"], a["Hkv"], a["d"], a["num_blocks"],
+                                   a["block_size"], a["max_blocks"], a["causal"], a["scale"], s)
+
+    assert call(d=96) == fl.FA_ERR_UNSUPPORTED
+    assert call(Hkv=3) == fl.FA_ERR_INVALID_ARG          # Hq % Hkv != 0
+    assert call(num_seqs=0) == fl.FA_ERR_INVALID_ARG
+    assert call(total_q=-1) == fl.FA_ERR_INVALID_ARG
+    assert call(num_blocks=0) == fl.FA_ERR_INVALID_ARG
+    assert call(max_blocks=0) == fl.FA_ERR_INVALID_ARG
+    assert call(scale=-1.0) == fl.FA_ERR_INVALID_ARG
+    for bad_bs in (4, 12, 24, 48, 136, 200):            # not a multiple of 8 dividing 128 or of 128
+        assert call(block_size=bad_bs) == fl.FA_ERR_UNSUPPORTED, bad_bs
+    for good_bs in (8, 16, 32, 64, 128, 256, 384):
+        assert call(block_size=good_bs, total_q=0) == fl.FA_OK, good_bs
+    assert call(num_seqs=65536) == fl.FA_ERR_UNSUPPORTED
+    assert call(num_blocks=1 << 27) == fl.FA_ERR_UNSUPPORTED  # cache rows past int32
+    assert call(q=None) == fl.FA_ERR_INVALID_ARG
+    assert call(bt=None) == fl.FA_ERR_INVALID_ARG
+    assert call(q=ctypes.c_void_p(0x10000002)) == fl.FA_ERR_INVALID_ARG
+    assert call(total_q=0) == fl.FA_OK                  # no-op
 
 
 def test_backward_argument_validation(so):
