@@ -66,9 +66,9 @@ NOMINAL = {"bf16_tflops": 2250.0, "hbm_gbs": 8000.0}
 # ncu dram bytes (read + write) per launch of the dominant kernel, with the
 # hash of the kernel source they were taken on (null once the source changes)
 TRAFFIC_RECORD = {"kernel": "fwd_kernel<128>", "source": "exact_io_aware_10_gb300/csrc/fa_fwd.cu",
-                  "sha256": "d1437597a63a3a755449c92bdebb8a39a44893d7551b18c8aa4bf9e50cfac9d5",
-                  "bytes_per_launch_N16384": 546389504 + 49661952,
-                  "bytes_per_launch_N65536": 7735814656 + 270459136}
+                  "sha256": "bd79231d50e7841c2a285b6e2779ae8e73f29a564ce32c436160aaa2bebd930b",
+                  "bytes_per_launch_N16384": 543019776 + 45682176,
+                  "bytes_per_launch_N65536": 7765754112 + 252772608}
 
 
 def load_peaks():

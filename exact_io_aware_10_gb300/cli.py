@@ -4,7 +4,7 @@ profiler:  python -m exact_io_aware_10_gb300.cli fwd --N 16384 --iters 2
 Subcommands: fwd, bwd (runs fwd once to produce O/LSE, then bwd), decode,
 varlen (packed ragged batch of --num-seqs sequences, lengths U[--seq-lo, --seq-hi]),
 prefill (paged chunked prefill: --num-seqs chunks of --chunk tokens after cached
-prefixes of U[0, --prefix-hi] tokens, --Hq/--Hkv heads, 16-token blocks).
+prefixes of U[0, --prefix-hi] tokens, --Hq/--Hkv heads, --block-size-token blocks).
 Prints the CUDA-event time of the last iteration.
 """
 from __future__ import annotations
@@ -41,6 +41,7 @@ def main(argv=None):
     ap.add_argument("--seq-hi", type=int, default=16384)
     ap.add_argument("--chunk", type=int, default=2048)
     ap.add_argument("--prefix-hi", type=int, default=30720)
+    ap.add_argument("--block-size", type=int, default=16)
     a = ap.parse_args(argv)
     dev = torch.device("cuda")
     lib.load()
@@ -74,11 +75,12 @@ def main(argv=None):
         g = torch.Generator().manual_seed(a.seed)
         prefix = torch.randint(0, a.prefix_hi + 1, (a.num_seqs,), generator=g).tolist()
         kv = [p + a.chunk for p in prefix]
-        sl, table, NB, _ = wl.paged_layout(a.num_seqs, 0, 0, 16, a.seed, None, kv)
+        bs = a.block_size
+        sl, table, NB, _ = wl.paged_layout(a.num_seqs, 0, 0, bs, a.seed, None, kv)
         cu = torch.arange(0, (a.num_seqs + 1) * a.chunk, a.chunk, dtype=torch.int32, device=dev)
         q = wl.device_normal_bf16((a.num_seqs * a.chunk, a.Hq, a.d), a.seed + 1, dev)
-        kc = wl.device_normal_bf16((NB, 16, a.Hkv, a.d), a.seed + 2, dev)
-        vc = wl.device_normal_bf16((NB, 16, a.Hkv, a.d), a.seed + 3, dev)
+        kc = wl.device_normal_bf16((NB, bs, a.Hkv, a.d), a.seed + 2, dev)
+        vc = wl.device_normal_bf16((NB, bs, a.Hkv, a.d), a.seed + 3, dev)
         sl, table = sl.to(dev), table.to(dev)
         o, lse = lib.fa_paged_prefill(q, kc, vc, table, cu, sl, a.chunk, causal=causal)
         for _ in range(a.iters):
