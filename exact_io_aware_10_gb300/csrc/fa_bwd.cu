@@ -20,8 +20,9 @@
 //                        dK_j += dS^T Q_i          (A = dS^T from shared memory)
 //                        dQ_i^T = K_j^T dS^T       (d = 128: lanes = head dim, over dP^T)
 //                        dQ_i   = dS K_j           (d = 64: lanes = queries, over dP^T)
-//                      MMA order per tile: dV_i, S_{i+1}, dK_i, dQ_i, dP_{i+1}, so
-//                      the next tile's scores are ready while dS_i is formed.
+//                      MMA order per tile: dV_i, dK_i, dQ_i, S_{i+1}, dP_{i+1}:
+//                      dQ_i is ready for read-out as soon as dS_i is, and the
+//                      next tile's scores run while dQ_i is staged.
 //                      dQ_i is added into the fp32 accumulator in L2: at
 //                      d = 128 by one TMA bulk reduction of a 128 x 32 box per
 //                      compute warpgroup, staged in shared memory, at d = 64 by
@@ -361,13 +362,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                    (it > 0 || k > 0) ? 1u : 0u);
           }
           mma_commit(bar(BAR_DO_EMPTY));
-          // S_{i+1} = K_j Q_{i+1}^T over the S^T columns (after dV has read P^T)
-          if (next) {
-            if (!(ok = mbar_wait(bar(BAR_Q_FULL + ((it + 1) & 1)), ((it + 1) >> 1) & 1, wc))) break;
-            tc_fence_after();
-            mma_kmajor_d(C::kColS, kK, kq(it + 1));
-            mma_commit(bar(BAR_S));
-          }
           // dK_j += dS^T Q_i  and  dQ_i over the dP^T columns
           if (!(ok = mbar_wait(bar(BAR_DS), it & 1, wc))) break;
           tc_fence_after();
@@ -392,6 +386,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mma_commit(bar(BAR_DQ_FULL));
           mma_commit(bar(BAR_Q_EMPTY + (it & 1)));
+          // S_{i+1} = K_j Q_{i+1}^T over the S^T columns (after dV has read P^T).
+          // Issued behind dK_i and dQ_i, so dQ_i reaches the compute warps (which
+          // read it out next) without waiting for S_{i+1}.
+          if (next) {
+            if (!(ok = mbar_wait(bar(BAR_Q_FULL + ((it + 1) & 1)), ((it + 1) >> 1) & 1, wc))) break;
+            tc_fence_after();
+            mma_kmajor_d(C::kColS, kK, kq(it + 1));
+            mma_commit(bar(BAR_S));
+          }
           // dP_{i+1} = V_j dO_{i+1}^T over the dP^T columns (after dQ_i has been read out)
           if (next) {
             if (!(ok = mbar_wait(bar(BAR_DO_FULL), (it + 1) & 1, wc))) break;
