@@ -47,6 +47,10 @@ from .paged_prefill import (  # noqa: F401
     paged_prefill,
     paged_prefill_rows,
 )
+from .block_sparse import (  # noqa: F401
+    expand_block_mask,
+    block_sparse_forward,
+)
 from .io_model import (  # noqa: F401
     standard_hbm_accesses,
     flash_hbm_accesses,
