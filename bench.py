@@ -58,6 +58,9 @@ VARLEN = {
 # tokens (GQA heads, 16-token blocks, seeded random block placement)
 PAGED_PREFILL = dict(num_seqs=16, q_len=2048, prefix_lo=0, prefix_hi=30720, Hq=32, Hkv=8, d=128, block_size=16,
                      config_id=7)
+# block-sparse forward, timed after the step on the long-context shapes: a
+# butterfly mask plus a local window of BLOCK_SPARSE_WINDOW key blocks
+BLOCK_SPARSE_WINDOW = 15
 WORKLOAD = ("long-context causal prefill B1 H16 d128 (fwd+bwd N=16384, fwd N=65536) + paged GQA decode "
             "B64 Hq32 Hkv8 d128 L~U[512,32768] block16 splits16")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -334,6 +337,30 @@ def time_paged_prefill(dev, seed, steps, warmup, barrier, max_over_ranks, world,
     return out
 
 
+def time_block_sparse(w, steps, warmup, barrier, max_over_ranks, world, peak_tf, part_ms):
+    """TFLOP/s (useful FLOPs: visible pairs of kept blocks) of the block-sparse
+    forward at N = 16384 and 65536 on the step's own inputs, with its speed-up
+    over the dense forward of the same step."""
+    P = PREFILL
+    out = {"mask": f"butterfly + local window of {BLOCK_SPARSE_WINDOW} key blocks, 128 x 128 blocks, causal"}
+    for tag, (Q, K, V, O, L, dense_part) in {"N16384": (w.Q, w.K, w.V, w.O, w.L, "fwd16"),
+                                             "N65536": (w.Q64, w.K64, w.V64, w.O64, w.L64, "fwd64")}.items():
+        N = Q.shape[2]
+        m = wl.block_mask(N // 128, "butterfly", window=BLOCK_SPARSE_WINDOW)
+        flops = acc.block_sparse_flops(m.numpy(), P["B"], P["H"], N, P["d"], True)
+        md = m.to(Q.device)
+        _, ms = time_parts(lambda p: w.lib.fa_fwd_block_sparse(Q, K, V, md, causal=True, O=O, LSE=L), ("bs",),
+                           steps, warmup, barrier)
+        assert w.lib.fa_get_device_status() == w.lib.FA_OK, "device status word reported an error"
+        t = max_over_ranks(ms["bs"])
+        tf = world * steps * flops / (t * 1e-3) / 1e12
+        out[tag] = {"kept_fraction_of_causal_pairs": flops / acc.fwd_flops(P["B"], P["H"], N, P["d"], True),
+                    "flops": flops, "TFLOP/s": tf, "frac": tf / world / peak_tf,
+                    "frac_of_nominal": tf / world / NOMINAL["bf16_tflops"], "ms": t / steps,
+                    "speedup_vs_dense_forward": (part_ms[dense_part] / steps) / (t / steps)}
+    return out
+
+
 class HostBuffers:
     """Pinned host copies of a step's inputs and outputs for the end-to-end run."""
 
@@ -491,6 +518,8 @@ def run_ours(args):
         next_rows = time_varlen(dev, args.seed, args.steps, args.warmup, barrier, max_over_ranks, world, peak_tf)
         next_rows["paged_prefill"] = time_paged_prefill(dev, args.seed, args.steps, args.warmup, barrier,
                                                         max_over_ranks, world, peak_tf)
+        next_rows["block_sparse"] = time_block_sparse(w, args.steps, args.warmup, barrier, max_over_ranks, world,
+                                                      peak_tf, part_ms)
         next_rows["note"] = "timed after the step, outside value and ms_per_step; TFLOP/s count useful FLOPs only"
 
     cpu = None
@@ -597,7 +626,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--skip-next-rows", action="store_true",
-                    help="skip the ragged-batch forward and paged-prefill timings")
+                    help="skip the ragged-batch, paged-prefill and block-sparse timings")
     ap.add_argument("--ref-prefix", type=int, default=2048)
     args = ap.parse_args()
     if args.warmup < 3:

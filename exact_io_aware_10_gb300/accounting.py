@@ -6,6 +6,9 @@ Conventions (matmul work only; exp, masking and reductions are not counted):
   key padding: the effective forward count is 4 * H * N * d * sum_b L_b
   packed ragged batch: the sum of the forward count of every sequence,
             4 * H * d * sum_s L_s^2, halved when causal
+  block-sparse: 4 * H * d per visible (query, key) pair of the kept blocks
+            (counted per block: the pairs of a block that lie inside N and,
+            when causal, on or below the diagonal)
   paged chunked prefill: 4 * Hq * d per visible (query, key) pair, counted
             exactly: a causal chunk of q rows after a prefix of p keys has
             q * p + q (q + 1) / 2 pairs; non-causal q * (p + q)
@@ -50,6 +53,24 @@ def paged_prefill_flops(q_lens, kv_lens, Hq, d, causal=True):
             for_rows = max(r, 0) * (max(r, 0) + 1) // 2
         pairs += for_rows
     return 4.0 * Hq * d * pairs
+
+
+def block_sparse_flops(block_mask, B, H, N, d, causal=True, block=128):
+    """block_mask: [nb, nb] (shared) or [B, H, nb, nb] array-like of 0/1."""
+    import numpy as np
+
+    m = np.asarray(block_mask).astype(bool)
+    nb = m.shape[-1]
+    qi = np.arange(nb)
+    rows = np.minimum(block, N - qi * block)  # valid rows (and keys) per block
+    pairs = rows[:, None] * rows[None, :]
+    if causal:
+        diag = rows * (rows + 1) // 2
+        pairs = np.where(qi[:, None] > qi[None, :], pairs, 0)
+        pairs[qi, qi] = diag
+    per_mask = (m * pairs).reshape(-1, nb, nb).sum(axis=(1, 2))
+    total = per_mask.sum() * (B * H if m.ndim == 2 else 1)
+    return 4.0 * d * float(total)
 
 
 def fwd_bytes(B, H, N, d):

@@ -1,7 +1,8 @@
 """Run one attention entry point on seeded synthetic inputs, e.g. for a
 profiler:  python -m exact_io_aware_10_gb300.cli fwd --N 16384 --iters 2
 
-Subcommands: fwd, bwd (runs fwd once to produce O/LSE, then bwd), decode,
+Subcommands: fwd (block-sparse with --sparse-window W: butterfly mask plus W
+local key blocks), bwd (runs fwd once to produce O/LSE, then bwd), decode,
 varlen (packed ragged batch of --num-seqs sequences, lengths U[--seq-lo, --seq-hi]),
 prefill (paged chunked prefill: --num-seqs chunks of --chunk tokens after cached
 prefixes of U[0, --prefix-hi] tokens, --Hq/--Hkv heads, --block-size-token blocks).
@@ -42,6 +43,7 @@ def main(argv=None):
     ap.add_argument("--chunk", type=int, default=2048)
     ap.add_argument("--prefix-hi", type=int, default=30720)
     ap.add_argument("--block-size", type=int, default=16)
+    ap.add_argument("--sparse-window", type=int, default=None)
     a = ap.parse_args(argv)
     dev = torch.device("cuda")
     lib.load()
@@ -51,9 +53,14 @@ def main(argv=None):
         shp = (a.B, a.H, a.N, a.d)
         Q, K, V, dO = (wl.device_normal_bf16(shp, a.seed + i, dev) for i in range(4))
         O, L = lib.fa_fwd(Q, K, V, causal=causal)
+        mask = None
+        if a.sparse_window is not None:
+            mask = wl.block_mask((a.N + 127) // 128, "butterfly", window=a.sparse_window).to(dev)
         for _ in range(a.iters):
             start.record()
-            if a.op == "fwd":
+            if a.op == "fwd" and mask is not None:
+                lib.fa_fwd_block_sparse(Q, K, V, mask, causal=causal, O=O, LSE=L)
+            elif a.op == "fwd":
                 lib.fa_fwd(Q, K, V, causal=causal, O=O, LSE=L)
             else:
                 lib.fa_bwd(Q, K, V, O, dO, L, causal=causal)

@@ -145,14 +145,28 @@ const char* fa_status_string(int status) {
   }
 }
 
-int fa_version(void) { return 102; }
+int fa_version(void) { return 103; }
 
 int fa_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d, int causal,
               float scale, const int32_t* kv_lens, void* stream) {
   int st = check_attn(Q, K, V, O, LSE, B, H, N, d, scale);
   if (st != FA_OK || N == 0) return st;
   if (B > 65535) return FA_ERR_UNSUPPORTED;  // batch entries are the grid's z dimension
-  return fa::fwd_launch(Q, K, V, O, LSE, B, H, N, d, causal, scale, kv_lens, static_cast<cudaStream_t>(stream));
+  return fa::fwd_launch(Q, K, V, O, LSE, B, H, N, d, causal, scale, kv_lens, nullptr, 0,
+                        static_cast<cudaStream_t>(stream));
+}
+
+int fa_fwd_block_sparse(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d,
+                        int causal, float scale, const int32_t* kv_lens, const uint8_t* block_mask,
+                        int mask_per_head, void* stream) {
+  int st = check_attn(Q, K, V, O, LSE, B, H, N, d, scale);
+  if (st != FA_OK || N == 0) return st;
+  if (block_mask == nullptr) return FA_ERR_INVALID_ARG;
+  if (B > 65535 || N > fa::kBlockSparseMaxN) return FA_ERR_UNSUPPORTED;
+  const long long nb = (static_cast<long long>(N) + 127) / 128;
+  const long long stride = mask_per_head ? nb * nb : 0;
+  return fa::fwd_launch(Q, K, V, O, LSE, B, H, N, d, causal, scale, kv_lens, block_mask, stride,
+                        static_cast<cudaStream_t>(stream));
 }
 
 int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d, int causal,

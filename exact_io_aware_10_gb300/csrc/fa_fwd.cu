@@ -53,7 +53,8 @@ struct FwdCfg {
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = kOffQ + 2 * kTileBytes;
   static constexpr int kOffBar = kOffKV + kSlots * kTileBytes;
-  static constexpr int kSmemBytes = kOffBar + 256 + 1024;  // barriers + alignment slack
+  static constexpr int kOffMask = kOffBar + 256;  // block-sparse key-tile bitmasks and counts
+  static constexpr int kSmemBytes = kOffMask + 1024 + 1024;  // + alignment slack
   static constexpr uint32_t kTmemCols = 512;
   // TMEM columns: S of tile t at 128 t, O of tile t at 256 + D t
   __device__ static constexpr uint32_t col_s(int t) { return 128u * static_cast<uint32_t>(t); }
@@ -72,6 +73,9 @@ enum : int {
   kNumBars = 24,
 };
 constexpr int kOffTmemSlot = kNumBars * 8;
+// block-sparse: bitmasks over at most kMaskWords * 32 key tiles (union of the
+// CTA's two query tiles, then each tile's own row), then the two stream counts
+constexpr int kMaskWords = 64;
 constexpr int kOffAbort = kOffTmemSlot + 4;
 
 struct FwdArgs {
@@ -93,6 +97,12 @@ struct FwdArgs {
   // of the (D, Hkv, num_rows) tensor maps; query head h reads KV head h / group
   const int32_t* block_table;
   int max_blocks, block_size, box_rows, num_rows, num_blocks, group;
+  // block-sparse (nullptr: dense): uint8 [nqb, nkb] per (batch, head), 1 keeps
+  // the 128 x 128 score tile; mask_stride = bytes between (batch, head) masks
+  // (0: one mask for all)
+  const uint8_t* block_mask;
+  long long mask_stride;
+  int nkb;
 };
 
 // Wait for a barrier phase ignoring the abort flag, for at most ~50 ms; used
@@ -167,7 +177,56 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (args.causal) end = min(end, qoff + qt * kRows + kRows);
     n_t[t] = (valid_t[t] && end > 0) ? (end + kKeys - 1) / kKeys : 0;
   }
-  const int nmax = max(n_t[0], n_t[1]);
+  // Block-sparse: the CTA streams the key tiles that either query tile keeps
+  // (the union of its two mask rows, each cut to the tile's causal / key-length
+  // range).  A tile kept only for the other query tile is computed fully masked.
+  // n_t becomes the number of streamed tiles within tile t's range (a prefix of
+  // the stream, as for the dense tile counts).
+  const bool sparse = args.block_mask != nullptr;
+  uint32_t* mwords = reinterpret_cast<uint32_t*>(smem + C::kOffMask);  // [3][kMaskWords]
+  int* mcount = reinterpret_cast<int*>(smem + C::kOffMask + 3 * kMaskWords * 4);
+  if (sparse && warp == 10) {
+    const uint8_t* mrow = args.block_mask + static_cast<size_t>(bh) * args.mask_stride;
+    int c0 = 0, c1 = 0;
+    for (int w = lane; w < kMaskWords; w += 32) {
+      uint32_t r0 = 0, r1 = 0;
+      if (32 * w < n_t[1] || 32 * w < n_t[0]) {
+#pragma unroll 4
+        for (int bt = 0; bt < 32; ++bt) {
+          const int j = 32 * w + bt;
+          if (j < n_t[0] && mrow[static_cast<size_t>(2 * mblk) * args.nkb + j]) r0 |= 1u << bt;
+          if (j < n_t[1] && mrow[static_cast<size_t>(2 * mblk + 1) * args.nkb + j]) r1 |= 1u << bt;
+        }
+      }
+      const uint32_t u = r0 | r1;
+      mwords[w] = u;
+      mwords[kMaskWords + w] = r0;
+      mwords[2 * kMaskWords + w] = r1;
+      // streamed tiles inside each query tile's range
+      const int lo0 = n_t[0] - 32 * w, lo1 = n_t[1] - 32 * w;
+      const uint32_t rng0 = lo0 >= 32 ? ~0u : (lo0 <= 0 ? 0u : (1u << lo0) - 1u);
+      const uint32_t rng1 = lo1 >= 32 ? ~0u : (lo1 <= 0 ? 0u : (1u << lo1) - 1u);
+      c0 += __popc(u & rng0);
+      c1 += __popc(u & rng1);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      c0 += __shfl_xor_sync(0xffffffffu, c0, off);
+      c1 += __shfl_xor_sync(0xffffffffu, c1, off);
+    }
+    if (lane == 0) {
+      mcount[0] = c0;
+      mcount[1] = c1;
+    }
+  }
+  // first streamed key tile at or after `from` (sparse); bounded by the words
+  auto next_kt = [&](int from) -> int {
+    int w = from >> 5;
+    if (w >= kMaskWords) return 0;
+    uint32_t x = mwords[w] & (~0u << (from & 31));
+    while (x == 0 && w + 1 < kMaskWords) x = mwords[++w];
+    return x == 0 ? 0 : (w << 5) + __ffs(x) - 1;
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(bar(BAR_Q), 1);
@@ -196,6 +255,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (sparse) {
+    n_t[0] = mcount[0];
+    n_t[1] = mcount[1];
+  }
+  const int nmax = max(n_t[0], n_t[1]);
   const uint32_t tmem = *tmem_slot;
   const WaitCtx wc{abort_flag, args.status};
 
@@ -248,7 +312,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     int crow = args.num_rows;  // cache row of this lane's box in the current key tile
     bool bad_table = false;
     int issued = 0;
+    int kt = -1;  // key tile of the current stream step
     for (int u = 0; u < 2 * nmax; ++u) {
+      if ((u & 1) == 0) kt = sparse ? next_kt(kt + 1) : (u >> 1);
       const int slot = u % C::kSlots;
       const uint32_t ph = static_cast<uint32_t>(u / C::kSlots) & 1u;
       int ok = 1;
@@ -259,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive_expect_tx(bar(BAR_KV_FULL + slot), C::kTileBytes);
       if (paged) {
         if ((u & 1) == 0) {  // K and V of a key tile share its boxes
-          const int key0 = (u >> 1) * kKeys;
+          const int key0 = kt * kKeys;
           const int e0 = key0 / args.block_size;
           if ((e0 >> 5) != win) {
             cur = ((e0 >> 5) == win + 1) ? nxt : table_window(e0 >> 5);
@@ -284,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else if (lane == 0) {
         for (int s = 0; s < C::kSub; ++s)
-          load_rows(dst + s * C::kSubBytes, tm, bar(BAR_KV_FULL + slot), s * 64, (u >> 1) * kKeys);
+          load_rows(dst + s * C::kSubBytes, tm, bar(BAR_KV_FULL + slot), s * 64, kt * kKeys);
       }
       issued = u + 1;
     }
@@ -385,6 +451,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     float l_sum = 0.f;
     bool aborted = false;
     const int n = (t == 0) ? n_t[0] : n_t[1];  // selects, not a runtime-indexed (stack) array
+    const uint32_t* rowbits = mwords + (1 + t) * kMaskWords;
+    int kt = -1;  // key tile of the current stream step
     const bool valid = (t == 0) ? valid_t[0] : valid_t[1];
     for (int j = 0; j < n; ++j) {
       if (!mbar_wait(bar(BAR_S_FULL + t), static_cast<uint32_t>(j) & 1u, wc)) {
@@ -394,7 +462,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       float s[kKeys];
       tmem_ld128f(tS, s);
-      const int lim = last_key - j * kKeys;  // last visible key index within this tile
+      kt = sparse ? next_kt(kt + 1) : j;
+      const bool kept = !sparse || ((rowbits[kt >> 5] >> (kt & 31)) & 1u);
+      const int lim = kept ? last_key - kt * kKeys : -1;  // last visible key index within this tile
       if (lim < kKeys - 1) {
 #pragma unroll
         for (int i = 0; i < kKeys; ++i)
@@ -501,7 +571,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D>
 fa_status fwd_launch_d(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N,
-                       int causal, float scale, const int32_t* kv_lens, cudaStream_t stream) {
+                       int causal, float scale, const int32_t* kv_lens, const uint8_t* block_mask,
+                       long long mask_stride, cudaStream_t stream) {
   using C = FwdCfg<D>;
   const uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(N), static_cast<uint64_t>(B) * H};
   const uint64_t strides[2] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(N) * D * 2};
@@ -526,6 +597,9 @@ fa_status fwd_launch_d(const void* Q, const void* K, const void* V, void* O, flo
   a.total = 0;
   a.H = H;
   a.N = N;
+  a.block_mask = block_mask;
+  a.mask_stride = mask_stride;
+  a.nkb = ceil_div(N, kKeys);
   a.causal = causal ? 1 : 0;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.status = status;
@@ -651,9 +725,12 @@ fa_status fwd_varlen_launch(const void* Q, const void* K, const void* V, void* O
 }
 
 fa_status fwd_launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d,
-                     int causal, float scale, const int32_t* kv_lens, cudaStream_t stream) {
-  if (d == 64) return fwd_launch_d<64>(Q, K, V, O, LSE, B, H, N, causal, scale, kv_lens, stream);
-  if (d == 128) return fwd_launch_d<128>(Q, K, V, O, LSE, B, H, N, causal, scale, kv_lens, stream);
+                     int causal, float scale, const int32_t* kv_lens, const uint8_t* block_mask,
+                     long long mask_stride, cudaStream_t stream) {
+  if (d == 64)
+    return fwd_launch_d<64>(Q, K, V, O, LSE, B, H, N, causal, scale, kv_lens, block_mask, mask_stride, stream);
+  if (d == 128)
+    return fwd_launch_d<128>(Q, K, V, O, LSE, B, H, N, causal, scale, kv_lens, block_mask, mask_stride, stream);
   return FA_ERR_UNSUPPORTED;
 }
 

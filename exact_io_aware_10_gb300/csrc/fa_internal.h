@@ -37,7 +37,10 @@ inline fa_status launch_status() {
 // Launchers implemented by the kernel translation units.  Arguments are
 // validated by the public entry points before these are called.
 fa_status fwd_launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d,
-                     int causal, float scale, const int32_t* kv_lens, cudaStream_t stream);
+                     int causal, float scale, const int32_t* kv_lens, const uint8_t* block_mask,
+                     long long mask_stride, cudaStream_t stream);
+// largest N the block-sparse forward takes (its key-tile bitmask holds 2048 tiles)
+constexpr int kBlockSparseMaxN = 2048 * 128;
 fa_status fwd_varlen_launch(const void* Q, const void* K, const void* V, void* O, float* LSE,
                             const int32_t* cu_seqlens, int num_seqs, int total, int max_seqlen, int H, int d,
                             int causal, float scale, cudaStream_t stream);

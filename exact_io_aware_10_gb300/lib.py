@@ -32,6 +32,7 @@ SIGNATURES = {
     "fa_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp]),
     "fa_fwd_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp, _vp]),
     "fa_fwd_varlen": (_i, [_vp] * 6 + [_i, _i, _i, _i, _i, _i, _f, _vp]),
+    "fa_fwd_block_sparse": (_i, [_vp] * 5 + [_i] * 5 + [_f, _vp, _vp, _i, _vp]),
     "fa_paged_prefill": (_i, [_vp] * 8 + [_i] * 10 + [_f, _vp]),
     "fa_bwd_workspace_size": (_sz, [_i, _i, _i, _i]),
     "fa_bwd": (_i, [_vp] * 9 + [_i, _i, _i, _i, _i, _f, _vp, _vp, _sz, _vp]),
@@ -126,6 +127,37 @@ def fa_fwd(Q, K, V, causal=False, scale=None, kv_lens=None, O=None, LSE=None, st
     st = lib.fa_fwd_ex(_p(Q), _p(K), _p(V), _p(O), _p(LSE), B, H, N, d, int(bool(causal)), scale, _p(kv_lens),
                        _stream(stream))
     _check(st, "fa_fwd")
+    return O, LSE
+
+
+def fa_fwd_block_sparse(Q, K, V, block_mask, causal=False, scale=None, kv_lens=None, O=None, LSE=None,
+                        stream=None):
+    """Block-sparse forward: block_mask is a CUDA uint8 tensor [nb, nb] (shared)
+    or [B, H, nb, nb], nb = ceil(N / 128); non-zero keeps a 128 x 128 block."""
+    lib = load()
+    B, H, N, d = Q.shape
+    for t, n in ((Q, "Q"), (K, "K"), (V, "V")):
+        _need(t, torch.bfloat16, (B, H, N, d), n)
+    nb = (N + 127) // 128
+    _need(block_mask, torch.uint8, None, "block_mask")
+    if tuple(block_mask.shape) == (nb, nb):
+        per_head = 0
+    elif tuple(block_mask.shape) == (B, H, nb, nb):
+        per_head = 1
+    else:
+        raise ValueError(f"block_mask must be [{nb}, {nb}] or [{B}, {H}, {nb}, {nb}]")
+    if O is None:
+        O = torch.empty_like(Q)
+    if LSE is None:
+        LSE = torch.empty((B, H, N), dtype=torch.float32, device=Q.device)
+    _need(O, torch.bfloat16, (B, H, N, d), "O")
+    _need(LSE, torch.float32, (B, H, N), "LSE")
+    if kv_lens is not None:
+        _need(kv_lens, torch.int32, (B,), "kv_lens")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    st = lib.fa_fwd_block_sparse(_p(Q), _p(K), _p(V), _p(O), _p(LSE), B, H, N, d, int(bool(causal)), scale,
+                                 _p(kv_lens), _p(block_mask), per_head, _stream(stream))
+    _check(st, "fa_fwd_block_sparse")
     return O, LSE
 
 

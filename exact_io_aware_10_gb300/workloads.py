@@ -21,6 +21,12 @@ Long Range Arena -- are stood in for by these synthetic tensors):
 * ``paged_prefill``  query chunks of lengths q_len_b packed [total_q, Hq, d]
                  (cu_seqlens_q) over a ``paged`` cache whose sequences hold
                  kv_len_b >= q_len_b tokens (cached prefix + the chunk).
+* ``block_mask`` 0/1 masks over 128 x 128 score blocks: ``butterfly`` keeps
+                 block (i, j) when i == j or i XOR j is a power of two (the
+                 fixed butterfly pattern family block-sparse FlashAttention
+                 was measured with) plus the w nearest key blocks before i;
+                 ``random`` keeps each block with probability p (diagonal
+                 always kept).
 * ``paged``      decode queries [B, Hq, d], a paged KV cache
                  [num_blocks, block_size, Hkv, d], context lengths
                  L_b ~ U{lo..hi}, and a block table whose physical ids are a
@@ -40,6 +46,7 @@ __all__ = [
     "padded_lengths",
     "boosted_inputs",
     "paged_inputs",
+    "block_mask",
     "VarlenInputs",
     "PagedPrefillInputs",
     "paged_prefill_inputs",
@@ -243,6 +250,23 @@ def paged_prefill_inputs(q_lens, kv_lens, Hq, Hkv, d, block_size=16, seed=0, std
     k_cache = _normal_bf16((max(NB, 1), block_size, Hkv, d), g, std)
     v_cache = _normal_bf16((max(NB, 1), block_size, Hkv, d), g, std)
     return PagedPrefillInputs(q, k_cache, v_cache, table, cu.to(torch.int32), seq_lens, block_size)
+
+
+def block_mask(nb, pattern="butterfly", window=2, p=0.25, seed=0, heads=None) -> torch.Tensor:
+    """uint8 block mask [nb, nb] (or [*heads, nb, nb] for per-head random masks)."""
+    if pattern == "butterfly":
+        i = torch.arange(nb)[:, None]
+        j = torch.arange(nb)[None, :]
+        x = i ^ j
+        keep = (x == 0) | ((x & (x - 1)) == 0) | ((i - j >= 0) & (i - j <= window))
+        return keep.to(torch.uint8)
+    if pattern == "random":
+        g = _gen(seed + 307)
+        shape = (nb, nb) if heads is None else (*heads, nb, nb)
+        keep = torch.rand(shape, generator=g) < p
+        keep[..., torch.arange(nb), torch.arange(nb)] = True
+        return keep.to(torch.uint8)
+    raise ValueError(f"unknown pattern {pattern!r}")
 
 
 def device_normal_bf16(shape, seed, device, std=1.0):

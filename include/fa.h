@@ -76,6 +76,24 @@ int fa_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* LSE, 
               int causal, float scale, const int32_t* kv_lens, void* stream);
 
 /*
+ * Block-sparse forward attention ("精读笔记 08：FlashAttention" §4.4): the
+ * scores are cut into 128 x 128 blocks (query block qb = i / 128, key block
+ * kb = j / 128) and a 0/1 block mask keeps or drops each block; dropped
+ * blocks are masked like causal ones, and key tiles no query tile of a CTA
+ * keeps are never loaded or multiplied.  The result is exact attention under
+ * that mask (the approximation is the mask itself).
+ *   Q, K, V, O, LSE, causal, scale, kv_lens : as fa_fwd_ex (masks combine by AND).
+ *   block_mask : device uint8, nb = ceil(N / 128); [nb, nb] shared by every
+ *                (batch, head) when mask_per_head = 0, else [B, H, nb, nb].
+ *                Non-zero keeps the block.
+ * A row whose blocks are all dropped gets O = 0, LSE = -inf.
+ * N <= 262144 (else FA_ERR_UNSUPPORTED); B <= 65535.  Errors as fa_fwd.
+ */
+int fa_fwd_block_sparse(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d,
+                        int causal, float scale, const int32_t* kv_lens, const uint8_t* block_mask,
+                        int mask_per_head, void* stream);
+
+/*
  * Forward attention over a packed ragged batch: num_seqs sequences of
  * different lengths laid end to end, each attending only to itself (with
  * per-sequence causal masking).  This is the irregular-batch case of the

@@ -40,3 +40,19 @@ def test_decode_bytes_count_each_key_once_per_kv_head():
     b = acc.decode_bytes(sl, 8, 2, 64, 16, with_lse=False)
     kv = sum(sl) * 2 * 64 * 2 * 2
     assert b >= kv and b - kv < 64 * 1024
+
+
+@pytest.mark.parametrize("N", [128, 300, 512])
+@pytest.mark.parametrize("causal", [False, True])
+def test_block_sparse_counts_visible_pairs(N, causal):
+    nb = (N + 127) // 128
+    m = np.random.default_rng(N).random((nb, nb)) < 0.5
+    vis = oracle.expand_block_mask(m, N, N, 128)
+    if causal:
+        vis &= np.tril(np.ones((N, N), bool))
+    assert acc.block_sparse_flops(m, 2, 3, N, 8, causal) == 4 * 8 * 2 * 3 * _pairs(vis)
+    per = np.stack([np.stack([m, ~m]), np.stack([m, m])])  # [B=2, H=2] per-head masks
+    want = sum(_pairs(oracle.expand_block_mask(per[b, h], N, N, 128) & (np.tril(np.ones((N, N), bool))
+                                                                      if causal else True))
+               for b in range(2) for h in range(2))
+    assert acc.block_sparse_flops(per, 2, 2, N, 8, causal) == 4 * 8 * want

@@ -43,7 +43,7 @@ def test_status_strings(so):
                        (4, "FA_ERR_TIMEOUT"), (5, "FA_ERR_BAD_BLOCK_TABLE")]:
         assert so.fa_status_string(code).decode() == name
     assert so.fa_status_string(99).decode() == "FA_ERR_UNKNOWN"
-    assert so.fa_version() == 102
+    assert so.fa_version() == 103
 
 
 def _fake(n=1):
@@ -65,6 +65,20 @@ def test_forward_argument_validation(so):
     assert so.fa_fwd(Q, K, V, O, L, 65536, 1, 16, 64, 0, 0.1, s) == fl.FA_ERR_UNSUPPORTED
     # N = 0 is a valid no-op and launches nothing
     assert so.fa_fwd(Q, K, V, O, L, 1, 1, 0, 64, 0, 0.1, s) == fl.FA_OK
+
+
+def test_block_sparse_argument_validation(so):
+    Q, K, V, O, L, M = _fake(6)
+    s = ctypes.c_void_p(0)
+    f = so.fa_fwd_block_sparse
+    # (Q, K, V, O, LSE, B, H, N, d, causal, scale, kv_lens, block_mask, per_head, stream)
+    assert f(Q, K, V, O, L, 1, 2, 1024, 96, 0, 0.1, None, M, 0, s) == fl.FA_ERR_UNSUPPORTED
+    assert f(Q, K, V, O, L, 1, 2, 1024, 128, 0, 0.1, None, None, 0, s) == fl.FA_ERR_INVALID_ARG
+    assert f(Q, K, V, O, L, 0, 2, 1024, 128, 0, 0.1, None, M, 0, s) == fl.FA_ERR_INVALID_ARG
+    assert f(Q, K, V, O, L, 1, 2, 1024, 128, 0, 0.0, None, M, 0, s) == fl.FA_ERR_INVALID_ARG
+    assert f(Q, K, V, O, L, 1, 2, 262144 + 1, 128, 0, 0.1, None, M, 0, s) == fl.FA_ERR_UNSUPPORTED
+    assert f(Q, K, V, O, L, 65536, 1, 1024, 128, 0, 0.1, None, M, 0, s) == fl.FA_ERR_UNSUPPORTED
+    assert f(Q, K, V, O, L, 1, 2, 0, 128, 0, 0.1, None, M, 0, s) == fl.FA_OK  # N = 0: no-op
 
 
 def test_varlen_forward_argument_validation(so):
