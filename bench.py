@@ -61,6 +61,10 @@ PAGED_PREFILL = dict(num_seqs=16, q_len=2048, prefix_lo=0, prefix_hi=30720, Hq=3
 # block-sparse forward, timed after the step on the long-context shapes: a
 # butterfly mask plus a local window of BLOCK_SPARSE_WINDOW key blocks
 BLOCK_SPARSE_WINDOW = 15
+# decode launch overhead, timed after the step: one decode step of
+# DECODE_STEP["layers"] paged decodes (B sequences of `context` tokens, Hq/Hkv
+# heads, 16-token blocks), issued eagerly call by call or replayed as one graph
+DECODE_STEP = dict(layers=32, B=1, Hq=32, Hkv=8, d=128, context=2048, config_id=8)
 WORKLOAD = ("long-context causal prefill B1 H16 d128 (fwd+bwd N=16384, fwd N=65536) + paged GQA decode "
             "B64 Hq32 Hkv8 d128 L~U[512,32768] block16 splits16")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -361,6 +365,48 @@ def time_block_sparse(w, steps, warmup, barrier, max_over_ranks, world, peak_tf,
     return out
 
 
+def time_decode_step(dev, seed, steps, warmup, barrier, max_over_ranks):
+    """Per-step time of a small-batch decode step (one paged decode per layer):
+    eager calls with 16 splits (split + combine) or 1 split (one fused launch),
+    and the same step replayed as a CUDA graph.  Event time spans the whole
+    step, so host launch gaps count."""
+    from exact_io_aware_10_gb300 import lib
+
+    c = DECODE_STEP
+    sd = wl.config_seed(seed, c["config_id"])
+    sl, table, NB, _ = wl.paged_layout(c["B"], 0, 0, 16, sd, None, [c["context"]] * c["B"])
+    sl, table = sl.to(dev), table.to(dev)
+    layers = []
+    for i in range(c["layers"]):
+        q = wl.device_normal_bf16((c["B"], c["Hq"], c["d"]), sd + 10 * i + 1, dev)
+        kc = wl.device_normal_bf16((NB, 16, c["Hkv"], c["d"]), sd + 10 * i + 2, dev)
+        vc = wl.device_normal_bf16((NB, 16, c["Hkv"], c["d"]), sd + 10 * i + 3, dev)
+        layers.append((q, kc, vc, torch.empty_like(q), torch.empty(c["B"], c["Hq"], dtype=torch.float32,
+                                                                   device=dev)))
+    ws = torch.empty(lib.fa_paged_decode_workspace_size(c["B"], c["Hq"], c["d"], 16), dtype=torch.uint8, device=dev)
+
+    def eager(splits):
+        def run(_):
+            for q, kc, vc, o, lse in layers:
+                lib.fa_paged_decode(q, kc, vc, table, sl, num_splits=splits, o=o, lse=lse, workspace=ws)
+        return run
+
+    graphs = {s_: lib.DecodeGraph(layers, table, sl, num_splits=s_, workspace=ws) for s_ in (16, 1)}
+    out = {"layers": c["layers"], "B": c["B"], "Hq": c["Hq"], "Hkv": c["Hkv"], "context": c["context"]}
+    for name, fn, launches in (("eager_splits16", eager(16), 2 * c["layers"]),
+                               ("eager_splits1", eager(1), c["layers"]),
+                               ("graph_splits16", lambda _: graphs[16].launch(), graphs[16].kernel_count),
+                               ("graph_splits1", lambda _: graphs[1].launch(), graphs[1].kernel_count)):
+        _, ms = time_parts(fn, ("step",), steps, warmup, barrier)
+        out[name] = {"ms_per_step": max_over_ranks(ms["step"]) / steps, "kernel_launches_per_step": launches}
+    assert lib.fa_get_device_status() == lib.FA_OK, "device status word reported an error"
+    for g in graphs.values():
+        g.close()
+    out["speedup_graph_vs_eager_splits16"] = out["eager_splits16"]["ms_per_step"] / out["graph_splits16"][
+        "ms_per_step"]
+    return out
+
+
 class HostBuffers:
     """Pinned host copies of a step's inputs and outputs for the end-to-end run."""
 
@@ -520,6 +566,7 @@ def run_ours(args):
                                                         max_over_ranks, world, peak_tf)
         next_rows["block_sparse"] = time_block_sparse(w, args.steps, args.warmup, barrier, max_over_ranks, world,
                                                       peak_tf, part_ms)
+        next_rows["decode_step"] = time_decode_step(dev, args.seed, args.steps, args.warmup, barrier, max_over_ranks)
         next_rows["note"] = "timed after the step, outside value and ms_per_step; TFLOP/s count useful FLOPs only"
 
     cpu = None
@@ -626,7 +673,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--skip-next-rows", action="store_true",
-                    help="skip the ragged-batch, paged-prefill and block-sparse timings")
+                    help="skip the ragged-batch, paged-prefill, block-sparse and decode-step timings")
     ap.add_argument("--ref-prefix", type=int, default=2048)
     args = ap.parse_args()
     if args.warmup < 3:

@@ -59,21 +59,23 @@ bool encode_f32_tmap(CUtensorMap* map, const void* base, int rank, const uint64_
                      strides_bytes, box);
 }
 
+bool encode_init() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_encode == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+      return false;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  return true;
+}
+
 namespace {
 bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, CUtensorMapSwizzle swizzle, const void* base, int rank,
                  const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box) {
-  {
-    std::lock_guard<std::mutex> lk(g_mu);
-    if (g_encode == nullptr) {
-      void* fn = nullptr;
-      cudaDriverEntryPointQueryResult q;
-      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
-              cudaSuccess ||
-          q != cudaDriverEntryPointSuccess || fn == nullptr)
-        return false;
-      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    }
-  }
+  if (!encode_init()) return false;
   cuuint64_t gdim[5];
   cuuint64_t gstr[4];
   cuuint32_t bdim[5];
@@ -145,7 +147,7 @@ const char* fa_status_string(int status) {
   }
 }
 
-int fa_version(void) { return 103; }
+int fa_version(void) { return 104; }
 
 int fa_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d, int causal,
               float scale, const int32_t* kv_lens, void* stream) {
@@ -238,6 +240,7 @@ int fa_bwd(const void* Q, const void* K, const void* V, const void* O, const voi
 
 size_t fa_paged_decode_workspace_size(int B, int Hq, int d, int num_splits) {
   if (B < 1 || Hq < 1 || d < 1 || num_splits < 0 || num_splits > 16) return 0;
+  if (num_splits == 1) return 0;  // one split writes the output directly
   const int S = num_splits == 0 ? 16 : num_splits;
   const size_t n = static_cast<size_t>(B) * Hq * S;
   return round256(n * d * sizeof(float)) + round256(n * 2 * sizeof(float));
@@ -252,7 +255,8 @@ int fa_paged_decode(const void* q, const void* k_cache, const void* v_cache, con
   if (bad_scale(scale)) return FA_ERR_INVALID_ARG;
   if (d != 128 || block_size != 16) return FA_ERR_UNSUPPORTED;
   if (Hq / Hkv > 16 || num_splits > 16) return FA_ERR_UNSUPPORTED;
-  if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !o || !workspace) return FA_ERR_INVALID_ARG;
+  if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !o) return FA_ERR_INVALID_ARG;
+  if (num_splits != 1 && !workspace) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o)) return FA_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_INVALID_ARG;
   if (static_cast<long long>(num_blocks) * block_size > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;

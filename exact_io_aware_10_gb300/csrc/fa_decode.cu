@@ -12,6 +12,10 @@
 // At the end the four warp states merge in shared memory into one partial
 // (m, l, o) per (b, head, split), written to the workspace.
 //
+// With a single split the first kernel finishes the job itself: it normalises
+// o by l and writes o and lse, so one launch and no workspace serve short
+// contexts (the launch-overhead remark closing the S12 chapter).
+//
 // Kernel 2 (combine): one warp per (b, query head) merges the splits:
 // m = max m_s, l = sum 2^(m_s - m) l_s, o = sum 2^(m_s - m) o_s / l, skipping
 // empty splits ("精读笔记 08：FlashAttention" §3.1 merge rule).
@@ -40,10 +44,15 @@ constexpr int kOffBar = kStages * kStageBytes;   // 64 KiB of stages
 constexpr int kMergeBytes = kConsumers * (16 * kD + 32) * 4;  // per-warp O rows + m, l
 constexpr int kSmemBytes = kOffBar + 256 + 1024;
 static_assert(kMergeBytes <= kOffBar, "merge scratch reuses the stage ring");
-constexpr int kMinBlocksPerSplit = 32;  // at most one split per 512 keys
+// A split covers at least kMinBlocksPerSplit blocks (512 keys) when the batch
+// alone fills the GPU (B * Hkv >= kFewUnits), else kMinBlocksPerSplitFew (128
+// keys), so a small batch still spreads its keys over enough CTAs.
+constexpr int kMinBlocksPerSplit = 32;
+constexpr int kMinBlocksPerSplitFew = 8;
+constexpr int kFewUnits = 152;
 
-__host__ __device__ inline int splits_for(int nblocks, int max_splits) {
-  int s = (nblocks + kMinBlocksPerSplit - 1) / kMinBlocksPerSplit;
+__host__ __device__ inline int splits_for(int nblocks, int max_splits, int min_blocks) {
+  int s = (nblocks + min_blocks - 1) / min_blocks;
   return max(1, min(max_splits, s));
 }
 
@@ -56,6 +65,8 @@ struct DecArgs {
   __nv_bfloat16* o;
   float* lse;
   int B, Hq, Hkv, G, max_blocks, num_blocks, S;
+  int direct;  // S == 1: the split kernel writes o and lse itself
+  int min_blocks;  // smallest split, in blocks
   float scale_log2;
   unsigned* status;
 };
@@ -97,7 +108,7 @@ __global__ void __launch_bounds__(kThreads, 3)
   const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int L = min(max(a.seq_lens[b], 0), a.max_blocks * kBlk);
   const int nb = (L + kBlk - 1) / kBlk;
-  const int S_b = splits_for(nb, a.S);
+  const int S_b = splits_for(nb, a.S, a.min_blocks);
   if (s >= S_b) return;  // this sequence uses fewer splits
   const int lo = static_cast<int>((static_cast<long long>(s) * nb) / S_b);
   const int hi = static_cast<int>((static_cast<long long>(s + 1) * nb) / S_b);
@@ -289,6 +300,14 @@ __global__ void __launch_bounds__(kThreads, 3)
           l += f * sML[(w * 16 + r) * 2 + 1];
         }
       }
+      if (a.direct) {
+        const size_t row = static_cast<size_t>(b) * a.Hq + g * a.G + r;
+        const float inv = (l > 0.f) ? 1.f / l : 0.f;
+        a.o[row * kD + dcol] = __float2bfloat16_rn(o * inv);
+        if (a.lse != nullptr && dcol == 0)
+          a.lse[row] = (l > 0.f) ? (m + lg2_approx(l)) * 0.69314718055994531f : -INFINITY;
+        continue;
+      }
       const size_t idx = (static_cast<size_t>(b) * a.Hq + g * a.G + r) * a.S + s;
       a.part_o[idx * kD + dcol] = o;
       if (dcol == 0) {
@@ -306,7 +325,7 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecArgs a) {
   if (gw >= a.B * a.Hq) return;
   const int b = gw / a.Hq;
   const int L = min(max(a.seq_lens[b], 0), a.max_blocks * kBlk);
-  const int S_b = splits_for((L + kBlk - 1) / kBlk, a.S);
+  const int S_b = splits_for((L + kBlk - 1) / kBlk, a.S, a.min_blocks);
   const float* po = a.part_o + static_cast<size_t>(gw) * a.S * kD;
   const float* pml = a.part_ml + static_cast<size_t>(gw) * a.S * 2;
   float m = -INFINITY;
@@ -338,6 +357,17 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecArgs a) {
 
 }  // namespace
 
+fa_status decode_prepare() {
+  static bool attr_set = false;  // setting it twice is harmless
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(decode_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+        cudaSuccess)
+      return FA_ERR_CUDA;
+    attr_set = true;
+  }
+  return FA_OK;
+}
+
 fa_status decode_launch(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
                         const int32_t* seq_lens, void* o, float* lse, int B, int Hq, int Hkv, int d, int block_size,
                         int max_blocks, int num_blocks, int num_splits, float scale, void* workspace,
@@ -350,13 +380,7 @@ fa_status decode_launch(const void* q, const void* k_cache, const void* v_cache,
   CUtensorMap tk, tv;
   if (!encode_bf16_tmap(&tk, k_cache, 3, dims, strides, box) || !encode_bf16_tmap(&tv, v_cache, 3, dims, strides, box))
     return FA_ERR_CUDA;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(decode_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
-        cudaSuccess)
-      return FA_ERR_CUDA;
-    attr_set = true;
-  }
+  if (decode_prepare() != FA_OK) return FA_ERR_CUDA;
   unsigned* status = device_status_ptr();
   if (status == nullptr) return FA_ERR_CUDA;
   DecArgs a;
@@ -375,10 +399,13 @@ fa_status decode_launch(const void* q, const void* k_cache, const void* v_cache,
   a.max_blocks = max_blocks;
   a.num_blocks = num_blocks;
   a.S = num_splits;
+  a.direct = num_splits == 1 ? 1 : 0;
+  a.min_blocks = (static_cast<long long>(B) * Hkv >= kFewUnits) ? kMinBlocksPerSplit : kMinBlocksPerSplitFew;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.status = status;
   dim3 grid(num_splits, Hkv, B);
   decode_split_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tk, tv, a);
+  if (a.direct) return launch_status();
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   decode_combine_kernel<<<ceil_div(static_cast<long long>(B) * Hq, 8), 256, 0, stream>>>(a);
   return launch_status();

@@ -51,6 +51,11 @@ fa_status fwd_paged_launch(const void* q, const void* k_cache, const void* v_cac
 fa_status bwd_launch(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
                      void* dQ, void* dK, void* dV, int B, int H, int N, int d, int causal, float scale,
                      const int32_t* kv_lens, void* workspace, cudaStream_t stream);
+// One-time host setup of the decode kernels (shared-memory attribute), done
+// outside any stream capture by the graph builder.
+fa_status decode_prepare();
+// Loads the tensor-map encoder entry point if needed; false if unavailable.
+bool encode_init();
 fa_status decode_launch(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
                         const int32_t* seq_lens, void* o, float* lse, int B, int Hq, int Hkv, int d, int block_size,
                         int max_blocks, int num_blocks, int num_splits, float scale, void* workspace,

@@ -33,6 +33,10 @@ SIGNATURES = {
     "fa_fwd_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp, _vp]),
     "fa_fwd_varlen": (_i, [_vp] * 6 + [_i, _i, _i, _i, _i, _i, _f, _vp]),
     "fa_fwd_block_sparse": (_i, [_vp] * 5 + [_i] * 5 + [_f, _vp, _vp, _i, _vp]),
+    "fa_decode_graph_create": (_i, [_vp, _i] + [_vp] * 7 + [_i] * 8 + [_f, _vp, _sz]),
+    "fa_decode_graph_launch": (_i, [_vp, _vp]),
+    "fa_decode_graph_kernel_count": (_i, [_vp]),
+    "fa_decode_graph_destroy": (None, [_vp]),
     "fa_paged_prefill": (_i, [_vp] * 8 + [_i] * 10 + [_f, _vp]),
     "fa_bwd_workspace_size": (_sz, [_i, _i, _i, _i]),
     "fa_bwd": (_i, [_vp] * 9 + [_i, _i, _i, _i, _i, _f, _vp, _vp, _sz, _vp]),
@@ -289,6 +293,68 @@ def fa_paged_prefill(q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens_k,
                               int(bool(causal)), scale, _stream(stream))
     _check(st, "fa_paged_prefill")
     return o, lse
+
+
+class DecodeGraph:
+    """A decode step (one paged decode per layer) recorded as a CUDA graph.
+
+    ``layers`` is a list of (q, k_cache, v_cache, o, lse) tensors, one per
+    call; lse may be None.  block_table, seq_lens, num_splits, scale and the
+    workspace are shared by every call.  The graph keeps the tensors' device
+    addresses: update their contents between launches, and keep them alive.
+    """
+
+    def __init__(self, layers, block_table, seq_lens, scale=None, num_splits=0, workspace=None):
+        lib = load()
+        q0, k0 = layers[0][0], layers[0][1]
+        B, Hq, d = q0.shape
+        NB, bs, Hkv, _ = k0.shape
+        for q, kc, vc, o, lse in layers:
+            _need(q, torch.bfloat16, (B, Hq, d), "q")
+            _need(kc, torch.bfloat16, (NB, bs, Hkv, d), "k_cache")
+            _need(vc, torch.bfloat16, (NB, bs, Hkv, d), "v_cache")
+            _need(o, torch.bfloat16, (B, Hq, d), "o")
+            if lse is not None:
+                _need(lse, torch.float32, (B, Hq), "lse")
+        _need(block_table, torch.int32, None, "block_table")
+        _need(seq_lens, torch.int32, (B,), "seq_lens")
+        if block_table.dim() != 2 or block_table.shape[0] != B:
+            raise ValueError("block_table must be [B, max_blocks]")
+        ws_bytes = fa_paged_decode_workspace_size(B, Hq, d, num_splits)
+        if workspace is None:
+            workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=q0.device)
+        n = len(layers)
+        arr = ctypes.c_void_p * n
+        ptrs = [arr(*[t.data_ptr() for t in col]) for col in zip(*[(l[0], l[1], l[2], l[3]) for l in layers])]
+        have_lse = all(l[4] is not None for l in layers)
+        lse_arr = arr(*[l[4].data_ptr() for l in layers]) if have_lse else None
+        scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+        h = ctypes.c_void_p()
+        st = lib.fa_decode_graph_create(ctypes.byref(h), n, ptrs[0], ptrs[1], ptrs[2], ptrs[3], lse_arr,
+                                        _p(block_table), _p(seq_lens), B, Hq, Hkv, d, bs, int(block_table.shape[1]),
+                                        NB, int(num_splits), scale, _p(workspace),
+                                        workspace.numel() * workspace.element_size())
+        _check(st, "fa_decode_graph_create")
+        self._lib, self._h = lib, h
+        self._keep = (layers, block_table, seq_lens, workspace)  # the graph holds their addresses
+
+    @property
+    def kernel_count(self) -> int:
+        return int(self._lib.fa_decode_graph_kernel_count(self._h))
+
+    def launch(self, stream=None):
+        _check(self._lib.fa_decode_graph_launch(self._h, _stream(stream)), "fa_decode_graph_launch")
+
+    def close(self):
+        if self._h:
+            self._lib.fa_decode_graph_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def fa_paged_decode_noalloc(q, k_cache, v_cache, block_table, seq_lens, scale=None, num_splits=0, o=None, lse=None,

@@ -189,7 +189,8 @@ int fa_bwd(const void* Q, const void* K, const void* V, const void* O, const voi
  * Bytes of device workspace fa_paged_decode needs for `num_splits` partial
  * (m, l, o) states per (batch, query head): fp32 o [B, Hq, num_splits, d] and
  * fp32 (m, l) [B, Hq, num_splits, 2], each rounded up to 256 bytes.
- * num_splits = 0 means the automatic choice (16).
+ * num_splits = 0 means the automatic choice (16).  num_splits = 1 needs none
+ * (returns 0): a single split writes o and lse itself, in one launch.
  */
 size_t fa_paged_decode_workspace_size(int B, int Hq, int d, int num_splits);
 
@@ -211,13 +212,46 @@ size_t fa_paged_decode_workspace_size(int B, int Hq, int d, int num_splits);
  *   Query head h reads KV head h / (Hq / Hkv); Hq % Hkv must be 0.
  *   block_size  : 16.  num_splits: 1..16, or 0 for automatic (16).
  *   workspace   : at least fa_paged_decode_workspace_size(B, Hq, d,
- *                 num_splits) bytes, 256-byte aligned.
+ *                 num_splits) bytes, 256-byte aligned; may be NULL when
+ *                 num_splits = 1 (one fused launch, the short-context and
+ *                 small-batch choice).
  * Errors: FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA.
  */
 int fa_paged_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
                     const int32_t* seq_lens, void* o, float* lse, int B, int Hq, int Hkv, int d, int block_size,
                     int max_blocks, int num_blocks, int num_splits, float scale, void* workspace, size_t ws_bytes,
                     void* stream);
+
+/*
+ * A decode step replayed as one CUDA graph (the launch-overhead remark that
+ * closes the S12 chapter: at small batch the GPU waits on the host between
+ * kernel launches).  fa_decode_graph_create records num_calls paged decodes
+ * -- typically one per layer -- into a graph; each call i has its own q[i],
+ * k_cache[i], v_cache[i], o[i] and lse[i] (HOST arrays of device pointers;
+ * lse itself may be NULL for no LSE output), and all share block_table,
+ * seq_lens, the sizes, num_splits, scale and the workspace exactly as in
+ * fa_paged_decode (whose validation applies to every call).  Nothing runs at
+ * creation.  fa_decode_graph_launch replays the step on `stream`; the graph
+ * keeps the device pointers it was built with, so between launches the caller
+ * updates the buffers' contents (new queries, new cache rows, longer seq_lens
+ * and table rows), never their addresses.  The caller owns every buffer and
+ * must keep them alive while the graph exists; launches on one stream run in
+ * order and share the workspace, launches on different streams must not
+ * overlap.  Create and destroy are host calls that must not run inside
+ * another stream capture.
+ * Errors: FA_ERR_INVALID_ARG (including a NULL graph handle), any error of
+ * fa_paged_decode for a call, FA_ERR_CUDA.
+ */
+typedef struct fa_decode_graph fa_decode_graph;
+int fa_decode_graph_create(fa_decode_graph** graph, int num_calls, const void* const* q, const void* const* k_cache,
+                           const void* const* v_cache, void* const* o, float* const* lse,
+                           const int32_t* block_table, const int32_t* seq_lens, int B, int Hq, int Hkv, int d,
+                           int block_size, int max_blocks, int num_blocks, int num_splits, float scale,
+                           void* workspace, size_t ws_bytes);
+int fa_decode_graph_launch(fa_decode_graph* graph, void* stream);
+/* Number of kernel launches one fa_decode_graph_launch replays (0 for NULL). */
+int fa_decode_graph_kernel_count(const fa_decode_graph* graph);
+void fa_decode_graph_destroy(fa_decode_graph* graph);
 
 /*
  * fa_paged_decode without a caller workspace.  (The pages have no counterpart

@@ -27,7 +27,8 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for n in ("fa_fwd", "fa_fwd_ex", "fa_bwd", "fa_bwd_workspace_size", "fa_paged_decode",
+    for n in ("fa_fwd", "fa_fwd_ex", "fa_fwd_varlen", "fa_fwd_block_sparse", "fa_paged_prefill", "fa_bwd",
+              "fa_bwd_workspace_size", "fa_paged_decode", "fa_decode_graph_create", "fa_decode_graph_launch",
               "fa_paged_decode_workspace_size", "fa_get_device_status", "fa_status_string", "fa_version"):
         assert n in names
 
@@ -43,7 +44,7 @@ def test_status_strings(so):
                        (4, "FA_ERR_TIMEOUT"), (5, "FA_ERR_BAD_BLOCK_TABLE")]:
         assert so.fa_status_string(code).decode() == name
     assert so.fa_status_string(99).decode() == "FA_ERR_UNKNOWN"
-    assert so.fa_version() == 103
+    assert so.fa_version() == 104
 
 
 def _fake(n=1):
@@ -132,6 +133,19 @@ def test_paged_prefill_argument_validation(so):
     assert call(bt=None) == fl.FA_ERR_INVALID_ARG
     assert call(q=ctypes.c_void_p(0x10000002)) == fl.FA_ERR_INVALID_ARG
     assert call(total_q=0) == fl.FA_OK                  # no-op
+
+
+def test_decode_graph_argument_validation(so):
+    ptrs = (ctypes.c_void_p * 2)(0x10000000, 0x10001000)
+    h = ctypes.c_void_p()
+    args = [ptrs, ptrs, ptrs, ptrs, None, ctypes.c_void_p(0x10002000), ctypes.c_void_p(0x10003000),
+            1, 8, 2, 128, 16, 4, 10, 0, 0.1, ctypes.c_void_p(0x10004000), 1 << 20]
+    assert so.fa_decode_graph_create(None, 2, *args) == fl.FA_ERR_INVALID_ARG  # no handle
+    assert so.fa_decode_graph_create(ctypes.byref(h), 0, *args) == fl.FA_ERR_INVALID_ARG  # no calls
+    assert not h.value
+    assert so.fa_decode_graph_launch(None, None) == fl.FA_ERR_INVALID_ARG
+    assert so.fa_decode_graph_kernel_count(None) == 0
+    so.fa_decode_graph_destroy(None)  # a no-op
 
 
 def test_backward_argument_validation(so):
