@@ -50,6 +50,12 @@ struct FwdCfg {
   static constexpr int kSubBytes = kRows * 128;      // one sub-tile: 128 rows x 128 B
   static constexpr int kTileBytes = kRows * D * 2;   // Q/K/V tile
   static constexpr int kSlots = (D == 128) ? 5 : 8;  // K/V ring slots
+  // The ring is filled and released in groups: group 0 = K_0, group p = V_{p-1}
+  // and K_p, the pair the MMA issuer consumes together (one barrier wait and
+  // one release per key tile).  Group p reuses slots of group p - kAhead, so
+  // kAhead groups are in flight; kGroupBars barrier pairs rotate.
+  static constexpr int kAhead = kSlots / 2;
+  static constexpr int kGroupBars = kAhead + 1;
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = kOffQ + 2 * kTileBytes;
   static constexpr int kOffBar = kOffKV + kSlots * kTileBytes;
@@ -64,8 +70,8 @@ struct FwdCfg {
 // barrier indices (8 bytes each) inside the barrier block
 enum : int {
   BAR_Q = 0,
-  BAR_KV_FULL = 1,    // + slot (max 8)
-  BAR_KV_EMPTY = 9,   // + slot
+  BAR_KV_FULL = 1,    // + group barrier (max 8)
+  BAR_KV_EMPTY = 9,   // + group barrier
   BAR_S_FULL = 17,    // + tile
   BAR_P_FULL = 19,    // + tile
   BAR_O_FINAL = 21,   // + tile
@@ -230,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar(BAR_Q), 1);
-    for (int s = 0; s < C::kSlots; ++s) {
+    for (int s = 0; s < C::kGroupBars; ++s) {
       mbar_init(bar(BAR_KV_FULL + s), 1);
       mbar_init(bar(BAR_KV_EMPTY + s), 1);
     }
@@ -309,22 +315,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       cur = table_window(0);
       nxt = table_window(1);
     }
-    int crow = args.num_rows;  // cache row of this lane's box in the current key tile
+    int crow = args.num_rows;  // cache row of this lane's box in the newest key tile
+    int crow_v = args.num_rows;  // ... and in the key tile whose V is loaded next
     bool bad_table = false;
-    int issued = 0;
-    int kt = -1;  // key tile of the current stream step
-    for (int u = 0; u < 2 * nmax; ++u) {
-      if ((u & 1) == 0) kt = sparse ? next_kt(kt + 1) : (u >> 1);
-      const int slot = u % C::kSlots;
-      const uint32_t ph = static_cast<uint32_t>(u / C::kSlots) & 1u;
+    int groups = 0;  // groups issued
+    int kt = -1, kt_v = -1;  // key tiles of the newest K and of the next V
+    for (int p = 0; p <= nmax; ++p) {
+      const bool has_v = p > 0, has_k = p < nmax;
+      const int gb = p % C::kGroupBars;
       int ok = 1;
-      if (lane == 0) ok = mbar_wait(bar(BAR_KV_EMPTY + slot), ph ^ 1u, wc) ? 1 : 0;
+      if (lane == 0 && p >= C::kAhead) {
+        const int pe = p - C::kAhead;  // the group whose slots this one reuses
+        ok = mbar_wait(bar(BAR_KV_EMPTY + pe % C::kGroupBars), static_cast<uint32_t>(pe / C::kGroupBars) & 1u, wc)
+                 ? 1 : 0;
+      }
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      const uint32_t dst = sbase + C::kOffKV + slot * C::kTileBytes;
-      const CUtensorMap* tm = (u & 1) ? &tmV : &tmK;
-      if (lane == 0) mbar_arrive_expect_tx(bar(BAR_KV_FULL + slot), C::kTileBytes);
-      if (paged) {
-        if ((u & 1) == 0) {  // K and V of a key tile share its boxes
+      kt_v = kt;
+      crow_v = crow;
+      if (has_k) {
+        kt = sparse ? next_kt(kt + 1) : p;
+        if (paged) {  // K and V of a key tile share its boxes
           const int key0 = kt * kKeys;
           const int e0 = key0 / args.block_size;
           if ((e0 >> 5) != win) {
@@ -342,25 +352,35 @@ __global__ void __launch_bounds__(kThreads, 1)
               bad_table = true;
           }
         }
-        __syncwarp();  // the transaction count is armed before any box lands
-        if (lane < boxes) {
-          for (int s = 0; s < C::kSub; ++s)
-            tma_load_3d(dst + s * C::kSubBytes + lane * args.box_rows * 128, tm, bar(BAR_KV_FULL + slot), s * 64,
-                        kv_head, crow);
-        }
-      } else if (lane == 0) {
-        for (int s = 0; s < C::kSub; ++s)
-          load_rows(dst + s * C::kSubBytes, tm, bar(BAR_KV_FULL + slot), s * 64, kt * kKeys);
       }
-      issued = u + 1;
+      const uint32_t fb = bar(BAR_KV_FULL + gb);
+      if (lane == 0) mbar_arrive_expect_tx(fb, (has_v ? C::kTileBytes : 0) + (has_k ? C::kTileBytes : 0));
+      __syncwarp();  // the transaction count is armed before any copy lands
+      for (int part = 0; part < 2; ++part) {  // V_{p-1}, then K_p
+        if (part == 0 ? !has_v : !has_k) continue;
+        const int u = part == 0 ? 2 * p - 1 : 2 * p;
+        const uint32_t dst = sbase + C::kOffKV + (u % C::kSlots) * C::kTileBytes;
+        const CUtensorMap* tm = part == 0 ? &tmV : &tmK;
+        if (paged) {
+          if (lane < boxes) {
+            const int cr = part == 0 ? crow_v : crow;
+            for (int s = 0; s < C::kSub; ++s)
+              tma_load_3d(dst + s * C::kSubBytes + lane * args.box_rows * 128, tm, fb, s * 64, kv_head, cr);
+          }
+        } else if (lane == 0) {
+          const int ktile = part == 0 ? kt_v : kt;
+          for (int s = 0; s < C::kSub; ++s) load_rows(dst + s * C::kSubBytes, tm, fb, s * 64, ktile * kKeys);
+        }
+      }
+      groups = p + 1;
     }
     if (__any_sync(0xffffffffu, bad_table) && lane == 0) atomicOr(args.status, kStatusBadTableBit);
     if (lane == 0) {
       // let every issued copy land before the CTA can exit
       if (qbytes != 0 && nmax > 0) drain_wait(bar(BAR_Q), 0);
-      for (int s = 0; s < C::kSlots && s < issued; ++s) {
-        const int u_last = s + C::kSlots * ((issued - 1 - s) / C::kSlots);
-        drain_wait(bar(BAR_KV_FULL + s), static_cast<uint32_t>(u_last / C::kSlots) & 1u);
+      for (int g = 0; g < C::kGroupBars && g < groups; ++g) {
+        const int p_last = g + C::kGroupBars * ((groups - 1 - g) / C::kGroupBars);
+        drain_wait(bar(BAR_KV_FULL + g), static_cast<uint32_t>(p_last / C::kGroupBars) & 1u);
       }
     }
   } else if (warp == 9) {
@@ -392,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ts(dcol, acol + 8 * k, sdesc_advance(db, k * 16 * 128), idPV, (acc || k > 0) ? 1u : 0u);
       };
       bool ok = mbar_wait(bar(BAR_Q), 0, wc);
-      if (ok) ok = mbar_wait(bar(BAR_KV_FULL + 0), 0, wc);
+      if (ok) ok = mbar_wait(bar(BAR_KV_FULL + 0), 0, wc);  // group 0: K_0
       if (ok) {
         tc_fence_after();
         for (int t = 0; t < 2; ++t)
@@ -403,11 +423,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(bar(BAR_KV_EMPTY + 0));
       }
       for (int j = 0; ok && j < nmax; ++j) {
-        const int uV = 2 * j + 1, uK = 2 * j + 2;
-        const int sV = uV % C::kSlots, sK = uK % C::kSlots;
-        const bool next = (j + 1) < nmax;
-        if (!mbar_wait(bar(BAR_KV_FULL + sV), static_cast<uint32_t>(uV / C::kSlots) & 1u, wc)) break;
-        if (next && !mbar_wait(bar(BAR_KV_FULL + sK), static_cast<uint32_t>(uK / C::kSlots) & 1u, wc)) break;
+        const int g = j + 1;  // group of V_j and K_{j+1}
+        const int gb = g % C::kGroupBars;
+        const int sV = (2 * j + 1) % C::kSlots, sK = (2 * j + 2) % C::kSlots;
+        if (!mbar_wait(bar(BAR_KV_FULL + gb), static_cast<uint32_t>(g / C::kGroupBars) & 1u, wc)) break;
         tc_fence_after();
         for (int t = 0; t < 2; ++t) {
           if (j < n_t[t]) {
@@ -425,8 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (!ok) break;
-        mma_commit(bar(BAR_KV_EMPTY + sV));
-        if (next) mma_commit(bar(BAR_KV_EMPTY + sK));
+        mma_commit(bar(BAR_KV_EMPTY + gb));
       }
       // every MMA issued above completes before the CTA releases TMEM
       mma_commit(bar(BAR_DRAIN));
