@@ -125,3 +125,41 @@ def test_full_gqa_decode_config_sampled(fa):
         sub = _compact(P, b)
         oref, lref = oracle.paged_decode(sub.q, sub.k_cache, sub.v_cache, sub.block_table, sub.seq_lens, 16)
         _check(o[b:b + 1], lse[b:b + 1], oref, lref)
+
+
+def _plant_retrieval(P, seed, limits):
+    """Integer mirror of the gather: q is c * e_0 for every head, every key is
+    zero except one target key per (sequence, KV head) whose first coordinate
+    is 64, so the target's logit exceeds every other by ~45 and softmax puts
+    weight 1 on it to fp32 precision: o must equal that key's V row exactly.
+    limits[b] bounds the target's logical position.  Returns the targets."""
+    g = torch.Generator().manual_seed(seed)
+    B, Hq, d = P.q.shape
+    Hkv = P.k_cache.shape[2]
+    P.q.zero_()
+    P.q[..., 0] = 8.0
+    P.k_cache.zero_()
+    targets = torch.zeros(B, Hkv, dtype=torch.long)
+    for b in range(B):
+        for kv in range(Hkv):
+            t = int(torch.randint(0, int(limits[b]), (1,), generator=g))
+            targets[b, kv] = t
+            phys = int(P.block_table[b, t // P.block_size])
+            P.k_cache[phys, t % P.block_size, kv, 0] = 64.0
+    return targets
+
+
+def test_gather_retrieves_exact_rows(fa):
+    # block-table indexing checked bit for bit: every (sequence, query head)
+    # returns exactly the V row its target key maps to through the table
+    for num_splits in (0, 1, 5):
+        P = wl.paged_inputs(6, 16, 4, 128, 1, 1, seed=21, seq_lens=[1, 16, 17, 333, 4096, 9999])
+        tg = _plant_retrieval(P, 5, P.seq_lens.tolist())
+        o, lse = _run(fa, P, num_splits)
+        G = 16 // 4
+        for b in range(6):
+            for h in range(16):
+                t = int(tg[b, h // G])
+                phys = int(P.block_table[b, t // 16])
+                want = P.v_cache[phys, t % 16, h // G].float().numpy()
+                assert np.array_equal(o[b, h], want), (num_splits, b, h)
