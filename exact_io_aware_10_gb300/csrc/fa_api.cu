@@ -253,13 +253,15 @@ int fa_paged_decode(const void* q, const void* k_cache, const void* v_cache, con
   if (B < 1 || Hq < 1 || Hkv < 1 || max_blocks < 1 || num_blocks < 1 || num_splits < 0) return FA_ERR_INVALID_ARG;
   if (Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
   if (bad_scale(scale)) return FA_ERR_INVALID_ARG;
-  if (d != 128 || block_size != 16) return FA_ERR_UNSUPPORTED;
+  if (d != 128 || block_size < 16 || block_size % 16 != 0) return FA_ERR_UNSUPPORTED;
   if (Hq / Hkv > 16 || num_splits > 16) return FA_ERR_UNSUPPORTED;
   if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !o) return FA_ERR_INVALID_ARG;
   if (num_splits != 1 && !workspace) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o)) return FA_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_INVALID_ARG;
-  if (static_cast<long long>(num_blocks) * block_size > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(num_blocks) * block_size > 0x7fffffffLL ||
+      static_cast<long long>(max_blocks) * block_size > 0x7fffffffLL)
+    return FA_ERR_UNSUPPORTED;
   const int S = num_splits == 0 ? 16 : num_splits;
   if (ws_bytes < fa_paged_decode_workspace_size(B, Hq, d, S)) return FA_ERR_INVALID_ARG;
   return fa::decode_launch(q, k_cache, v_cache, block_table, seq_lens, o, lse, B, Hq, Hkv, d, block_size, max_blocks,

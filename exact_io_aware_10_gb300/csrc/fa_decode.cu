@@ -34,7 +34,7 @@ namespace fa {
 namespace {
 
 constexpr int kD = 128;            // head dimension
-constexpr int kBlk = 16;           // tokens per cache block
+constexpr int kBlk = 16;           // tokens per chunk (one ring stage); cache blocks hold a multiple of it
 constexpr int kConsumers = 4;      // consumer warps
 constexpr int kThreads = 32 * (kConsumers + 1);
 constexpr int kStages = 8;
@@ -66,6 +66,7 @@ struct DecArgs {
   float* lse;
   int B, Hq, Hkv, G, max_blocks, num_blocks, S;
   int direct;  // S == 1: the split kernel writes o and lse itself
+  int block_size;  // tokens per cache block, a multiple of kBlk
   int min_blocks;  // smallest split, in blocks
   float scale_log2;
   unsigned* status;
@@ -106,7 +107,9 @@ __global__ void __launch_bounds__(kThreads, 3)
     decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                         const DecArgs a) {
   const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
-  const int L = min(max(a.seq_lens[b], 0), a.max_blocks * kBlk);
+  // the work is cut into 16-token chunks; chunk c lives in cache block
+  // table[c * 16 / block_size] at row (c * 16) % block_size
+  const int L = min(max(a.seq_lens[b], 0), a.max_blocks * a.block_size);
   const int nb = (L + kBlk - 1) / kBlk;
   const int S_b = splits_for(nb, a.S, a.min_blocks);
   if (s >= S_b) return;  // this sequence uses fewer splits
@@ -150,11 +153,12 @@ __global__ void __launch_bounds__(kThreads, 3)
       for (int i = 0; i < nblk; ++i) {
         const int st = i % kStages;
         if (!mbar_wait(empty(st), ((i / kStages) & 1) ^ 1, wc)) break;
-        const int phys = __ldg(table + lo + i);
+        const int chunk_key = (lo + i) * kBlk;
+        const int phys = __ldg(table + chunk_key / a.block_size);
         if (phys >= 0 && phys < a.num_blocks) {
           mbar_arrive_expect_tx(full(st), kStageBytes);
           const uint32_t dst = sbase + st * kStageBytes;
-          const int z = phys * kBlk;
+          const int z = phys * a.block_size + chunk_key % a.block_size;
           tma_load_3d(dst, &tmK, full(st), 0, g, z);
           tma_load_3d(dst + kHalfBytes, &tmK, full(st), 64, g, z);
           tma_load_3d(dst + 2 * kHalfBytes, &tmV, full(st), 0, g, z);
@@ -198,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, 3)
       if (!mbar_wait(full(st), (i / kStages) & 1, wc)) break;
       const uint32_t stK = sbase + st * kStageBytes;
       const uint32_t stV = stK + 2 * kHalfBytes;
-      const int phys = __ldg(table + lo + i);
+      const int phys = __ldg(table + (lo + i) * kBlk / a.block_size);
       const bool bad = !(phys >= 0 && phys < a.num_blocks);
       // ---- S = Q K^T over 16 keys (two n8 tiles)
       float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -324,7 +328,7 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecArgs a) {
   const int lane = threadIdx.x & 31;
   if (gw >= a.B * a.Hq) return;
   const int b = gw / a.Hq;
-  const int L = min(max(a.seq_lens[b], 0), a.max_blocks * kBlk);
+  const int L = min(max(a.seq_lens[b], 0), a.max_blocks * a.block_size);
   const int S_b = splits_for((L + kBlk - 1) / kBlk, a.S, a.min_blocks);
   const float* po = a.part_o + static_cast<size_t>(gw) * a.S * kD;
   const float* pml = a.part_ml + static_cast<size_t>(gw) * a.S * 2;
@@ -372,9 +376,9 @@ fa_status decode_launch(const void* q, const void* k_cache, const void* v_cache,
                         const int32_t* seq_lens, void* o, float* lse, int B, int Hq, int Hkv, int d, int block_size,
                         int max_blocks, int num_blocks, int num_splits, float scale, void* workspace,
                         cudaStream_t stream) {
-  if (d != kD || block_size != kBlk) return FA_ERR_UNSUPPORTED;
+  if (d != kD || block_size < kBlk || block_size % kBlk != 0) return FA_ERR_UNSUPPORTED;
   const uint64_t dims[3] = {static_cast<uint64_t>(kD), static_cast<uint64_t>(Hkv),
-                            static_cast<uint64_t>(num_blocks) * kBlk};
+                            static_cast<uint64_t>(num_blocks) * block_size};
   const uint64_t strides[2] = {static_cast<uint64_t>(kD) * 2, static_cast<uint64_t>(Hkv) * kD * 2};
   const uint32_t box[3] = {64, 1, kBlk};
   CUtensorMap tk, tv;
@@ -400,6 +404,7 @@ fa_status decode_launch(const void* q, const void* k_cache, const void* v_cache,
   a.num_blocks = num_blocks;
   a.S = num_splits;
   a.direct = num_splits == 1 ? 1 : 0;
+  a.block_size = block_size;
   a.min_blocks = (static_cast<long long>(B) * Hkv >= kFewUnits) ? kMinBlocksPerSplit : kMinBlocksPerSplitFew;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.status = status;
@@ -466,7 +471,7 @@ extern "C" int fa_paged_decode_noalloc(const void* q, const void* k_cache, const
   if (B < 1 || Hq < 1 || Hkv < 1 || max_blocks < 1 || num_blocks < 1 || num_splits < 0) return FA_ERR_INVALID_ARG;
   if (Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !isfinite(scale)) return FA_ERR_INVALID_ARG;
-  if (d != fa::kD || block_size != fa::kBlk) return FA_ERR_UNSUPPORTED;
+  if (d != fa::kD || block_size < fa::kBlk || block_size % fa::kBlk != 0) return FA_ERR_UNSUPPORTED;
   if (Hq / Hkv > 16 || num_splits > 16) return FA_ERR_UNSUPPORTED;
   if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !o) return FA_ERR_INVALID_ARG;
   if (!al16(q) || !al16(k_cache) || !al16(v_cache) || !al16(o)) return FA_ERR_INVALID_ARG;

@@ -210,7 +210,8 @@ size_t fa_paged_decode_workspace_size(int B, int Hq, int d, int num_splits);
  *                 block_size (larger values are clamped to that bound).
  *   o           : [B, Hq, d] bf16, written.  lse: [B, Hq] fp32 or NULL.
  *   Query head h reads KV head h / (Hq / Hkv); Hq % Hkv must be 0.
- *   block_size  : 16.  num_splits: 1..16, or 0 for automatic (16).
+ *   block_size  : a multiple of 16 (16, 32, 64, ...).
+ *   num_splits  : 1..16, or 0 for automatic (16).
  *   workspace   : at least fa_paged_decode_workspace_size(B, Hq, d,
  *                 num_splits) bytes, 256-byte aligned; may be NULL when
  *                 num_splits = 1 (one fused launch, the short-context and

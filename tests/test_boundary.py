@@ -176,8 +176,10 @@ def test_decode_argument_validation(so):
 
     assert call(Hkv=5) == fl.FA_ERR_INVALID_ARG          # Hq % Hkv != 0
     assert call(d=64) == fl.FA_ERR_UNSUPPORTED
-    assert call(bs=32) == fl.FA_ERR_UNSUPPORTED
+    for bad_bs in (8, 24, 40):                             # not a multiple of 16
+        assert call(bs=bad_bs) == fl.FA_ERR_UNSUPPORTED
     assert call(S=17) == fl.FA_ERR_UNSUPPORTED
+    assert so.fa_paged_decode_workspace_size(4, 32, 128, 1) == 0  # one split: fused, no workspace
     assert call(nb=0) == fl.FA_ERR_INVALID_ARG
 
 

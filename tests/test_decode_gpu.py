@@ -152,14 +152,24 @@ def _plant_retrieval(P, seed, limits):
 def test_gather_retrieves_exact_rows(fa):
     # block-table indexing checked bit for bit: every (sequence, query head)
     # returns exactly the V row its target key maps to through the table
-    for num_splits in (0, 1, 5):
-        P = wl.paged_inputs(6, 16, 4, 128, 1, 1, seed=21, seq_lens=[1, 16, 17, 333, 4096, 9999])
+    for bs, num_splits in ((16, 0), (16, 1), (16, 5), (64, 0), (64, 1)):
+        P = wl.paged_inputs(6, 16, 4, 128, 1, 1, block_size=bs, seed=21, seq_lens=[1, 16, 17, 333, 4096, 9999])
         tg = _plant_retrieval(P, 5, P.seq_lens.tolist())
         o, lse = _run(fa, P, num_splits)
         G = 16 // 4
         for b in range(6):
             for h in range(16):
                 t = int(tg[b, h // G])
-                phys = int(P.block_table[b, t // 16])
-                want = P.v_cache[phys, t % 16, h // G].float().numpy()
-                assert np.array_equal(o[b, h], want), (num_splits, b, h)
+                phys = int(P.block_table[b, t // bs])
+                want = P.v_cache[phys, t % bs, h // G].float().numpy()
+                assert np.array_equal(o[b, h], want), (bs, num_splits, b, h)
+
+
+@pytest.mark.parametrize("bs", [32, 64, 256])
+def test_larger_cache_blocks(fa, bs):
+    # blocks of 32..256 tokens are walked as 16-token chunks through the table
+    P = wl.paged_inputs(4, 16, 4, 128, 1, 1, block_size=bs, seed=bs, seq_lens=[1, bs - 1, bs + 17, 3000])
+    for num_splits in (0, 1, 7):
+        o, lse = _run(fa, P, num_splits)
+        oref, lref = oracle.paged_decode(P.q, P.k_cache, P.v_cache, P.block_table, P.seq_lens, bs)
+        _check(o, lse, oref, lref)
