@@ -253,7 +253,7 @@ int fa_paged_decode(const void* q, const void* k_cache, const void* v_cache, con
   if (B < 1 || Hq < 1 || Hkv < 1 || max_blocks < 1 || num_blocks < 1 || num_splits < 0) return FA_ERR_INVALID_ARG;
   if (Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
   if (bad_scale(scale)) return FA_ERR_INVALID_ARG;
-  if (d != 128 || block_size < 16 || block_size % 16 != 0) return FA_ERR_UNSUPPORTED;
+  if ((d != 64 && d != 128) || block_size < 16 || block_size % 16 != 0) return FA_ERR_UNSUPPORTED;
   if (Hq / Hkv > 16 || num_splits > 16) return FA_ERR_UNSUPPORTED;
   if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !o) return FA_ERR_INVALID_ARG;
   if (num_splits != 1 && !workspace) return FA_ERR_INVALID_ARG;

@@ -33,17 +33,22 @@
 namespace fa {
 namespace {
 
-constexpr int kD = 128;            // head dimension
+constexpr int kDMax = 128;         // largest head dimension (64 and 128 are built)
 constexpr int kBlk = 16;           // tokens per chunk (one ring stage); cache blocks hold a multiple of it
 constexpr int kConsumers = 4;      // consumer warps
 constexpr int kThreads = 32 * (kConsumers + 1);
 constexpr int kStages = 8;
 constexpr int kHalfBytes = kBlk * 128;           // 16 rows x 128 B (64 bf16)
-constexpr int kStageBytes = 4 * kHalfBytes;      // K lo, K hi, V lo, V hi
-constexpr int kOffBar = kStages * kStageBytes;   // 64 KiB of stages
-constexpr int kMergeBytes = kConsumers * (16 * kD + 32) * 4;  // per-warp O rows + m, l
-constexpr int kSmemBytes = kOffBar + 256 + 1024;
-static_assert(kMergeBytes <= kOffBar, "merge scratch reuses the stage ring");
+
+template <int D>
+struct DecCfg {
+  static constexpr int kHalves = D / 64;                        // 128-byte halves per row
+  static constexpr int kStageBytes = 2 * kHalves * kHalfBytes;  // K halves, then V halves
+  static constexpr int kOffBar = kStages * kStageBytes;
+  static constexpr int kMergeBytes = kConsumers * (16 * D + 32) * 4;  // per-warp O rows + m, l
+  static constexpr int kSmemBytes = kOffBar + 256 + 1024;
+  static_assert(kMergeBytes <= kOffBar, "merge scratch reuses the stage ring");
+};
 // A split covers at least kMinBlocksPerSplit blocks (512 keys) when the batch
 // alone fills the GPU (B * Hkv >= kFewUnits), else kMinBlocksPerSplitFew (128
 // keys), so a small batch still spreads its keys over enough CTAs.
@@ -103,9 +108,13 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
+template <int D>
 __global__ void __launch_bounds__(kThreads, 3)
     decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                         const DecArgs a) {
+  using C = DecCfg<D>;
+  constexpr int kOffBar = C::kOffBar;
+  constexpr int kStageBytes = C::kStageBytes;
   const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   // the work is cut into 16-token chunks; chunk c lives in cache block
   // table[c * 16 / block_size] at row (c * 16) % block_size
@@ -140,9 +149,9 @@ __global__ void __launch_bounds__(kThreads, 3)
   // per-thread softmax state for rows r0 = lane / 4 and r0 + 8 of the group
   float m_run[2] = {-INFINITY, -INFINITY};
   float l_run[2] = {0.f, 0.f};
-  float acc[16][4];
+  float acc[D / 8][4];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+  for (int i = 0; i < D / 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
 
   if (warp == kConsumers) {
     // ------------------------------------------------------------ producer
@@ -159,10 +168,11 @@ __global__ void __launch_bounds__(kThreads, 3)
           mbar_arrive_expect_tx(full(st), kStageBytes);
           const uint32_t dst = sbase + st * kStageBytes;
           const int z = phys * a.block_size + chunk_key % a.block_size;
-          tma_load_3d(dst, &tmK, full(st), 0, g, z);
-          tma_load_3d(dst + kHalfBytes, &tmK, full(st), 64, g, z);
-          tma_load_3d(dst + 2 * kHalfBytes, &tmV, full(st), 0, g, z);
-          tma_load_3d(dst + 3 * kHalfBytes, &tmV, full(st), 64, g, z);
+#pragma unroll
+          for (int h = 0; h < C::kHalves; ++h) {
+            tma_load_3d(dst + h * kHalfBytes, &tmK, full(st), 64 * h, g, z);
+            tma_load_3d(dst + (C::kHalves + h) * kHalfBytes, &tmV, full(st), 64 * h, g, z);
+          }
         } else {
           atomicOr(a.status, kStatusBadTableBit);
           mbar_arrive(full(st));  // nothing to load: the consumer masks this block
@@ -180,13 +190,13 @@ __global__ void __launch_bounds__(kThreads, 3)
     const int c2 = 2 * (lane & 3);
     const int h0 = g * a.G;
     // Q as the A operand (16 x 128, rows >= G are zero), kept in registers
-    uint32_t qa[8][4];
+    uint32_t qa[D / 16][4];
     {
-      const uint32_t* q0 = reinterpret_cast<const uint32_t*>(a.q + (static_cast<size_t>(b) * a.Hq + h0 + r0) * kD);
-      const uint32_t* q8 = reinterpret_cast<const uint32_t*>(a.q + (static_cast<size_t>(b) * a.Hq + h0 + r0 + 8) * kD);
+      const uint32_t* q0 = reinterpret_cast<const uint32_t*>(a.q + (static_cast<size_t>(b) * a.Hq + h0 + r0) * D);
+      const uint32_t* q8 = reinterpret_cast<const uint32_t*>(a.q + (static_cast<size_t>(b) * a.Hq + h0 + r0 + 8) * D);
       const bool v0 = r0 < a.G, v8 = r0 + 8 < a.G;
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
+      for (int ks = 0; ks < D / 16; ++ks) {
         const int col = (16 * ks + c2) >> 1;  // in bf16 pairs
         qa[ks][0] = v0 ? __ldg(q0 + col) : 0u;
         qa[ks][1] = v8 ? __ldg(q8 + col) : 0u;
@@ -201,13 +211,13 @@ __global__ void __launch_bounds__(kThreads, 3)
       const int st = i % kStages;
       if (!mbar_wait(full(st), (i / kStages) & 1, wc)) break;
       const uint32_t stK = sbase + st * kStageBytes;
-      const uint32_t stV = stK + 2 * kHalfBytes;
+      const uint32_t stV = stK + C::kHalves * kHalfBytes;
       const int phys = __ldg(table + (lo + i) * kBlk / a.block_size);
       const bool bad = !(phys >= 0 && phys < a.num_blocks);
       // ---- S = Q K^T over 16 keys (two n8 tiles)
       float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
+      for (int ks = 0; ks < D / 16; ++ks) {
         uint32_t k0, k1, k2, k3;
         const int key = 8 * (lm >> 1) + li;
         ldsm_x4(chunk_addr(stK, key, 2 * ks + (lm & 1)), k0, k1, k2, k3);
@@ -242,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 3)
         pa[2 + rr] = pack_bf16x2(p2, p3);  // keys 8-15: a4a5 / a6a7
       }
 #pragma unroll
-      for (int dn = 0; dn < 16; ++dn) {
+      for (int dn = 0; dn < D / 8; ++dn) {
         acc[dn][0] *= alpha[0];
         acc[dn][1] *= alpha[0];
         acc[dn][2] *= alpha[1];
@@ -250,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 3)
       }
       // ---- O += P V  (V^T fragments through ldmatrix.trans)
 #pragma unroll
-      for (int dn2 = 0; dn2 < 8; ++dn2) {
+      for (int dn2 = 0; dn2 < D / 16; ++dn2) {
         uint32_t v0, v1, v2, v3;
         const int key = 8 * (lm & 1) + li;
         ldsm_x4_t(chunk_addr(stV, key, 2 * dn2 + (lm >> 1)), v0, v1, v2, v3);
@@ -271,14 +281,14 @@ __global__ void __launch_bounds__(kThreads, 3)
   // ---------------------------------------------------------------- merge warps
   __syncthreads();  // every stage consumed; the ring becomes merge scratch
   float* sO = reinterpret_cast<float*>(smem);               // [warp][16][D]
-  float* sML = sO + kConsumers * 16 * kD;                   // [warp][16][2]
+  float* sML = sO + kConsumers * 16 * D;                   // [warp][16][2]
   if (warp < kConsumers) {
     const int r0 = lane >> 2, c2 = 2 * (lane & 3);
-    float* w = sO + warp * 16 * kD;
+    float* w = sO + warp * 16 * D;
 #pragma unroll
-    for (int dn = 0; dn < 16; ++dn) {
-      *reinterpret_cast<float2*>(w + r0 * kD + 8 * dn + c2) = make_float2(acc[dn][0], acc[dn][1]);
-      *reinterpret_cast<float2*>(w + (r0 + 8) * kD + 8 * dn + c2) = make_float2(acc[dn][2], acc[dn][3]);
+    for (int dn = 0; dn < D / 8; ++dn) {
+      *reinterpret_cast<float2*>(w + r0 * D + 8 * dn + c2) = make_float2(acc[dn][0], acc[dn][1]);
+      *reinterpret_cast<float2*>(w + (r0 + 8) * D + 8 * dn + c2) = make_float2(acc[dn][2], acc[dn][3]);
     }
     if ((lane & 3) == 0) {
       sML[(warp * 16 + r0) * 2 + 0] = m_run[0];
@@ -288,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 3)
     }
   }
   __syncthreads();
-  if (threadIdx.x < kD) {
+  if (threadIdx.x < D) {
     const int dcol = threadIdx.x;
     for (int r = 0; r < a.G; ++r) {
       float m = -INFINITY;
@@ -300,20 +310,20 @@ __global__ void __launch_bounds__(kThreads, 3)
         for (int w = 0; w < kConsumers; ++w) {
           const float wm = sML[(w * 16 + r) * 2];
           const float f = ex2_approx(wm - m);  // 0 for warps that saw nothing
-          o += f * sO[(w * 16 + r) * kD + dcol];
+          o += f * sO[(w * 16 + r) * D + dcol];
           l += f * sML[(w * 16 + r) * 2 + 1];
         }
       }
       if (a.direct) {
         const size_t row = static_cast<size_t>(b) * a.Hq + g * a.G + r;
         const float inv = (l > 0.f) ? 1.f / l : 0.f;
-        a.o[row * kD + dcol] = __float2bfloat16_rn(o * inv);
+        a.o[row * D + dcol] = __float2bfloat16_rn(o * inv);
         if (a.lse != nullptr && dcol == 0)
           a.lse[row] = (l > 0.f) ? (m + lg2_approx(l)) * 0.69314718055994531f : -INFINITY;
         continue;
       }
       const size_t idx = (static_cast<size_t>(b) * a.Hq + g * a.G + r) * a.S + s;
-      a.part_o[idx * kD + dcol] = o;
+      a.part_o[idx * D + dcol] = o;
       if (dcol == 0) {
         a.part_ml[2 * idx] = m;
         a.part_ml[2 * idx + 1] = l;
@@ -322,39 +332,56 @@ __global__ void __launch_bounds__(kThreads, 3)
   }
 }
 
-// One warp per (b, query head): merge the sequence's split states.
+// One warp per (b, query head): merge the sequence's split states; each lane
+// handles D / 32 consecutive entries of o.
+template <int D>
 __global__ void __launch_bounds__(256) decode_combine_kernel(const DecArgs a) {
+  constexpr int kPer = D / 32;
   const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (gw >= a.B * a.Hq) return;
   const int b = gw / a.Hq;
   const int L = min(max(a.seq_lens[b], 0), a.max_blocks * a.block_size);
   const int S_b = splits_for((L + kBlk - 1) / kBlk, a.S, a.min_blocks);
-  const float* po = a.part_o + static_cast<size_t>(gw) * a.S * kD;
+  const float* po = a.part_o + static_cast<size_t>(gw) * a.S * D;
   const float* pml = a.part_ml + static_cast<size_t>(gw) * a.S * 2;
   float m = -INFINITY;
   for (int s = 0; s < S_b; ++s)
     if (pml[2 * s + 1] > 0.f) m = fmaxf(m, pml[2 * s]);
-  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+  float o[kPer];
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) o[e] = 0.f;
   float l = 0.f;
   if (m != -INFINITY) {
     for (int s = 0; s < S_b; ++s) {
       const float ls = pml[2 * s + 1];
       if (!(ls > 0.f)) continue;
       const float f = ex2_approx(pml[2 * s] - m);
-      const float4 v = *reinterpret_cast<const float4*>(po + static_cast<size_t>(s) * kD + 4 * lane);
-      o.x += f * v.x;
-      o.y += f * v.y;
-      o.z += f * v.z;
-      o.w += f * v.w;
+      const float* src = po + static_cast<size_t>(s) * D + kPer * lane;
+      if constexpr (kPer == 4) {
+        const float4 v = *reinterpret_cast<const float4*>(src);
+        o[0] += f * v.x;
+        o[1] += f * v.y;
+        o[2] += f * v.z;
+        o[3] += f * v.w;
+      } else {
+        const float2 v = *reinterpret_cast<const float2*>(src);
+        o[0] += f * v.x;
+        o[1] += f * v.y;
+      }
       l += f * ls;
     }
   }
   const float inv = (l > 0.f) ? 1.f / l : 0.f;
-  uint2 w;
-  w.x = pack_bf16x2(o.x * inv, o.y * inv);
-  w.y = pack_bf16x2(o.z * inv, o.w * inv);
-  *reinterpret_cast<uint2*>(a.o + static_cast<size_t>(gw) * kD + 4 * lane) = w;
+  __nv_bfloat16* dst = a.o + static_cast<size_t>(gw) * D + kPer * lane;
+  if constexpr (kPer == 4) {
+    uint2 w;
+    w.x = pack_bf16x2(o[0] * inv, o[1] * inv);
+    w.y = pack_bf16x2(o[2] * inv, o[3] * inv);
+    *reinterpret_cast<uint2*>(dst) = w;
+  } else {
+    *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(o[0] * inv, o[1] * inv);
+  }
   if (a.lse != nullptr && lane == 0)
     a.lse[gw] = (l > 0.f) ? (m + lg2_approx(l)) * 0.69314718055994531f : -INFINITY;
 }
@@ -364,22 +391,25 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecArgs a) {
 fa_status decode_prepare() {
   static bool attr_set = false;  // setting it twice is harmless
   if (!attr_set) {
-    if (cudaFuncSetAttribute(decode_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(decode_split_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             DecCfg<128>::kSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(decode_split_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             DecCfg<64>::kSmemBytes) != cudaSuccess)
       return FA_ERR_CUDA;
     attr_set = true;
   }
   return FA_OK;
 }
 
-fa_status decode_launch(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
-                        const int32_t* seq_lens, void* o, float* lse, int B, int Hq, int Hkv, int d, int block_size,
-                        int max_blocks, int num_blocks, int num_splits, float scale, void* workspace,
-                        cudaStream_t stream) {
-  if (d != kD || block_size < kBlk || block_size % kBlk != 0) return FA_ERR_UNSUPPORTED;
-  const uint64_t dims[3] = {static_cast<uint64_t>(kD), static_cast<uint64_t>(Hkv),
+namespace {
+template <int D>
+fa_status decode_launch_d(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                          const int32_t* seq_lens, void* o, float* lse, int B, int Hq, int Hkv, int block_size,
+                          int max_blocks, int num_blocks, int num_splits, float scale, void* workspace,
+                          cudaStream_t stream) {
+  const uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(Hkv),
                             static_cast<uint64_t>(num_blocks) * block_size};
-  const uint64_t strides[2] = {static_cast<uint64_t>(kD) * 2, static_cast<uint64_t>(Hkv) * kD * 2};
+  const uint64_t strides[2] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(Hkv) * D * 2};
   const uint32_t box[3] = {64, 1, kBlk};
   CUtensorMap tk, tv;
   if (!encode_bf16_tmap(&tk, k_cache, 3, dims, strides, box) || !encode_bf16_tmap(&tv, v_cache, 3, dims, strides, box))
@@ -393,7 +423,7 @@ fa_status decode_launch(const void* q, const void* k_cache, const void* v_cache,
   a.seq_lens = seq_lens;
   const size_t n_part = static_cast<size_t>(B) * Hq * num_splits;
   a.part_o = static_cast<float*>(workspace);
-  a.part_ml = a.part_o + ((n_part * kD + 63) & ~static_cast<size_t>(63));
+  a.part_ml = a.part_o + ((n_part * D + 63) & ~static_cast<size_t>(63));
   a.o = static_cast<__nv_bfloat16*>(o);
   a.lse = lse;
   a.B = B;
@@ -409,11 +439,26 @@ fa_status decode_launch(const void* q, const void* k_cache, const void* v_cache,
   a.scale_log2 = scale * 1.4426950408889634f;
   a.status = status;
   dim3 grid(num_splits, Hkv, B);
-  decode_split_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tk, tv, a);
+  decode_split_kernel<D><<<grid, kThreads, DecCfg<D>::kSmemBytes, stream>>>(tk, tv, a);
   if (a.direct) return launch_status();
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
-  decode_combine_kernel<<<ceil_div(static_cast<long long>(B) * Hq, 8), 256, 0, stream>>>(a);
+  decode_combine_kernel<D><<<ceil_div(static_cast<long long>(B) * Hq, 8), 256, 0, stream>>>(a);
   return launch_status();
+}
+}  // namespace
+
+fa_status decode_launch(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                        const int32_t* seq_lens, void* o, float* lse, int B, int Hq, int Hkv, int d, int block_size,
+                        int max_blocks, int num_blocks, int num_splits, float scale, void* workspace,
+                        cudaStream_t stream) {
+  if (block_size < kBlk || block_size % kBlk != 0) return FA_ERR_UNSUPPORTED;
+  if (d == 128)
+    return decode_launch_d<128>(q, k_cache, v_cache, block_table, seq_lens, o, lse, B, Hq, Hkv, block_size,
+                                max_blocks, num_blocks, num_splits, scale, workspace, stream);
+  if (d == 64)
+    return decode_launch_d<64>(q, k_cache, v_cache, block_table, seq_lens, o, lse, B, Hq, Hkv, block_size,
+                               max_blocks, num_blocks, num_splits, scale, workspace, stream);
+  return FA_ERR_UNSUPPORTED;
 }
 
 }  // namespace fa
@@ -441,7 +486,7 @@ namespace fa {
 namespace {
 
 constexpr size_t kNoAllocMaxStates = 32768;
-static __device__ __align__(256) float g_decode_scratch[kNoAllocMaxStates * (kD + 2)];
+static __device__ __align__(256) float g_decode_scratch[kNoAllocMaxStates * (kDMax + 2)];
 
 std::mutex g_scratch_mu;
 float* g_scratch_ptr[64] = {};
@@ -471,7 +516,7 @@ extern "C" int fa_paged_decode_noalloc(const void* q, const void* k_cache, const
   if (B < 1 || Hq < 1 || Hkv < 1 || max_blocks < 1 || num_blocks < 1 || num_splits < 0) return FA_ERR_INVALID_ARG;
   if (Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !isfinite(scale)) return FA_ERR_INVALID_ARG;
-  if (d != fa::kD || block_size < fa::kBlk || block_size % fa::kBlk != 0) return FA_ERR_UNSUPPORTED;
+  if ((d != 64 && d != 128) || block_size < fa::kBlk || block_size % fa::kBlk != 0) return FA_ERR_UNSUPPORTED;
   if (Hq / Hkv > 16 || num_splits > 16) return FA_ERR_UNSUPPORTED;
   if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !o) return FA_ERR_INVALID_ARG;
   if (!al16(q) || !al16(k_cache) || !al16(v_cache) || !al16(o)) return FA_ERR_INVALID_ARG;

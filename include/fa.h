@@ -197,7 +197,7 @@ size_t fa_paged_decode_workspace_size(int B, int Hq, int d, int num_splits);
 /*
  * Paged, split-KV, grouped-query decode (S12 "实现" paged loop, flash-decoding
  * split + (m, l, o) merge, GQA head sharing).
- *   q           : [B, Hq, d] bf16, one query token per sequence.
+ *   q           : [B, Hq, d] bf16, one query token per sequence (d = 64 or 128).
  *   k_cache,
  *   v_cache     : [num_blocks, block_size, Hkv, d] bf16; key t of sequence b
  *                 and KV head g is k_cache[block_table[b][t / block_size],

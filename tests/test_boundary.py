@@ -175,7 +175,7 @@ def test_decode_argument_validation(so):
                                   a["nb"], a["S"], 0.088, ws, need, s)
 
     assert call(Hkv=5) == fl.FA_ERR_INVALID_ARG          # Hq % Hkv != 0
-    assert call(d=64) == fl.FA_ERR_UNSUPPORTED
+    assert call(d=96) == fl.FA_ERR_UNSUPPORTED
     for bad_bs in (8, 24, 40):                             # not a multiple of 16
         assert call(bs=bad_bs) == fl.FA_ERR_UNSUPPORTED
     assert call(S=17) == fl.FA_ERR_UNSUPPORTED

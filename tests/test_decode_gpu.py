@@ -173,3 +173,31 @@ def test_larger_cache_blocks(fa, bs):
         o, lse = _run(fa, P, num_splits)
         oref, lref = oracle.paged_decode(P.q, P.k_cache, P.v_cache, P.block_table, P.seq_lens, bs)
         _check(o, lse, oref, lref)
+
+
+@pytest.mark.parametrize("G", [1, 4, 8])
+def test_head_dim_64(fa, G):
+    Hkv = 4
+    P = wl.paged_inputs(5, G * Hkv, Hkv, 64, 1, 1, seed=40 + G, seq_lens=[0, 1, 17, 700, 5000])
+    for num_splits in (0, 1, 3):
+        o, lse = _run(fa, P, num_splits)
+        oref, lref = oracle.paged_decode(P.q, P.k_cache, P.v_cache, P.block_table, P.seq_lens, 16)
+        _check(o, lse, oref, lref)
+
+
+def test_head_dim_64_exact_retrieval_and_graph(fa):
+    P = wl.paged_inputs(3, 8, 2, 64, 1, 1, block_size=32, seed=44, seq_lens=[5, 300, 2000])
+    tg = _plant_retrieval(P, 9, P.seq_lens.tolist())
+    o, _ = _run(fa, P)
+    for b in range(3):
+        for h in range(8):
+            t = int(tg[b, h // 4])
+            want = P.v_cache[int(P.block_table[b, t // 32]), t % 32, h // 4].float().numpy()
+            assert np.array_equal(o[b, h], want)
+    q, kc, vc, bt, sl = _dev(P)
+    layer = (q, kc, vc, torch.empty_like(q), torch.empty(3, 8, dtype=torch.float32, device=q.device))
+    g = fa.DecodeGraph([layer], bt, sl)
+    g.launch()
+    torch.cuda.synchronize()
+    assert np.array_equal(layer[3].float().cpu().numpy(), o)
+    g.close()
