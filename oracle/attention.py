@@ -288,3 +288,20 @@ def attention_forward_varlen(Q, K, V, cu_seqlens, causal=False, scale=None):
         O[a:b] = o[0].transpose(1, 0, 2)
         LSE[:, a:b] = lse[0]
     return O, LSE
+
+
+def attention_backward_varlen(Q, K, V, dO, cu_seqlens, causal=False, scale=None):
+    """Gradients of sum(dO * O) for the packed ragged batch of
+    attention_forward_varlen: attention_backward applied to each sequence
+    (sequences do not interact).  Q, K, V, dO [total, H, d] -> dQ, dK, dV."""
+    Q, K, V, dO = to_f64(Q), to_f64(K), to_f64(V), to_f64(dO)
+    cu = np.asarray(cu_seqlens.cpu().numpy() if hasattr(cu_seqlens, "cpu") else cu_seqlens, dtype=np.int64)
+    dQ, dK, dV = np.zeros_like(Q), np.zeros_like(K), np.zeros_like(V)
+    for s in range(len(cu) - 1):
+        a, b = int(cu[s]), int(cu[s + 1])
+        if b <= a:
+            continue
+        q, k, v, g = (x[a:b].transpose(1, 0, 2)[None] for x in (Q, K, V, dO))
+        gq, gk, gv = attention_backward(q, k, v, g, causal=causal, scale=scale)
+        dQ[a:b], dK[a:b], dV[a:b] = (x[0].transpose(1, 0, 2) for x in (gq, gk, gv))
+    return dQ, dK, dV

@@ -395,3 +395,49 @@ def test_varlen_oracle_is_per_sequence_attention_and_ignores_neighbours():
         keep = np.r_[0:int(cu[2]), int(cu[3]):total]
         np.testing.assert_array_equal(O2[keep], O[keep])
         assert not np.allclose(O2[int(cu[2]):int(cu[3])], O[int(cu[2]):int(cu[3])])
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_backward_matches_finite_differences_of_the_packed_loss(causal):
+    # the packed gradients are the derivative of sum(dO * O_varlen): central
+    # differences through attention_forward_varlen on every coordinate of a
+    # tiny ragged batch (lengths 3, 1, 0, 4), independent of the per-sequence
+    # unpacking inside the backward
+    H, d = 2, 3
+    lens = [3, 1, 0, 4]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    total = int(cu[-1])
+    Q, K, V, dO = (_rand((total, H, d), s) for s in (70, 71, 72, 73))
+    scale = 0.7
+    dQ, dK, dV = oracle.attention_backward_varlen(Q, K, V, dO, cu, causal=causal, scale=scale)
+
+    def loss(q, k, v):
+        o, _ = oracle.attention_forward_varlen(q, k, v, cu, causal=causal, scale=scale)
+        return float((o * dO).sum())
+
+    h = 1e-6
+    for name, X, G in (("Q", Q, dQ), ("K", K, dK), ("V", V, dV)):
+        num = np.zeros_like(X)
+        for idx in np.ndindex(X.shape):
+            Xp, Xm = X.copy(), X.copy()
+            Xp[idx] += h
+            Xm[idx] -= h
+            args_p = [Xp if n == name else Y for n, Y in (("Q", Q), ("K", K), ("V", V))]
+            args_m = [Xm if n == name else Y for n, Y in (("Q", Q), ("K", K), ("V", V))]
+            num[idx] = (loss(*args_p) - loss(*args_m)) / (2 * h)
+        np.testing.assert_allclose(G, num, atol=1e-7, rtol=1e-6, err_msg=name)
+
+
+def test_varlen_backward_sequences_are_independent():
+    H, d = 2, 4
+    lens = [5, 9, 2]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    total = int(cu[-1])
+    Q, K, V, dO = (_rand((total, H, d), s) for s in (80, 81, 82, 83))
+    g1 = oracle.attention_backward_varlen(Q, K, V, dO, cu, causal=True)
+    K2 = K.copy()
+    K2[5:14] += _rand((9, H, d), 84)  # sequence 1 only
+    g2 = oracle.attention_backward_varlen(Q, K2, V, dO, cu, causal=True)
+    keep = np.r_[0:5, 14:16]
+    for a, b in zip(g1, g2):
+        np.testing.assert_array_equal(a[keep], b[keep])
