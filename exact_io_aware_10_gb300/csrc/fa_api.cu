@@ -147,7 +147,7 @@ const char* fa_status_string(int status) {
   }
 }
 
-int fa_version(void) { return 104; }
+int fa_version(void) { return 105; }
 
 int fa_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d, int causal,
               float scale, const int32_t* kv_lens, void* stream) {
@@ -236,6 +236,32 @@ int fa_bwd(const void* Q, const void* K, const void* V, const void* O, const voi
   if (ws_bytes < fa_bwd_workspace_size(B, H, N, d)) return FA_ERR_INVALID_ARG;
   return fa::bwd_launch(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, causal, scale, kv_lens, workspace,
                         static_cast<cudaStream_t>(stream));
+}
+
+size_t fa_bwd_varlen_workspace_size(int num_seqs, int total, int max_seqlen, int H, int d) {
+  if (num_seqs < 1 || total < 0 || max_seqlen < 0 || H < 1 || d < 1) return 0;
+  const size_t rows = static_cast<size_t>(num_seqs) * H * ((static_cast<size_t>(max_seqlen) + 127) / 128 * 128);
+  return 2 * round256(rows * sizeof(float)) + round256(static_cast<size_t>(total) * H * d * sizeof(float));
+}
+
+int fa_bwd_varlen(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
+                  void* dQ, void* dK, void* dV, const int32_t* cu_seqlens, int num_seqs, int total, int max_seqlen,
+                  int H, int d, int causal, float scale, void* workspace, size_t ws_bytes, void* stream) {
+  if (num_seqs < 1 || total < 0 || max_seqlen < 0 || H < 1) return FA_ERR_INVALID_ARG;
+  if (bad_scale(scale)) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (num_seqs > 65535 || static_cast<long long>(num_seqs) * H > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  if ((static_cast<long long>(max_seqlen) + 127) / 128 * 4 > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  if (total == 0 || max_seqlen == 0) return FA_OK;
+  if (!Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV || !cu_seqlens || !workspace)
+    return FA_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(dO) || !aligned16(dQ) ||
+      !aligned16(dK) || !aligned16(dV))
+    return FA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_INVALID_ARG;
+  if (ws_bytes < fa_bwd_varlen_workspace_size(num_seqs, total, max_seqlen, H, d)) return FA_ERR_INVALID_ARG;
+  return fa::bwd_varlen_launch(Q, K, V, O, dO, LSE, dQ, dK, dV, cu_seqlens, num_seqs, total, max_seqlen, H, d, causal,
+                               scale, workspace, static_cast<cudaStream_t>(stream));
 }
 
 size_t fa_paged_decode_workspace_size(int B, int Hq, int d, int num_splits) {

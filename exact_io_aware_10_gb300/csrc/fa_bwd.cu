@@ -110,6 +110,12 @@ struct BwdArgs {
   float scale;
   float scale_log2;
   unsigned* status;
+  // packed ragged batch (nullptr: dense): Q/K/V/O/dO/dQ/dK/dV and dQacc are
+  // [total, H, D], LSE is [H, total]; "batch entry" b is sequence b, rows
+  // cu_seqlens[b] .. cu_seqlens[b+1]-1, and N is the longest sequence.  Kept
+  // last: the dense kernel's register allocation is sensitive to the layout.
+  const int32_t* cu_seqlens;
+  int total;
 };
 
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
@@ -130,6 +136,19 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
                : "memory");
 }
 
+// Rows of sequence b in a packed batch: [tok0, tok0 + len).  The offsets must
+// be non-decreasing, start at 0, end at total, and no sequence may be longer
+// than N (the longest sequence the launch was sized for); otherwise len = -1.
+__device__ __forceinline__ int packed_range(const BwdArgs& a, int b, int& tok0) {
+  tok0 = a.cu_seqlens[b];
+  const int tok1 = a.cu_seqlens[b + 1];
+  const int nseq = a.BH / a.H;
+  if (tok0 < 0 || tok1 < tok0 || tok1 > a.total || tok1 - tok0 > a.N || (b == 0 && tok0 != 0) ||
+      (b == nseq - 1 && tok1 != a.total))
+    return -1;
+  return tok1 - tok0;
+}
+
 // --------------------------------------------------------------------------- 1. preprocess
 // One warp per row: -D = -rowsum(dO * O) in fp32, -LSE in log2 units, dQacc row = 0.
 template <int D>
@@ -142,14 +161,26 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
   if (gw >= rows) return;
   const int bh = static_cast<int>(gw / a.Npad);
   const int r = static_cast<int>(gw % a.Npad);
-  if (r >= a.N) {
+  int len = a.N;
+  int tok0 = 0;
+  if (a.cu_seqlens != nullptr) {
+    len = packed_range(a, bh / a.H, tok0);
+    if (len < 0) {
+      if (r == 0 && lane == 0) atomicOr(a.status, kStatusBadArgBit);
+      len = 0;
+    }
+  }
+  if (r >= len) {
     if (lane == 0) {
       a.Dpad[gw] = 0.f;
       a.Lpad[gw] = -INFINITY;
     }
     return;
   }
-  const size_t row = static_cast<size_t>(bh) * a.N + r;
+  // [B, H, N, D] rows, or [total, H, D] rows when packed (LSE [H, total])
+  const size_t row = a.cu_seqlens != nullptr ? static_cast<size_t>(tok0 + r) * a.H + bh % a.H
+                                             : static_cast<size_t>(bh) * a.N + r;
+  const size_t lrow = a.cu_seqlens != nullptr ? static_cast<size_t>(bh % a.H) * a.total + tok0 + r : row;
   constexpr int kPer = D / 32;  // 2 or 4 elements per lane
   float acc = 0.f;
   if constexpr (kPer == 4) {
@@ -176,7 +207,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
   for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   if (lane == 0) {
     a.Dpad[gw] = -acc;
-    a.Lpad[gw] = -LSE[row] * kLog2e;
+    a.Lpad[gw] = -LSE[lrow] * kLog2e;
   }
 }
 
@@ -193,7 +224,9 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ d
 }
 
 // --------------------------------------------------------------------------- 2. main
-template <int D>
+// kPacked selects the packed ragged-batch layout at compile time, so the dense
+// instantiation carries none of its indexing.
+template <int D, bool kPacked>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -224,12 +257,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (bh >= a.BH) return;
   const int b = bh / a.H;
   const int j = static_cast<int>(blockIdx.x / kHeadGroup);
-  const int N = a.N;
+  const int head = bh % a.H;
+  // N = rows of this batch entry (dense) or sequence (packed); tok0 = its first token
+  int n_rows = a.N, tok0 = 0;
+  if constexpr (kPacked) {
+    n_rows = packed_range(a, b, tok0);
+    if (n_rows < 0 || j * kTile >= n_rows) return;  // bad offsets (reported by the preprocess) or past the end
+  }
+  const int N = n_rows;
   int kv_len = N;
   if (a.kv_lens != nullptr) kv_len = min(max(a.kv_lens[b], 0), N);
   const bool live = j * kTile < kv_len;  // any unmasked key in this tile
   const int i0 = a.causal ? j : 0;
-  const int nt = live ? (a.nq - i0) : 0;  // query tiles to visit
+  const int nq = kPacked ? (N + kTile - 1) / kTile : a.nq;
+  const int nt = live ? (nq - i0) : 0;  // query tiles to visit
+  // TMA coordinates (y, z) of 128 rows from `row`: dense maps are (d, N, B*H)
+  // -> (row, bh), packed maps (d, H, total) -> (head, tok0 + row)
+#define BWD_CRD(row) (kPacked ? head : (row)), (kPacked ? tok0 + (row) : bh)
 
   if (threadIdx.x == 0) {
     mbar_init(bar(BAR_KV), 1);
@@ -272,8 +316,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tmdO);
         mbar_arrive_expect_tx(bar(BAR_KV), 2 * C::kTileBytes);
         for (int s = 0; s < C::kSub; ++s) {
-          tma_load_3d(sbase + C::kOffK + s * C::kSubBytes, &tmK, bar(BAR_KV), s * 64, j * kTile, bh);
-          tma_load_3d(sbase + C::kOffV + s * C::kSubBytes, &tmV, bar(BAR_KV), s * 64, j * kTile, bh);
+          tma_load_3d(sbase + C::kOffK + s * C::kSubBytes, &tmK, bar(BAR_KV), s * 64, BWD_CRD(j * kTile));
+          tma_load_3d(sbase + C::kOffV + s * C::kSubBytes, &tmV, bar(BAR_KV), s * 64, BWD_CRD(j * kTile));
         }
         int side_issued = 0, q_issued = 0, o_issued = 0;
         for (int it = 0; it < nt; ++it) {
@@ -290,14 +334,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(bar(BAR_Q_FULL + sd), C::kTileBytes);
           for (int s = 0; s < C::kSub; ++s)
             tma_load_3d(sbase + C::kOffRing + sd * C::kTileBytes + s * C::kSubBytes, &tmQ, bar(BAR_Q_FULL + sd),
-                        s * 64, i * kTile, bh);
+                        s * 64, BWD_CRD(i * kTile));
           q_issued = it + 1;
           // dO_i into the dO slot (free once dV of tile it-1 is done)
           if (!mbar_wait(bar(BAR_DO_EMPTY), (it & 1) ^ 1, wc)) break;
           mbar_arrive_expect_tx(bar(BAR_DO_FULL), C::kTileBytes);
           for (int s = 0; s < C::kSub; ++s)
             tma_load_3d(sbase + C::kOffRing + 2 * C::kTileBytes + s * C::kSubBytes, &tmdO, bar(BAR_DO_FULL), s * 64,
-                        i * kTile, bh);
+                        BWD_CRD(i * kTile));
           o_issued = it + 1;
         }
         drain_wait(bar(BAR_KV), 0);
@@ -540,7 +584,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         named_barrier_sync(2 + grp, 128);
         if (leader && q0 < N) {
-          tma_reduce_add_3d(&tmdQ, stg, 0, q0, bh);
+          // rows past a packed sequence carry exact zeros (their P is 0)
+          tma_reduce_add_3d(&tmdQ, stg, 0, BWD_CRD(q0));
           bulk_commit();
         }
         continue;  // DQ_READ already signalled
@@ -550,7 +595,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t rr[16];
         tmem_ld16(tmem + lane_off + C::kColDQ + grp * 16, rr);
         if (qrow < N) {
-          float* dst = a.dQacc + (static_cast<size_t>(bh) * N + qrow) * D + grp * 16;
+          const size_t qr = kPacked ? static_cast<size_t>(tok0 + qrow) * a.H + head : static_cast<size_t>(bh) * N + qrow;
+          float* dst = a.dQacc + qr * D + grp * 16;
 #pragma unroll
           for (int c = 0; c < 16; c += 4)
             red_add_v4(dst + c, __uint_as_float(rr[c]), __uint_as_float(rr[c + 1]), __uint_as_float(rr[c + 2]),
@@ -570,7 +616,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         constexpr int kCols = D / 4;
         const bool in_range = key < N;
-        const size_t rowoff = (static_cast<size_t>(bh) * N + key) * D + grp * kCols;
+        const size_t krow = kPacked ? static_cast<size_t>(tok0 + key) * a.H + head : static_cast<size_t>(bh) * N + key;
+        const size_t rowoff = krow * D + grp * kCols;
 #pragma unroll
         for (int which = 0; which < 2; ++which) {
           uint8_t* out = static_cast<uint8_t*>(which ? a.dK : a.dV) + rowoff * 2;
@@ -607,6 +654,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_dealloc(tmem, C::kTmemCols);
   }
 }
+#undef BWD_CRD
 
 template <int D>
 fa_status bwd_launch_d(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
@@ -624,6 +672,8 @@ fa_status bwd_launch_d(const void* Q, const void* K, const void* V, const void* 
   a.dK = dK;
   a.dV = dV;
   a.kv_lens = kv_lens;
+  a.cu_seqlens = nullptr;
+  a.total = 0;
   a.H = H;
   a.BH = BH;
   a.N = N;
@@ -648,8 +698,8 @@ fa_status bwd_launch_d(const void* Q, const void* K, const void* V, const void* 
   if (!encode_f32_tmap(&tdq, a.dQacc, 3, dims, qstrides, qbox)) return FA_ERR_CUDA;
   static bool attr_set = false;
   if (!attr_set) {
-    if (cudaFuncSetAttribute(bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(bwd_main_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::kSmemBytes) != cudaSuccess)
       return FA_ERR_CUDA;
     attr_set = true;
   }
@@ -658,7 +708,7 @@ fa_status bwd_launch_d(const void* Q, const void* K, const void* V, const void* 
       static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), LSE, a, BH);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   const dim3 grid(nq * kHeadGroup, ceil_div(BH, kHeadGroup));
-  bwd_main_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, a);
+  bwd_main_kernel<D, false><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, a);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   const long long n4 = static_cast<long long>(BH) * N * D / 4;
   bwd_dq_kernel<<<static_cast<unsigned>((n4 + 255) / 256), 256, 0, stream>>>(a.dQacc,
@@ -666,7 +716,80 @@ fa_status bwd_launch_d(const void* Q, const void* K, const void* V, const void* 
   return launch_status();
 }
 
+template <int D>
+fa_status bwd_varlen_launch_d(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                              const float* LSE, void* dQ, void* dK, void* dV, const int32_t* cu_seqlens, int num_seqs,
+                              int total, int max_seqlen, int H, int causal, float scale, void* workspace,
+                              cudaStream_t stream) {
+  using C = BwdCfg<D>;
+  const int BH = num_seqs * H;
+  const int nq = ceil_div(max_seqlen, kTile);
+  const int Npad = nq * kTile;
+  const size_t side = (static_cast<size_t>(BH) * Npad * sizeof(float) + 255) & ~static_cast<size_t>(255);
+  BwdArgs a;
+  a.Dpad = static_cast<float*>(workspace);
+  a.Lpad = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + side);
+  a.dQacc = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + 2 * side);
+  a.dK = dK;
+  a.dV = dV;
+  a.kv_lens = nullptr;
+  a.cu_seqlens = cu_seqlens;
+  a.total = total;
+  a.H = H;
+  a.BH = BH;
+  a.N = max_seqlen;
+  a.Npad = Npad;
+  a.nq = nq;
+  a.causal = causal ? 1 : 0;
+  a.scale = scale;
+  a.scale_log2 = scale * kLog2e;
+  a.status = device_status_ptr();
+  if (a.status == nullptr) return FA_ERR_CUDA;
+  // packed [total, H, D]: TMA dims (D, H, total), 128 consecutive tokens of one head
+  const uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(H), static_cast<uint64_t>(total)};
+  const uint64_t strides[2] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(H) * D * 2};
+  const uint32_t box[3] = {64, 1, kTile};
+  CUtensorMap tq, tk, tv, tdo, tdq;
+  if (!encode_bf16_tmap(&tq, Q, 3, dims, strides, box) || !encode_bf16_tmap(&tk, K, 3, dims, strides, box) ||
+      !encode_bf16_tmap(&tv, V, 3, dims, strides, box) || !encode_bf16_tmap(&tdo, dO, 3, dims, strides, box))
+    return FA_ERR_CUDA;
+  const uint64_t qstrides[2] = {static_cast<uint64_t>(D) * 4, static_cast<uint64_t>(H) * D * 4};
+  const uint32_t qbox[3] = {static_cast<uint32_t>(D), 1, 32};
+  if (!encode_f32_tmap(&tdq, a.dQacc, 3, dims, qstrides, qbox)) return FA_ERR_CUDA;
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(bwd_main_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::kSmemBytes) != cudaSuccess)
+      return FA_ERR_CUDA;
+    attr_set = true;
+  }
+  const long long pre_rows = static_cast<long long>(BH) * Npad;
+  bwd_pre_kernel<D><<<static_cast<unsigned>((pre_rows + 7) / 8), 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), LSE, a, BH);
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+  const dim3 grid(nq * kHeadGroup, ceil_div(BH, kHeadGroup));
+  bwd_main_kernel<D, true><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, a);
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+  const long long n4 = static_cast<long long>(total) * H * D / 4;
+  bwd_dq_kernel<<<static_cast<unsigned>((n4 + 255) / 256), 256, 0, stream>>>(a.dQacc,
+                                                                             static_cast<__nv_bfloat16*>(dQ), n4);
+  return launch_status();
+}
+
 }  // namespace
+
+fa_status bwd_varlen_launch(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                            const float* LSE, void* dQ, void* dK, void* dV, const int32_t* cu_seqlens, int num_seqs,
+                            int total, int max_seqlen, int H, int d, int causal, float scale, void* workspace,
+                            cudaStream_t stream) {
+  if (d == 64)
+    return bwd_varlen_launch_d<64>(Q, K, V, O, dO, LSE, dQ, dK, dV, cu_seqlens, num_seqs, total, max_seqlen, H,
+                                   causal, scale, workspace, stream);
+  if (d == 128)
+    return bwd_varlen_launch_d<128>(Q, K, V, O, dO, LSE, dQ, dK, dV, cu_seqlens, num_seqs, total, max_seqlen, H,
+                                    causal, scale, workspace, stream);
+  return FA_ERR_UNSUPPORTED;
+}
 
 fa_status bwd_launch(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
                      void* dQ, void* dK, void* dV, int B, int H, int N, int d, int causal, float scale,

@@ -48,6 +48,10 @@ fa_status fwd_paged_launch(const void* q, const void* k_cache, const void* v_cac
                            const int32_t* cu_seqlens_q, const int32_t* seq_lens_k, void* o, float* lse,
                            int num_seqs, int total_q, int max_seqlen_q, int Hq, int Hkv, int d, int num_blocks,
                            int block_size, int max_blocks, int causal, float scale, cudaStream_t stream);
+fa_status bwd_varlen_launch(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                            const float* LSE, void* dQ, void* dK, void* dV, const int32_t* cu_seqlens, int num_seqs,
+                            int total, int max_seqlen, int H, int d, int causal, float scale, void* workspace,
+                            cudaStream_t stream);
 fa_status bwd_launch(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
                      void* dQ, void* dK, void* dV, int B, int H, int N, int d, int causal, float scale,
                      const int32_t* kv_lens, void* workspace, cudaStream_t stream);

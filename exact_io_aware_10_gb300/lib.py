@@ -33,6 +33,8 @@ SIGNATURES = {
     "fa_fwd_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp, _vp]),
     "fa_fwd_varlen": (_i, [_vp] * 6 + [_i, _i, _i, _i, _i, _i, _f, _vp]),
     "fa_fwd_block_sparse": (_i, [_vp] * 5 + [_i] * 5 + [_f, _vp, _vp, _i, _vp]),
+    "fa_bwd_varlen_workspace_size": (_sz, [_i] * 5),
+    "fa_bwd_varlen": (_i, [_vp] * 10 + [_i] * 6 + [_f, _vp, _sz, _vp]),
     "fa_decode_graph_create": (_i, [_vp, _i] + [_vp] * 7 + [_i] * 8 + [_f, _vp, _sz]),
     "fa_decode_graph_launch": (_i, [_vp, _vp]),
     "fa_decode_graph_kernel_count": (_i, [_vp]),
@@ -190,6 +192,34 @@ def fa_fwd_varlen(Q, K, V, cu_seqlens, max_seqlen, causal=False, scale=None, O=N
                            H, d, int(bool(causal)), scale, _stream(stream))
     _check(st, "fa_fwd_varlen")
     return O, LSE
+
+
+def fa_bwd_varlen(Q, K, V, O, dO, LSE, cu_seqlens, max_seqlen, causal=False, scale=None, dQ=None, dK=None,
+                  dV=None, workspace=None, stream=None):
+    """dQ, dK, dV [total, H, d] for the packed ragged batch of fa_fwd_varlen."""
+    lib = load()
+    total, H, d = Q.shape
+    for t, n in ((Q, "Q"), (K, "K"), (V, "V"), (O, "O"), (dO, "dO")):
+        _need(t, torch.bfloat16, (total, H, d), n)
+    _need(LSE, torch.float32, (H, total), "LSE")
+    _need(cu_seqlens, torch.int32, None, "cu_seqlens")
+    if cu_seqlens.dim() != 1 or cu_seqlens.numel() < 2:
+        raise ValueError("cu_seqlens must be 1-D with num_seqs + 1 >= 2 entries")
+    num_seqs = cu_seqlens.numel() - 1
+    dQ = torch.empty_like(Q) if dQ is None else dQ
+    dK = torch.empty_like(K) if dK is None else dK
+    dV = torch.empty_like(V) if dV is None else dV
+    for t, n in ((dQ, "dQ"), (dK, "dK"), (dV, "dV")):
+        _need(t, torch.bfloat16, (total, H, d), n)
+    ws_bytes = int(lib.fa_bwd_varlen_workspace_size(num_seqs, total, int(max_seqlen), H, d))
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=Q.device)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    st = lib.fa_bwd_varlen(_p(Q), _p(K), _p(V), _p(O), _p(dO), _p(LSE), _p(dQ), _p(dK), _p(dV), _p(cu_seqlens),
+                           num_seqs, total, int(max_seqlen), H, d, int(bool(causal)), scale, _p(workspace),
+                           workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "fa_bwd_varlen")
+    return dQ, dK, dV
 
 
 def fa_bwd_workspace_size(B, H, N, d) -> int:

@@ -186,6 +186,35 @@ int fa_bwd(const void* Q, const void* K, const void* V, const void* O, const voi
            void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * Bytes of device workspace fa_bwd_varlen needs: two fp32 row buffers of
+ * num_sequences x H x Npad (Npad = max_seqlen rounded up to 128) and an fp32
+ * [total, H, d] dQ accumulator, each rounded up to 256 bytes.  0 on invalid sizes.
+ */
+size_t fa_bwd_varlen_workspace_size(int num_seqs, int total, int max_seqlen, int H, int d);
+
+/*
+ * Backward of fa_fwd_varlen (the packed ragged batch): the same gradients as
+ * fa_bwd, computed per sequence.
+ *   Q, K, V, O, dO : [total, H, d] bf16 (O and LSE from fa_fwd_varlen with the
+ *                    same cu_seqlens, causal and scale).
+ *   LSE            : [H, total] fp32.
+ *   dQ, dK, dV     : [total, H, d] bf16, written.
+ *   cu_seqlens     : device int32 [num_seqs + 1]; here it must start at 0 and
+ *                    end at total (every token belongs to a sequence), be
+ *                    non-decreasing, and no sequence may exceed max_seqlen.
+ *                    Offsets breaking this are found on the device:
+ *                    fa_get_device_status() then returns FA_ERR_INVALID_ARG
+ *                    and the gradients are undefined.
+ *   workspace      : at least fa_bwd_varlen_workspace_size() bytes, 256-byte
+ *                    aligned; contents on entry are ignored.
+ * Errors: FA_ERR_INVALID_ARG (including ws_bytes too small), FA_ERR_UNSUPPORTED,
+ * FA_ERR_CUDA.
+ */
+int fa_bwd_varlen(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
+                  void* dQ, void* dK, void* dV, const int32_t* cu_seqlens, int num_seqs, int total, int max_seqlen,
+                  int H, int d, int causal, float scale, void* workspace, size_t ws_bytes, void* stream);
+
+/*
  * Bytes of device workspace fa_paged_decode needs for `num_splits` partial
  * (m, l, o) states per (batch, query head): fp32 o [B, Hq, num_splits, d] and
  * fp32 (m, l) [B, Hq, num_splits, 2], each rounded up to 256 bytes.

@@ -44,7 +44,7 @@ def test_status_strings(so):
                        (4, "FA_ERR_TIMEOUT"), (5, "FA_ERR_BAD_BLOCK_TABLE")]:
         assert so.fa_status_string(code).decode() == name
     assert so.fa_status_string(99).decode() == "FA_ERR_UNKNOWN"
-    assert so.fa_version() == 104
+    assert so.fa_version() == 105
 
 
 def _fake(n=1):
@@ -146,6 +146,27 @@ def test_decode_graph_argument_validation(so):
     assert so.fa_decode_graph_launch(None, None) == fl.FA_ERR_INVALID_ARG
     assert so.fa_decode_graph_kernel_count(None) == 0
     so.fa_decode_graph_destroy(None)  # a no-op
+
+
+def test_varlen_backward_argument_validation(so):
+    p = _fake(11)
+    s = ctypes.c_void_p(0)
+    need = so.fa_bwd_varlen_workspace_size(2, 100, 64, 4, 128)
+    assert need == 2 * (((2 * 4 * 128 * 4) + 255) // 256 * 256) + (100 * 4 * 128 * 4 + 255) // 256 * 256
+    assert so.fa_bwd_varlen_workspace_size(0, 100, 64, 4, 128) == 0
+    f = so.fa_bwd_varlen
+
+    def call(num_seqs=2, total=100, max_seqlen=64, H=4, d=128, scale=0.1, ws=need, cu=p[9]):
+        return f(*p[:9], cu, num_seqs, total, max_seqlen, H, d, 1, scale, p[10], ws, s)
+
+    assert call(d=96) == fl.FA_ERR_UNSUPPORTED
+    assert call(num_seqs=0) == fl.FA_ERR_INVALID_ARG
+    assert call(H=0) == fl.FA_ERR_INVALID_ARG
+    assert call(scale=0.0) == fl.FA_ERR_INVALID_ARG
+    assert call(cu=None) == fl.FA_ERR_INVALID_ARG
+    assert call(ws=need - 1) == fl.FA_ERR_INVALID_ARG
+    assert call(num_seqs=65536) == fl.FA_ERR_UNSUPPORTED
+    assert call(total=0) == fl.FA_OK  # no-op
 
 
 def test_backward_argument_validation(so):

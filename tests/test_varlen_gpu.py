@@ -165,3 +165,82 @@ def test_deterministic(fa):
     a = _run(fa, x, True)
     b = _run(fa, x, True)
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+# ---------------------------------------------------------------- backward
+G_REL = 1e-2  # relative L2 bound on dQ, dK, dV
+
+
+def _bwd(fa, x, causal, max_seqlen=None):
+    dev = torch.device("cuda")
+    Q, K, V, dO, cu = (t.to(dev) for t in (x.Q, x.K, x.V, x.dO, x.cu_seqlens))
+    ms = x.max_seqlen if max_seqlen is None else max_seqlen
+    O, L = fa.fa_fwd_varlen(Q, K, V, cu, ms, causal=causal)
+    grads = fa.fa_bwd_varlen(Q, K, V, O, dO, L, cu, ms, causal=causal)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status() == fa.FA_OK
+    return [g.float().cpu().numpy() for g in grads]
+
+
+def _check_grads(grads, refs, rows=None):
+    for name, g, r in zip(("dQ", "dK", "dV"), grads, refs):
+        if rows is not None:
+            g, r = g[rows], r[rows]
+        assert np.isfinite(g).all(), name
+        assert np.linalg.norm(g - r) <= G_REL * np.linalg.norm(r), (name, np.linalg.norm(g - r) / np.linalg.norm(r))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [64, 128])
+def test_backward_edge_lengths(fa, d, causal):
+    lens = [1, 17, 0, 128, 129, 300, 1000, 256]
+    x = wl.varlen_inputs(lens, 3, d, seed=50 + d)
+    grads = _bwd(fa, x, causal)
+    refs = oracle.attention_backward_varlen(x.Q, x.K, x.V, x.dO, x.cu_seqlens, causal=causal)
+    _check_grads(grads, refs)
+
+
+def test_backward_packed_equals_dense(fa):
+    # equal-length sequences: dK and dV are bit-identical to the dense
+    # backward (same tiles, rows of other sequences contribute exact zeros);
+    # dQ is summed by reductions whose order varies, so it is compared in norm
+    B, H, N, d = 3, 4, 333, 128
+    x = wl.varlen_inputs([N] * B, H, d, seed=61)
+    dev = torch.device("cuda")
+    for causal in (False, True):
+        gv = _bwd(fa, x, causal)
+        dense = [t.reshape(B, N, H, d).permute(0, 2, 1, 3).contiguous().to(dev) for t in (x.Q, x.K, x.V, x.dO)]
+        O, L = fa.fa_fwd(*dense[:3], causal=causal)
+        gd = fa.fa_bwd(*dense[:3], O, dense[3], L, causal=causal)
+        torch.cuda.synchronize()
+        gd = [g.permute(0, 2, 1, 3).reshape(B * N, H, d).float().cpu().numpy() for g in gd]
+        assert np.array_equal(gv[1], gd[1]) and np.array_equal(gv[2], gd[2])
+        assert np.linalg.norm(gv[0] - gd[0]) <= 1e-3 * np.linalg.norm(gd[0])
+
+
+def test_backward_long_mix_two_sequences(fa):
+    # a mix of long sequences; the shortest and the longest are checked in full
+    lens = [512, 4096, 1500, 2900, 700, 3333]
+    H, d = 4, 128
+    x = wl.varlen_inputs(lens, H, d, seed=62)
+    grads = _bwd(fa, x, True)
+    cu = x.cu_seqlens.tolist()
+    for s in (0, 1):
+        a, b = cu[s], cu[s + 1]
+        refs = oracle.attention_backward_varlen(x.Q[a:b], x.K[a:b], x.V[a:b], x.dO[a:b], [0, b - a], causal=True)
+        _check_grads([g[a:b] for g in grads], refs)
+
+
+def test_backward_bad_offsets_are_reported(fa):
+    x = wl.varlen_inputs([100, 50], 2, 64, seed=63)
+    dev = torch.device("cuda")
+    Q, K, V, dO = (t.to(dev) for t in (x.Q, x.K, x.V, x.dO))
+    cu = x.cu_seqlens.to(dev)
+    O, L = fa.fa_fwd_varlen(Q, K, V, cu, 100, causal=True)
+    bad = torch.tensor([0, 100, 140], dtype=torch.int32, device=dev)  # ends before total = 150
+    fa.fa_bwd_varlen(Q, K, V, O, dO, L, bad, 100, causal=True)
+    assert fa.fa_get_device_status() == fa.FA_ERR_INVALID_ARG
+    # the context is still usable
+    grads = _bwd(fa, x, True)
+    refs = oracle.attention_backward_varlen(x.Q, x.K, x.V, x.dO, x.cu_seqlens, causal=True)
+    _check_grads(grads, refs)
