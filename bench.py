@@ -252,6 +252,10 @@ class VarlenWorkload:
         self.O = torch.empty_like(self.Q)
         self.L = torch.empty((c["H"], total), dtype=torch.float32, device=dev)
         self.flops = acc.varlen_fwd_flops(lens, c["H"], c["d"], c["causal"])
+        self.dO = wl.device_normal_bf16(shp, sd + 24, dev)
+        self.dQ, self.dK, self.dV = (torch.empty_like(self.Q) for _ in range(3))
+        self.ws = torch.empty(lib.fa_bwd_varlen_workspace_size(len(lens), total, max(lens), c["H"], c["d"]),
+                              dtype=torch.uint8, device=dev)
         self.padded = None
         if c["padded_N"] is not None:
             B, N = len(lens), c["padded_N"]
@@ -265,6 +269,10 @@ class VarlenWorkload:
         self.lib.fa_fwd_varlen(self.Q, self.K, self.V, self.cu, max(self.lengths), causal=self.c["causal"],
                                O=self.O, LSE=self.L)
 
+    def packed_bwd(self):
+        self.lib.fa_bwd_varlen(self.Q, self.K, self.V, self.O, self.dO, self.L, self.cu, max(self.lengths),
+                               causal=self.c["causal"], dQ=self.dQ, dK=self.dK, dV=self.dV, workspace=self.ws)
+
     def padded_fwd(self):
         self.lib.fa_fwd(*self.padded, causal=self.c["causal"], kv_lens=self.kv, O=self.Op, LSE=self.Lp)
 
@@ -275,7 +283,7 @@ def time_varlen(dev, seed, steps, warmup, barrier, max_over_ranks, world, peak_t
     out = {}
     for name in VARLEN:
         v = VarlenWorkload(dev, name, seed)
-        parts = ("packed",) if v.padded is None else ("packed", "padded_fwd")
+        parts = ("packed", "packed_bwd") if v.padded is None else ("packed", "padded_fwd")
         _, ms = time_parts(lambda p: getattr(v, p)(), parts, steps, warmup, barrier)
         assert v.lib.fa_get_device_status() == v.lib.FA_OK, "device status word reported an error"
         c = v.c
@@ -283,8 +291,9 @@ def time_varlen(dev, seed, steps, warmup, barrier, max_over_ranks, world, peak_t
              "lengths": f"U[{c['lo']},{c['hi']}]", "total_tokens": sum(v.lengths), "flops": v.flops}
         for p in parts:
             t = max_over_ranks(ms[p])
-            tf = world * steps * v.flops / (t * 1e-3) / 1e12
-            key = "packed" if p == "packed" else f"padded_to_{c['padded_N']}"
+            fl = v.flops * (2.5 if p == "packed_bwd" else 1.0)
+            tf = world * steps * fl / (t * 1e-3) / 1e12
+            key = {"packed": "packed", "packed_bwd": "packed_backward"}.get(p, f"padded_to_{c['padded_N']}")
             r[key] = {"TFLOP/s": tf, "frac": tf / world / peak_tf, "frac_of_nominal": tf / world / NOMINAL["bf16_tflops"],
                       "ms": t / steps}
         out[f"varlen_{name}"] = r
