@@ -194,6 +194,10 @@ def fa_fwd_varlen(Q, K, V, cu_seqlens, max_seqlen, causal=False, scale=None, O=N
     return O, LSE
 
 
+def fa_bwd_varlen_workspace_size(num_seqs, total, max_seqlen, H, d) -> int:
+    return int(load().fa_bwd_varlen_workspace_size(int(num_seqs), int(total), int(max_seqlen), int(H), int(d)))
+
+
 def fa_bwd_varlen(Q, K, V, O, dO, LSE, cu_seqlens, max_seqlen, causal=False, scale=None, dQ=None, dK=None,
                   dV=None, workspace=None, stream=None):
     """dQ, dK, dV [total, H, d] for the packed ragged batch of fa_fwd_varlen."""
@@ -211,7 +215,7 @@ def fa_bwd_varlen(Q, K, V, O, dO, LSE, cu_seqlens, max_seqlen, causal=False, sca
     dV = torch.empty_like(V) if dV is None else dV
     for t, n in ((dQ, "dQ"), (dK, "dK"), (dV, "dV")):
         _need(t, torch.bfloat16, (total, H, d), n)
-    ws_bytes = int(lib.fa_bwd_varlen_workspace_size(num_seqs, total, int(max_seqlen), H, d))
+    ws_bytes = fa_bwd_varlen_workspace_size(num_seqs, total, max_seqlen, H, d)
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=Q.device)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)

@@ -208,3 +208,12 @@ def test_selftest_argument_validation(so):
     s = ctypes.c_void_p(0)
     assert so.fa_selftest_wait_timeout(0, s) == fl.FA_ERR_INVALID_ARG
     assert so.fa_selftest_wait_timeout(2000000, s) == fl.FA_ERR_INVALID_ARG
+
+
+def test_binding_has_every_name_the_bench_and_smoke_use():
+    # bench.py and smoke() call the Python binding by attribute; a missing
+    # wrapper would only show up on the GPU machine
+    for path in ("bench.py", "__graft_entry__.py"):
+        src = open(os.path.join(ROOT, path)).read()
+        for name in set(re.findall(r"\blib\.([A-Za-z_][A-Za-z_0-9]*)", src)):
+            assert hasattr(fl, name), (path, name)
