@@ -108,7 +108,8 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
-template <int D>
+// kUnit: block_size == 16, so chunk c is simply block table[c] (no division)
+template <int D, bool kUnit>
 __global__ void __launch_bounds__(kThreads, 3)
     decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                         const DecArgs a) {
@@ -163,11 +164,11 @@ __global__ void __launch_bounds__(kThreads, 3)
         const int st = i % kStages;
         if (!mbar_wait(empty(st), ((i / kStages) & 1) ^ 1, wc)) break;
         const int chunk_key = (lo + i) * kBlk;
-        const int phys = __ldg(table + chunk_key / a.block_size);
+        const int phys = __ldg(table + (kUnit ? lo + i : chunk_key / a.block_size));
         if (phys >= 0 && phys < a.num_blocks) {
           mbar_arrive_expect_tx(full(st), kStageBytes);
           const uint32_t dst = sbase + st * kStageBytes;
-          const int z = phys * a.block_size + chunk_key % a.block_size;
+          const int z = kUnit ? phys * kBlk : phys * a.block_size + chunk_key % a.block_size;
 #pragma unroll
           for (int h = 0; h < C::kHalves; ++h) {
             tma_load_3d(dst + h * kHalfBytes, &tmK, full(st), 64 * h, g, z);
@@ -212,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, 3)
       if (!mbar_wait(full(st), (i / kStages) & 1, wc)) break;
       const uint32_t stK = sbase + st * kStageBytes;
       const uint32_t stV = stK + C::kHalves * kHalfBytes;
-      const int phys = __ldg(table + (lo + i) * kBlk / a.block_size);
+      const int phys = __ldg(table + (kUnit ? lo + i : (lo + i) * kBlk / a.block_size));
       const bool bad = !(phys >= 0 && phys < a.num_blocks);
       // ---- S = Q K^T over 16 keys (two n8 tiles)
       float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -391,9 +392,13 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecArgs a) {
 fa_status decode_prepare() {
   static bool attr_set = false;  // setting it twice is harmless
   if (!attr_set) {
-    if (cudaFuncSetAttribute(decode_split_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(decode_split_kernel<128, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              DecCfg<128>::kSmemBytes) != cudaSuccess ||
-        cudaFuncSetAttribute(decode_split_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(decode_split_kernel<128, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             DecCfg<128>::kSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(decode_split_kernel<64, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             DecCfg<64>::kSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(decode_split_kernel<64, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              DecCfg<64>::kSmemBytes) != cudaSuccess)
       return FA_ERR_CUDA;
     attr_set = true;
@@ -439,7 +444,10 @@ fa_status decode_launch_d(const void* q, const void* k_cache, const void* v_cach
   a.scale_log2 = scale * 1.4426950408889634f;
   a.status = status;
   dim3 grid(num_splits, Hkv, B);
-  decode_split_kernel<D><<<grid, kThreads, DecCfg<D>::kSmemBytes, stream>>>(tk, tv, a);
+  if (block_size == kBlk)
+    decode_split_kernel<D, true><<<grid, kThreads, DecCfg<D>::kSmemBytes, stream>>>(tk, tv, a);
+  else
+    decode_split_kernel<D, false><<<grid, kThreads, DecCfg<D>::kSmemBytes, stream>>>(tk, tv, a);
   if (a.direct) return launch_status();
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   decode_combine_kernel<D><<<ceil_div(static_cast<long long>(B) * Hq, 8), 256, 0, stream>>>(a);
