@@ -3,7 +3,7 @@ profiler:  python -m exact_io_aware_10_gb300.cli fwd --N 16384 --iters 2
 
 Subcommands: fwd (block-sparse with --sparse-window W: butterfly mask plus W
 local key blocks), bwd (runs fwd once to produce O/LSE, then bwd), decode,
-varlen (packed ragged batch of --num-seqs sequences, lengths U[--seq-lo, --seq-hi]),
+varlen / varlen_bwd (packed ragged batch of --num-seqs sequences, lengths U[--seq-lo, --seq-hi]),
 prefill (paged chunked prefill: --num-seqs chunks of --chunk tokens after cached
 prefixes of U[0, --prefix-hi] tokens, --Hq/--Hkv heads, --block-size-token blocks).
 Prints the CUDA-event time of the last iteration.
@@ -24,7 +24,7 @@ from exact_io_aware_10_gb300 import workloads as wl  # noqa: E402
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("op", choices=["fwd", "bwd", "decode", "varlen", "prefill"])
+    ap.add_argument("op", choices=["fwd", "bwd", "decode", "varlen", "varlen_bwd", "prefill"])
     ap.add_argument("--B", type=int, default=1)
     ap.add_argument("--H", type=int, default=16)
     ap.add_argument("--N", type=int, default=16384)
@@ -64,6 +64,23 @@ def main(argv=None):
                 lib.fa_fwd(Q, K, V, causal=causal, O=O, LSE=L)
             else:
                 lib.fa_bwd(Q, K, V, O, dO, L, causal=causal)
+            end.record()
+    elif a.op == "varlen_bwd":
+        lens = wl.varlen_lengths(a.num_seqs, a.seq_lo, a.seq_hi, seed=a.seed)
+        cu = [0]
+        for n in lens:
+            cu.append(cu[-1] + n)
+        shp = (cu[-1], a.H, a.d)
+        Q, K, V, dO = (wl.device_normal_bf16(shp, a.seed + i, dev) for i in range(4))
+        cu = torch.tensor(cu, dtype=torch.int32, device=dev)
+        O, L = lib.fa_fwd_varlen(Q, K, V, cu, max(lens), causal=causal)
+        ws = torch.empty(lib.fa_bwd_varlen_workspace_size(len(lens), shp[0], max(lens), a.H, a.d), dtype=torch.uint8,
+                         device=dev)
+        grads = lib.fa_bwd_varlen(Q, K, V, O, dO, L, cu, max(lens), causal=causal, workspace=ws)
+        for _ in range(a.iters):
+            start.record()
+            lib.fa_bwd_varlen(Q, K, V, O, dO, L, cu, max(lens), causal=causal, dQ=grads[0], dK=grads[1], dV=grads[2],
+                              workspace=ws)
             end.record()
     elif a.op == "varlen":
         lens = wl.varlen_lengths(a.num_seqs, a.seq_lo, a.seq_hi, seed=a.seed)
