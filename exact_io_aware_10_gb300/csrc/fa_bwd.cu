@@ -409,26 +409,33 @@ __global__ void __launch_bounds__(kThreads, 1)
           // dK_j += dS^T Q_i  and  dQ_i over the dP^T columns
           if (!(ok = mbar_wait(bar(BAR_DS), it & 1, wc))) break;
           tc_fence_after();
+          auto issue_dk = [&]() {
 #pragma unroll
-          for (int k = 0; k < kTile / 16; ++k) {
-            const uint32_t aoff = (k >> 2) * C::kSubBytes + (k & 3) * 32;
-            mma_ss(tmem + C::kColDK, sdesc_advance(kP, aoff), sdesc_advance(mq(it), k * 2048), idKN,
-                   (it > 0 || k > 0) ? 1u : 0u);
-          }
+            for (int k = 0; k < kTile / 16; ++k) {
+              const uint32_t aoff = (k >> 2) * C::kSubBytes + (k & 3) * 32;
+              mma_ss(tmem + C::kColDK, sdesc_advance(kP, aoff), sdesc_advance(mq(it), k * 2048), idKN,
+                     (it > 0 || k > 0) ? 1u : 0u);
+            }
+          };
           if constexpr (D == 128) {
+            issue_dk();
             constexpr uint32_t idQT = idesc_bf16_f32(128, 128, true, true);  // A = K^T, B = dS^T
 #pragma unroll
             for (int k = 0; k < kTile / 16; ++k)
               mma_ss(tmem + C::kColDQ, sdesc_advance(mK, k * 2048), sdesc_advance(mP, k * 2048), idQT,
                      k > 0 ? 1u : 0u);
+            mma_commit(bar(BAR_DQ_FULL));
           } else {
+            // d = 64: dQ first, so its vector reductions (no staging in the
+            // dS^T buffer) start while dK runs
             constexpr uint32_t idNN = idesc_bf16_f32(128, D, true, true);  // A = dS, B = K
 #pragma unroll
             for (int k = 0; k < kTile / 16; ++k)
               mma_ss(tmem + C::kColDQ, sdesc_advance(mP, k * 2048), sdesc_advance(mK, k * 2048), idNN,
                      k > 0 ? 1u : 0u);
+            mma_commit(bar(BAR_DQ_FULL));
+            issue_dk();
           }
-          mma_commit(bar(BAR_DQ_FULL));
           mma_commit(bar(BAR_Q_EMPTY + (it & 1)));
           // S_{i+1} = K_j Q_{i+1}^T over the S^T columns (after dV has read P^T).
           // Issued behind dK_i and dQ_i, so dQ_i reaches the compute warps (which
