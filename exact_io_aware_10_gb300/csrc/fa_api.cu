@@ -8,6 +8,8 @@
 #include <cudaTypedefs.h>
 
 #include <mutex>
+#include <utility>
+#include <vector>
 
 #include "fa_internal.h"
 #include "sm103.cuh"
@@ -57,6 +59,19 @@ bool encode_f32_tmap(CUtensorMap* map, const void* base, int rank, const uint64_
                      const uint64_t* strides_bytes, const uint32_t* box) {
   return encode_tmap(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, CU_TENSOR_MAP_SWIZZLE_NONE, base, rank, dims,
                      strides_bytes, box);
+}
+
+bool set_smem_limit(const void* func, int bytes) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  static std::mutex mu;
+  static std::vector<std::pair<const void*, int>> done;  // (kernel, device) pairs already raised
+  std::lock_guard<std::mutex> lk(mu);
+  for (const auto& e : done)
+    if (e.first == func && e.second == dev) return true;
+  if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) return false;
+  done.emplace_back(func, dev);
+  return true;
 }
 
 bool encode_init() {

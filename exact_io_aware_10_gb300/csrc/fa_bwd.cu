@@ -703,13 +703,8 @@ fa_status bwd_launch_d(const void* Q, const void* K, const void* V, const void* 
   const uint64_t qstrides[2] = {static_cast<uint64_t>(D) * 4, static_cast<uint64_t>(N) * D * 4};
   const uint32_t qbox[3] = {static_cast<uint32_t>(D), 32, 1};
   if (!encode_f32_tmap(&tdq, a.dQacc, 3, dims, qstrides, qbox)) return FA_ERR_CUDA;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(bwd_main_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::kSmemBytes) != cudaSuccess)
-      return FA_ERR_CUDA;
-    attr_set = true;
-  }
+  if (!set_smem_limit(reinterpret_cast<const void*>(&bwd_main_kernel<D, false>), C::kSmemBytes))
+    return FA_ERR_CUDA;
   const long long pre_rows = static_cast<long long>(BH) * Npad;
   bwd_pre_kernel<D><<<static_cast<unsigned>((pre_rows + 7) / 8), 256, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), LSE, a, BH);
@@ -763,13 +758,8 @@ fa_status bwd_varlen_launch_d(const void* Q, const void* K, const void* V, const
   const uint64_t qstrides[2] = {static_cast<uint64_t>(D) * 4, static_cast<uint64_t>(H) * D * 4};
   const uint32_t qbox[3] = {static_cast<uint32_t>(D), 1, 32};
   if (!encode_f32_tmap(&tdq, a.dQacc, 3, dims, qstrides, qbox)) return FA_ERR_CUDA;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(bwd_main_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::kSmemBytes) != cudaSuccess)
-      return FA_ERR_CUDA;
-    attr_set = true;
-  }
+  if (!set_smem_limit(reinterpret_cast<const void*>(&bwd_main_kernel<D, true>), C::kSmemBytes))
+    return FA_ERR_CUDA;
   const long long pre_rows = static_cast<long long>(BH) * Npad;
   bwd_pre_kernel<D><<<static_cast<unsigned>((pre_rows + 7) / 8), 256, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), LSE, a, BH);

@@ -390,20 +390,12 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecArgs a) {
 }  // namespace
 
 fa_status decode_prepare() {
-  static bool attr_set = false;  // setting it twice is harmless
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(decode_split_kernel<128, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             DecCfg<128>::kSmemBytes) != cudaSuccess ||
-        cudaFuncSetAttribute(decode_split_kernel<128, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             DecCfg<128>::kSmemBytes) != cudaSuccess ||
-        cudaFuncSetAttribute(decode_split_kernel<64, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             DecCfg<64>::kSmemBytes) != cudaSuccess ||
-        cudaFuncSetAttribute(decode_split_kernel<64, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             DecCfg<64>::kSmemBytes) != cudaSuccess)
-      return FA_ERR_CUDA;
-    attr_set = true;
-  }
-  return FA_OK;
+  auto raise = [](const void* f, int bytes) { return set_smem_limit(f, bytes); };
+  const bool ok = raise(reinterpret_cast<const void*>(&decode_split_kernel<128, true>), DecCfg<128>::kSmemBytes) &&
+                  raise(reinterpret_cast<const void*>(&decode_split_kernel<128, false>), DecCfg<128>::kSmemBytes) &&
+                  raise(reinterpret_cast<const void*>(&decode_split_kernel<64, true>), DecCfg<64>::kSmemBytes) &&
+                  raise(reinterpret_cast<const void*>(&decode_split_kernel<64, false>), DecCfg<64>::kSmemBytes);
+  return ok ? FA_OK : FA_ERR_CUDA;
 }
 
 namespace {

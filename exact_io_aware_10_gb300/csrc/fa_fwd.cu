@@ -599,12 +599,7 @@ fa_status fwd_launch_d(const void* Q, const void* K, const void* V, void* O, flo
   if (!encode_bf16_tmap(&tq, Q, 3, dims, strides, box) || !encode_bf16_tmap(&tk, K, 3, dims, strides, box) ||
       !encode_bf16_tmap(&tv, V, 3, dims, strides, box))
     return FA_ERR_CUDA;
-  static bool attr_set = false;  // per template instance; setting it twice is harmless
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
-      return FA_ERR_CUDA;
-    attr_set = true;
-  }
+  if (!set_smem_limit(reinterpret_cast<const void*>(&fwd_kernel<D>), C::kSmemBytes)) return FA_ERR_CUDA;
   unsigned* status = device_status_ptr();
   if (status == nullptr) return FA_ERR_CUDA;
   FwdArgs a{};  // zero: no paged K/V
@@ -639,12 +634,7 @@ fa_status fwd_varlen_launch_d(const void* Q, const void* K, const void* V, void*
   if (!encode_bf16_tmap(&tq, Q, 3, dims, strides, box) || !encode_bf16_tmap(&tk, K, 3, dims, strides, box) ||
       !encode_bf16_tmap(&tv, V, 3, dims, strides, box))
     return FA_ERR_CUDA;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
-      return FA_ERR_CUDA;
-    attr_set = true;
-  }
+  if (!set_smem_limit(reinterpret_cast<const void*>(&fwd_kernel<D>), C::kSmemBytes)) return FA_ERR_CUDA;
   unsigned* status = device_status_ptr();
   if (status == nullptr) return FA_ERR_CUDA;
   FwdArgs a{};  // zero: no paged K/V
@@ -684,12 +674,7 @@ fa_status fwd_paged_launch_d(const void* q, const void* k_cache, const void* v_c
   if (!encode_bf16_tmap(&tq, q, 3, qdims, qstrides, qbox) || !encode_bf16_tmap(&tk, k_cache, 3, kdims, kstrides, kbox) ||
       !encode_bf16_tmap(&tv, v_cache, 3, kdims, kstrides, kbox))
     return FA_ERR_CUDA;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
-      return FA_ERR_CUDA;
-    attr_set = true;
-  }
+  if (!set_smem_limit(reinterpret_cast<const void*>(&fwd_kernel<D>), C::kSmemBytes)) return FA_ERR_CUDA;
   unsigned* status = device_status_ptr();
   if (status == nullptr) return FA_ERR_CUDA;
   FwdArgs a{};

@@ -55,9 +55,12 @@ fa_status bwd_varlen_launch(const void* Q, const void* K, const void* V, const v
 fa_status bwd_launch(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
                      void* dQ, void* dK, void* dV, int B, int H, int N, int d, int causal, float scale,
                      const int32_t* kv_lens, void* workspace, cudaStream_t stream);
-// One-time host setup of the decode kernels (shared-memory attribute), done
-// outside any stream capture by the graph builder.
+// Host setup of the decode kernels on the current device (shared-memory limit),
+// done once per device; the graph builder calls it outside any stream capture.
 fa_status decode_prepare();
+// Raises `func`'s dynamic shared-memory limit to `bytes` on the current device,
+// once per (kernel, device); false on failure.
+bool set_smem_limit(const void* func, int bytes);
 // Loads the tensor-map encoder entry point if needed; false if unavailable.
 bool encode_init();
 fa_status decode_launch(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
