@@ -6,7 +6,8 @@ local key blocks), bwd (runs fwd once to produce O/LSE, then bwd), decode,
 varlen / varlen_bwd (packed ragged batch of --num-seqs sequences, lengths U[--seq-lo, --seq-hi]),
 prefill (paged chunked prefill: --num-seqs chunks of --chunk tokens after cached
 prefixes of U[0, --prefix-hi] tokens, --Hq/--Hkv heads, --block-size-token blocks).
-Prints the CUDA-event time of the last iteration.
+Prints the CUDA-event times of the last iteration and the median and minimum
+over all --iters iterations.
 """
 from __future__ import annotations
 
@@ -20,6 +21,18 @@ sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
 
 from exact_io_aware_10_gb300 import lib  # noqa: E402
 from exact_io_aware_10_gb300 import workloads as wl  # noqa: E402
+
+
+class _Marks:
+    """CUDA events recorded on the current stream, one per record() call."""
+
+    def __init__(self):
+        self.events = []
+
+    def record(self):
+        e = torch.cuda.Event(enable_timing=True)
+        e.record()
+        self.events.append(e)
 
 
 def main(argv=None):
@@ -48,7 +61,7 @@ def main(argv=None):
     dev = torch.device("cuda")
     lib.load()
     causal = not a.noncausal
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start, end = _Marks(), _Marks()
     if a.op in ("fwd", "bwd"):
         shp = (a.B, a.H, a.N, a.d)
         Q, K, V, dO = (wl.device_normal_bf16(shp, a.seed + i, dev) for i in range(4))
@@ -123,7 +136,10 @@ def main(argv=None):
             end.record()
     torch.cuda.synchronize()
     st = lib.fa_get_device_status()
-    print(f"{a.op}: {start.elapsed_time(end):.3f} ms (last iteration), status {lib.status_string(st)}")
+    times = sorted(s.elapsed_time(e) for s, e in zip(start.events, end.events))
+    last = start.events[-1].elapsed_time(end.events[-1])
+    print(f"{a.op}: {last:.3f} ms (last iteration), median {times[len(times) // 2]:.3f} ms, min {times[0]:.3f} ms "
+          f"over {len(times)}, status {lib.status_string(st)}")
     return 0 if st == lib.FA_OK else 1
 
 
