@@ -38,8 +38,8 @@ namespace fa {
 namespace {
 
 constexpr int kThreads = 384;
-constexpr uint32_t kRegsSoftmax = 216;  // 2 x 128 x 216 + 128 x 72 = 384 x 168 (the launch pool)
-constexpr uint32_t kRegsOther = 72;
+constexpr uint32_t kRegsSoftmax = 200;  // 2 x 128 x 200 + 128 x 96 = 63488 <= 384 x 168 (the launch pool)
+constexpr uint32_t kRegsOther = 96;
 constexpr int kRows = 128;   // query rows per tile = TMEM lanes
 constexpr int kKeys = 128;   // keys per K/V tile
 constexpr float kRescaleLog2 = 8.0f;
