@@ -116,6 +116,11 @@ __global__ void __launch_bounds__(kThreads, 3)
   using C = DecCfg<D>;
   constexpr int kOffBar = C::kOffBar;
   constexpr int kStageBytes = C::kStageBytes;
+  // launched as a programmatic dependent: the CTAs may be resident before the
+  // previous kernel in the stream has finished, so nothing it may write is
+  // read before griddep_wait(); the combine kernel may then be scheduled
+  griddep_wait();
+  griddep_launch_dependents();
   const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   // the work is cut into 16-token chunks; chunk c lives in cache block
   // table[c * 16 / block_size] at row (c * 16) % block_size
@@ -338,6 +343,8 @@ __global__ void __launch_bounds__(kThreads, 3)
 template <int D>
 __global__ void __launch_bounds__(256) decode_combine_kernel(const DecArgs a) {
   constexpr int kPer = D / 32;
+  griddep_wait();  // the split kernel's partial states are complete and visible
+  griddep_launch_dependents();
   const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (gw >= a.B * a.Hq) return;
@@ -435,14 +442,33 @@ fa_status decode_launch_d(const void* q, const void* k_cache, const void* v_cach
   a.min_blocks = (static_cast<long long>(B) * Hkv >= kFewUnits) ? kMinBlocksPerSplit : kMinBlocksPerSplitFew;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.status = status;
-  dim3 grid(num_splits, Hkv, B);
-  if (block_size == kBlk)
-    decode_split_kernel<D, true><<<grid, kThreads, DecCfg<D>::kSmemBytes, stream>>>(tk, tv, a);
-  else
-    decode_split_kernel<D, false><<<grid, kThreads, DecCfg<D>::kSmemBytes, stream>>>(tk, tv, a);
+  // Both kernels are programmatic dependents of whatever precedes them in the
+  // stream: their launch and start-up overlap the previous kernel's tail (a
+  // decode step is a chain of short kernels, one pair per layer).
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_splits, Hkv, B);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = DecCfg<D>::kSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = pdl;
+  cfg.numAttrs = 1;
+  cudaError_t e = (block_size == kBlk) ? cudaLaunchKernelEx(&cfg, decode_split_kernel<D, true>, tk, tv, a)
+                                       : cudaLaunchKernelEx(&cfg, decode_split_kernel<D, false>, tk, tv, a);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_CUDA;
+  }
   if (a.direct) return launch_status();
-  if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
-  decode_combine_kernel<D><<<ceil_div(static_cast<long long>(B) * Hq, 8), 256, 0, stream>>>(a);
+  cfg.gridDim = dim3(ceil_div(static_cast<long long>(B) * Hq, 8));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  if (cudaLaunchKernelEx(&cfg, decode_combine_kernel<D>, a) != cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_CUDA;
+  }
   return launch_status();
 }
 }  // namespace

@@ -88,6 +88,17 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, WaitCtx
   return mbar_wait_slow(bar, parity, ctx);
 }
 
+// ------------------------------------------------------------------ programmatic dependent launch
+// For kernels launched with the programmatic stream serialization attribute:
+// griddep_wait() returns once the grids this one depends on have completed
+// and their memory operations are visible; griddep_launch_dependents() lets
+// the next grid in the stream be scheduled (it still waits for this grid's
+// completion before touching memory, through its own griddep_wait()).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");

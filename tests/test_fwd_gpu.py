@@ -126,3 +126,18 @@ def test_long_context_sampled_rows(fa, N):
     Oref, Lref = oracle.attention_forward_rows(x.Q, x.K, x.V, rows, causal=True, heads=heads)
     for t, (b, h) in enumerate(heads):
         _check(O[b, h][rows], L[b, h][rows], Oref[t], Lref[t])
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_longest_sequence_sampled_rows(fa, causal):
+    """The largest single-sequence case the suite runs: N = 262144 (N^2 > 2^31,
+    2048 query tiles per head), checked on rows sampled across the whole
+    sequence, the first and last tiles and a tile boundary."""
+    B, H, N, d = 1, 2, 262144, 128
+    x = wl.dense_inputs(B, H, N, d, seed=wl.config_seed(0, 4) + 7)
+    O, L = _run(fa, x, causal)
+    rows = np.unique(np.concatenate([np.arange(0, N, 8191), [0, 127, 128, N - 129, N - 128, N - 1]]))
+    heads = [(0, 0), (0, H - 1)]
+    Oref, Lref = oracle.attention_forward_rows(x.Q, x.K, x.V, rows, causal=causal, heads=heads)
+    for t, (b, h) in enumerate(heads):
+        _check(O[b, h][rows], L[b, h][rows], Oref[t], Lref[t])
