@@ -45,8 +45,8 @@ namespace fa {
 namespace {
 
 constexpr int kThreads = 640;
-constexpr uint32_t kRegsCompute = 104;  // 4 x 128 x 104 + 128 x 64 = 640 x 96 (the launch pool)
-constexpr uint32_t kRegsOther = 64;
+constexpr uint32_t kRegsCompute = 96;  // 4 x 128 x 96 + 128 x 96 = 640 x 96 (the launch pool)
+constexpr uint32_t kRegsOther = 96;
 constexpr int kTile = 128;  // keys per CTA and queries per step
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -418,13 +418,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           };
           if constexpr (D == 128) {
-            issue_dk();
+            // dQ_i first: it is the only reader of the shared-memory dS^T, so
+            // DQ_FULL also frees that buffer for dQ staging; then dK_i with
+            // A = dS^T from TMEM (packed bf16 next to P^T, as for dV)
             constexpr uint32_t idQT = idesc_bf16_f32(128, 128, true, true);  // A = K^T, B = dS^T
 #pragma unroll
             for (int k = 0; k < kTile / 16; ++k)
               mma_ss(tmem + C::kColDQ, sdesc_advance(mK, k * 2048), sdesc_advance(mP, k * 2048), idQT,
                      k > 0 ? 1u : 0u);
             mma_commit(bar(BAR_DQ_FULL));
+#pragma unroll
+            for (int k = 0; k < kTile / 16; ++k) {
+              const uint32_t acol = 32 * (k >> 1) + 16 + 8 * (k & 1);
+              mma_ts(tmem + C::kColDK, tmem + C::kColS + acol, sdesc_advance(mq(it), k * 2048), idKN,
+                     (it > 0 || k > 0) ? 1u : 0u);
+            }
           } else {
             // d = 64: dQ first, so its vector reductions (no staging in the
             // dS^T buffer) start while dK runs
@@ -555,14 +563,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           named_barrier_sync(1, 32 * kComputeWarps);
         }
       }
+      // d = 128: dS^T also goes to TMEM, next to P^T (columns 32 grp + 16 ..):
+      // dK_i reads it from there, so only dQ_i reads the shared-memory copy
 #pragma unroll
-      for (int c8 = 0; c8 < 4; ++c8) {
-        const int chunk = 4 * (grp & 1) + c8;
-        st_shared_v4(dsrow + (((chunk ^ swz)) << 4), pack_bf16x2(p[8 * c8 + 0], p[8 * c8 + 1]),
-                     pack_bf16x2(p[8 * c8 + 2], p[8 * c8 + 3]), pack_bf16x2(p[8 * c8 + 4], p[8 * c8 + 5]),
-                     pack_bf16x2(p[8 * c8 + 6], p[8 * c8 + 7]));
+      for (int h = 0; h < 2; ++h) {
+        uint32_t pk[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) pk[c] = pack_bf16x2(p[16 * h + 2 * c], p[16 * h + 2 * c + 1]);
+        if constexpr (D == 128) tmem_st8(tmem + lane_off + C::kColS + grp * 32 + 16 + 8 * h, pk);
+#pragma unroll
+        for (int c8 = 0; c8 < 2; ++c8) {
+          const int chunk = 4 * (grp & 1) + 2 * h + c8;
+          st_shared_v4(dsrow + (((chunk ^ swz)) << 4), pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
+        }
       }
+      if constexpr (D == 128) tmem_st_wait();
       fence_proxy_async_smem();
+      if constexpr (D == 128) tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(BAR_DS));
       // ---- dQ_i += this tile's contribution
