@@ -32,7 +32,8 @@
 // Roles of the main kernel (20 warps = 5 warpgroups): warps 0-15 compute
 // (thread = key row of S^T / dP^T / dK / dV; warpgroup h takes query columns
 // 32h..32h+31 and head-dim columns h*d/4.. of dK/dV), warp 16 loads (TMA),
-// warp 17 issues the MMAs, warps 18-19 idle; the fifth warpgroup hands
+// warp 17 issues the MMAs, warp 18 (d = 128) folds the next query tile's load
+// into the dS barrier (Q watcher), warp 19 idle; the fifth warpgroup hands
 // registers to the compute warps.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -96,6 +97,10 @@ enum : int {
 constexpr int kOffTmemSlot = kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 4;
 constexpr int kComputeWarps = 16;
+// d = 128: warp 18 folds the wait for the next query tile into the dS barrier
+// (measured: 2 % faster at d = 128, 2 % slower at d = 64)
+template <int D>
+constexpr bool kQWatch = (D == 128);
 constexpr int kHeadGroup = 4;  // heads whose CTAs are interleaved in the grid
 
 struct BwdArgs {
@@ -288,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(BAR_S), 1);
     mbar_init(bar(BAR_P), kComputeWarps);
     mbar_init(bar(BAR_DP), 1);
-    mbar_init(bar(BAR_DS), kComputeWarps);
+    mbar_init(bar(BAR_DS), kComputeWarps + (kQWatch<D> ? 1 : 0));  // + the Q watcher (d = 128)
     mbar_init(bar(BAR_DQ_FULL), 1);
     mbar_init(bar(BAR_DQ_READ), kComputeWarps);
     mbar_init(bar(BAR_FINAL), 1);
@@ -449,8 +454,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           // Issued behind dK_i and dQ_i, so dQ_i reaches the compute warps (which
           // read it out next) without waiting for S_{i+1}.
           if (next) {
-            if (!(ok = mbar_wait(bar(BAR_Q_FULL + ((it + 1) & 1)), ((it + 1) >> 1) & 1, wc))) break;
-            tc_fence_after();
+            // d = 128: Q_i+1 has landed, the DS(i) barrier waited for above
+            // completes only after the Q watcher has seen it
+            if (!kQWatch<D> &&
+                !(ok = mbar_wait(bar(BAR_Q_FULL + ((it + 1) & 1)), ((it + 1) >> 1) & 1, wc)))
+              break;
+            if (!kQWatch<D>) tc_fence_after();
             mma_kmajor_d(C::kColS, kK, kq(it + 1));
             mma_commit(bar(BAR_S));
           }
@@ -466,6 +475,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) mma_commit(bar(BAR_FINAL));
         mma_commit(bar(BAR_DRAIN));
         drain_wait(bar(BAR_DRAIN), 0);
+      }
+    } else if (kQWatch<D> && warp == kComputeWarps + 2) {
+      // ---------------------------------------------------------- Q watcher
+      // Adds one arrival to DS(i), after Q_i+1 has landed, so the issuing
+      // thread's wait for dS_i also covers the next query tile (one barrier
+      // wait fewer per tile on the issuing thread).  It arrives for tile i only
+      // once DS(i - 1) has completed, so it never arrives twice in one phase.
+      if (lane == 0) {
+        for (int it = 0; it < nt; ++it) {
+          if (it > 0 && !mbar_wait(bar(BAR_DS), static_cast<uint32_t>(it - 1) & 1u, wc)) break;
+          if (it + 1 < nt &&
+              !mbar_wait(bar(BAR_Q_FULL + ((it + 1) & 1)), static_cast<uint32_t>((it + 1) >> 1) & 1u, wc))
+            break;
+          mbar_arrive(bar(BAR_DS));
+        }
       }
     }
   } else {
