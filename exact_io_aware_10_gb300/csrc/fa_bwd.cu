@@ -1,6 +1,6 @@
 // Backward attention by recomputation on sm_103a ("精读笔记 08：FlashAttention"
 // §3.3: keep O and the row statistics, rebuild the score tiles on chip; the
-// IO-explained page: "more FLOPs, fewer HBM accesses").  With P recomputed as
+// IO-explained page: recomputation trades extra FLOPs for fewer HBM accesses).  With P recomputed as
 // P = exp(scale Q K^T - LSE), the gradients of sum(dO * O) are
 //     dV = P^T dO,  dP = dO V^T,  D = rowsum(dO * O),  dS = P * (dP - D),
 //     dK = scale dS^T Q,  dQ = scale dS K.
@@ -17,12 +17,15 @@
 //                        S^T  = K_j Q_i^T          (TMEM cols   0..127)
 //                        dP^T = V_j dO_i^T         (TMEM cols 128..255)
 //                        dV_j += P^T dO_i          (A = P^T, bf16 in TMEM over S^T)
-//                        dK_j += dS^T Q_i          (A = dS^T from shared memory)
+//                        dK_j += dS^T Q_i          (A = dS^T: d = 128 bf16 in TMEM next
+//                                                   to P^T, d = 64 from shared memory)
 //                        dQ_i^T = K_j^T dS^T       (d = 128: lanes = head dim, over dP^T)
 //                        dQ_i   = dS K_j           (d = 64: lanes = queries, over dP^T)
-//                      MMA order per tile: dV_i, dK_i, dQ_i, S_{i+1}, dP_{i+1}:
-//                      dQ_i is ready for read-out as soon as dS_i is, and the
-//                      next tile's scores run while dQ_i is staged.
+//                      MMA order per tile: dV_i, dQ_i, dK_i, S_{i+1}, dP_{i+1}:
+//                      dQ_i is read out as soon as it is done (at d = 128 it is
+//                      the only reader of the shared-memory dS^T, so its
+//                      completion also frees that buffer for dQ staging), and
+//                      the next tile's scores run while dQ_i is staged.
 //                      dQ_i is added into the fp32 accumulator in L2: at
 //                      d = 128 by one TMA bulk reduction of a 128 x 32 box per
 //                      compute warpgroup, staged in shared memory, at d = 64 by

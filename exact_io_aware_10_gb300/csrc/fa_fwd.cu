@@ -28,7 +28,8 @@
 // than kRescaleLog2 moves the reference and rescales O (in TMEM) and l by
 // alpha = 2^(m_ref_old - m_ref_new).  Otherwise p = 2^(x - m_ref) <= 2^8 and
 // nothing is rescaled.  O and l share the reference, so O / l is exact
-// (S12: "one multiplication fixes everything accumulated so far").
+// (the S12 page's point: a single multiplication corrects all that has been
+// accumulated before the maximum moved).
 // A row whose running max is still -inf subtracts 0 instead of -inf, which
 // avoids exp(-inf - -inf) = NaN on fully masked tiles (S12 warning).
 #include <cuda.h>
