@@ -73,7 +73,7 @@ NOMINAL = {"bf16_tflops": 2250.0, "hbm_gbs": 8000.0}
 # ncu dram bytes (read + write) per launch of the dominant kernel, with the
 # hash of the kernel source they were taken on (null once the source changes)
 TRAFFIC_RECORD = {"kernel": "fwd_kernel<128>", "source": "exact_io_aware_10_gb300/csrc/fa_fwd.cu",
-                  "sha256": "b1add5fa20075b39d21642a48c996ef54ba14dca2c0397d4923c9654c93565fd",
+                  "sha256": "d050d5d829ff731c2cbd0c91aead004c19d72584a81e87e77242829965ede001",
                   "bytes_per_launch_N16384": 544236032 + 46380032,
                   "bytes_per_launch_N65536": 7733645056 + 253309184}
 
