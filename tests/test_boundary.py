@@ -217,3 +217,20 @@ def test_binding_has_every_name_the_bench_and_smoke_use():
         src = open(os.path.join(ROOT, path)).read()
         for name in set(re.findall(r"\blib\.([A-Za-z_][A-Za-z_0-9]*)", src)):
             assert hasattr(fl, name), (path, name)
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    # no fallback: without the built library the binding raises instead of computing
+    monkeypatch.setattr(fl, "_LIB", None)
+    monkeypatch.setattr(fl, "library_path", lambda: str(tmp_path / "libfa_gb300.so"))
+    with pytest.raises(FileNotFoundError):
+        fl.load()
+
+
+def test_host_tensors_are_refused(so):
+    # the binding takes device tensors only: host tensors raise before any call
+    import torch
+
+    x = torch.zeros(1, 1, 16, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        fl.fa_fwd(x, x, x)
