@@ -61,6 +61,12 @@ bool encode_f32_tmap(CUtensorMap* map, const void* base, int rank, const uint64_
                      strides_bytes, box);
 }
 
+bool encode_f32_sw128_tmap(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                           const uint64_t* strides_bytes, const uint32_t* box) {
+  return encode_tmap(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, CU_TENSOR_MAP_SWIZZLE_128B, base, rank, dims,
+                     strides_bytes, box);
+}
+
 bool set_smem_limit(const void* func, int bytes) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;

@@ -26,10 +26,10 @@
 //                      the only reader of the shared-memory dS^T, so its
 //                      completion also frees that buffer for dQ staging), and
 //                      the next tile's scores run while dQ_i is staged.
-//                      dQ_i is added into the fp32 accumulator in L2: at
-//                      d = 128 by one TMA bulk reduction of a 128 x 32 box per
-//                      compute warpgroup, staged in shared memory, at d = 64 by
-//                      vector reductions.
+//                      dQ_i is added into the fp32 accumulator in L2 by TMA
+//                      bulk reductions of boxes staged in shared memory: at
+//                      d = 128 one 128 x 32 box per compute warpgroup, at
+//                      d = 64 two swizzled 32 x 32 boxes per TMEM lane quarter.
 //  3. bwd_dq_kernel    dQ = bf16(dQacc).
 //
 // Roles of the main kernel (20 warps = 5 warpgroups): warps 0-15 compute
@@ -65,11 +65,12 @@ struct BwdCfg {
   static constexpr int kOffV = kOffK + kTileBytes;
   static constexpr int kOffP = kOffV + kTileBytes;  // dS^T (bf16, 128 x 128)
   static constexpr int kOffRing = kOffP + kPBytes;  // Q slots 0-1, then the dO slot
-  // dQ staging for the TMA reductions, 16 KB (32 queries x 128 fp32) per compute
-  // warpgroup: warpgroups 0-1 here, 2-3 in the dS^T buffer (idle while dQ is
-  // read out)
+  // dQ staging for the TMA reductions.  d = 128: 16 KB (32 queries x 128 fp32)
+  // per compute warpgroup, warpgroups 0-1 here, 2-3 in the dS^T buffer (idle
+  // while dQ is read out).  d = 64: 8 KB (32 queries x 64 fp32) per TMEM lane
+  // quarter, as two 128-byte-swizzled halves of 32 columns.
   static constexpr int kOffStage = kOffRing + kSlots * kTileBytes;
-  static constexpr int kStageBytes = (D == 128) ? 2 * 16384 : 0;
+  static constexpr int kStageBytes = (D == 128) ? 2 * 16384 : 4 * 8192;
   static constexpr int kOffSide = kOffStage + kStageBytes;  // 2 x (-LSE2[128], -D[128])
   static constexpr int kOffBar = kOffSide + 2 * 1024;
   static constexpr int kUsedBytes = kOffBar + 256;
@@ -136,11 +137,6 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
-               : "memory");
-}
-
-__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
                : "memory");
 }
 
@@ -641,18 +637,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         continue;  // DQ_READ already signalled
       } else {
-        // dQ: lane = query row r, columns = this warpgroup's 16 head-dim entries
-        const int qrow = i * kTile + r;
+        // dQ: lane = query row r, columns = this warpgroup's 16 head-dim
+        // entries.  The four warps of one TMEM lane quarter (q4, one per
+        // warpgroup) stage their 32 queries x 64 fp32 in shared memory, two
+        // 128-byte-swizzled halves of 32 columns (conflict-free 16-byte
+        // stores), and one of them adds the box into dQacc with two TMA
+        // reductions in L2.
         uint32_t rr[16];
         tmem_ld16(tmem + lane_off + C::kColDQ + grp * 16, rr);
-        if (qrow < N) {
-          const size_t qr = kPacked ? static_cast<size_t>(tok0 + qrow) * a.H + head : static_cast<size_t>(bh) * N + qrow;
-          float* dst = a.dQacc + qr * D + grp * 16;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(BAR_DQ_READ));
+        const uint32_t stg = sbase + C::kOffStage + q4 * 8192;
+        const bool leader = (grp == 0 && lane == 0);
+        if (it > 0 && leader) bulk_wait_read_all();  // this staging box's previous reductions
+        named_barrier_sync(2 + q4, 128);
+        const uint32_t srow = stg + (grp >> 1) * 4096 + lane * 128;
 #pragma unroll
-          for (int c = 0; c < 16; c += 4)
-            red_add_v4(dst + c, __uint_as_float(rr[c]), __uint_as_float(rr[c + 1]), __uint_as_float(rr[c + 2]),
-                       __uint_as_float(rr[c + 3]));
+        for (int c = 0; c < 4; ++c)
+          st_shared_v4(srow + ((((grp & 1) * 4 + c) ^ (lane & 7)) << 4), rr[4 * c], rr[4 * c + 1], rr[4 * c + 2],
+                       rr[4 * c + 3]);
+        fence_proxy_async_smem();
+        named_barrier_sync(2 + q4, 128);
+        const int q0 = i * kTile + q4 * 32;
+        if (leader && q0 < N) {
+          // rows past a packed sequence carry exact zeros (their P is 0)
+          tma_reduce_add_3d(&tmdQ, stg, 0, BWD_CRD(q0));
+          tma_reduce_add_3d(&tmdQ, stg + 4096, 32, BWD_CRD(q0));
+          bulk_commit();
         }
+        continue;  // DQ_READ already signalled
       }
       tc_fence_before();
       __syncwarp();
@@ -743,10 +757,13 @@ fa_status bwd_launch_d(const void* Q, const void* K, const void* V, const void* 
   if (!encode_bf16_tmap(&tq, Q, 3, dims, strides, box) || !encode_bf16_tmap(&tk, K, 3, dims, strides, box) ||
       !encode_bf16_tmap(&tv, V, 3, dims, strides, box) || !encode_bf16_tmap(&tdo, dO, 3, dims, strides, box))
     return FA_ERR_CUDA;
-  // fp32 dQ accumulator as D (head dim) x 32 (queries) boxes for the TMA reductions
+  // fp32 dQ accumulator as head-dim x 32-query boxes for the TMA reductions:
+  // d = 128 one plain 128-column box, d = 64 two 128-byte-swizzled 32-column boxes
   const uint64_t qstrides[2] = {static_cast<uint64_t>(D) * 4, static_cast<uint64_t>(N) * D * 4};
-  const uint32_t qbox[3] = {static_cast<uint32_t>(D), 32, 1};
-  if (!encode_f32_tmap(&tdq, a.dQacc, 3, dims, qstrides, qbox)) return FA_ERR_CUDA;
+  const uint32_t qbox[3] = {D == 128 ? 128u : 32u, 32, 1};
+  if (!(D == 128 ? encode_f32_tmap(&tdq, a.dQacc, 3, dims, qstrides, qbox)
+                 : encode_f32_sw128_tmap(&tdq, a.dQacc, 3, dims, qstrides, qbox)))
+    return FA_ERR_CUDA;
   if (!set_smem_limit(reinterpret_cast<const void*>(&bwd_main_kernel<D, false>), C::kSmemBytes))
     return FA_ERR_CUDA;
   const long long pre_rows = static_cast<long long>(BH) * Npad;
@@ -800,8 +817,10 @@ fa_status bwd_varlen_launch_d(const void* Q, const void* K, const void* V, const
       !encode_bf16_tmap(&tv, V, 3, dims, strides, box) || !encode_bf16_tmap(&tdo, dO, 3, dims, strides, box))
     return FA_ERR_CUDA;
   const uint64_t qstrides[2] = {static_cast<uint64_t>(D) * 4, static_cast<uint64_t>(H) * D * 4};
-  const uint32_t qbox[3] = {static_cast<uint32_t>(D), 1, 32};
-  if (!encode_f32_tmap(&tdq, a.dQacc, 3, dims, qstrides, qbox)) return FA_ERR_CUDA;
+  const uint32_t qbox[3] = {D == 128 ? 128u : 32u, 1, 32};
+  if (!(D == 128 ? encode_f32_tmap(&tdq, a.dQacc, 3, dims, qstrides, qbox)
+                 : encode_f32_sw128_tmap(&tdq, a.dQacc, 3, dims, qstrides, qbox)))
+    return FA_ERR_CUDA;
   if (!set_smem_limit(reinterpret_cast<const void*>(&bwd_main_kernel<D, true>), C::kSmemBytes))
     return FA_ERR_CUDA;
   const long long pre_rows = static_cast<long long>(BH) * Npad;

@@ -27,6 +27,11 @@ bool encode_bf16_tmap(CUtensorMap* map, const void* base, int rank, const uint64
 bool encode_f32_tmap(CUtensorMap* map, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
                      const uint32_t* box);
 
+// Encode a tiled fp32 tensor map with the 128-byte swizzle (box rows of 32
+// elements; in shared memory the 16-byte chunk c of row y sits at chunk c ^ (y % 8)).
+bool encode_f32_sw128_tmap(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                           const uint64_t* strides_bytes, const uint32_t* box);
+
 inline int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
 
 inline fa_status launch_status() {
