@@ -35,7 +35,7 @@
 // Roles of the main kernel (20 warps = 5 warpgroups): warps 0-15 compute
 // (thread = key row of S^T / dP^T / dK / dV; warpgroup h takes query columns
 // 32h..32h+31 and head-dim columns h*d/4.. of dK/dV), warp 16 loads (TMA),
-// warp 17 issues the MMAs, warp 18 (d = 128) folds the next query tile's load
+// warp 17 issues the MMAs, warp 18 folds the next query tile's load
 // into the dS barrier (Q watcher), warp 19 idle; the fifth warpgroup hands
 // registers to the compute warps.
 #include <cuda.h>
@@ -101,10 +101,11 @@ enum : int {
 constexpr int kOffTmemSlot = kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 4;
 constexpr int kComputeWarps = 16;
-// d = 128: warp 18 folds the wait for the next query tile into the dS barrier
-// (measured: 2 % faster at d = 128, 2 % slower at d = 64)
+// warp 18 folds the wait for the next query tile into the dS barrier
+// (measured: 2 % faster at d = 128; at d = 64 2 % slower while dQ went out as
+// per-thread reductions, 1.4-2.3 % faster with the staged TMA reductions)
 template <int D>
-constexpr bool kQWatch = (D == 128);
+constexpr bool kQWatch = true;
 constexpr int kHeadGroup = 4;  // heads whose CTAs are interleaved in the grid
 
 struct BwdArgs {
@@ -292,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(BAR_S), 1);
     mbar_init(bar(BAR_P), kComputeWarps);
     mbar_init(bar(BAR_DP), 1);
-    mbar_init(bar(BAR_DS), kComputeWarps + (kQWatch<D> ? 1 : 0));  // + the Q watcher (d = 128)
+    mbar_init(bar(BAR_DS), kComputeWarps + (kQWatch<D> ? 1 : 0));  // + the Q watcher
     mbar_init(bar(BAR_DQ_FULL), 1);
     mbar_init(bar(BAR_DQ_READ), kComputeWarps);
     mbar_init(bar(BAR_FINAL), 1);
@@ -438,8 +439,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                      (it > 0 || k > 0) ? 1u : 0u);
             }
           } else {
-            // d = 64: dQ first, so its vector reductions (no staging in the
-            // dS^T buffer) start while dK runs
+            // d = 64: dQ first, so its read-out and staged reductions (own
+            // staging buffer, not the dS^T one) start while dK runs
             constexpr uint32_t idNN = idesc_bf16_f32(128, D, true, true);  // A = dS, B = K
 #pragma unroll
             for (int k = 0; k < kTile / 16; ++k)
@@ -453,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // Issued behind dK_i and dQ_i, so dQ_i reaches the compute warps (which
           // read it out next) without waiting for S_{i+1}.
           if (next) {
-            // d = 128: Q_i+1 has landed, the DS(i) barrier waited for above
+            // with the watcher: Q_i+1 has landed, the DS(i) barrier waited for above
             // completes only after the Q watcher has seen it
             if (!kQWatch<D> &&
                 !(ok = mbar_wait(bar(BAR_Q_FULL + ((it + 1) & 1)), ((it + 1) >> 1) & 1, wc)))
