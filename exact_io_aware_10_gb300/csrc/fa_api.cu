@@ -44,6 +44,23 @@ unsigned* device_status_ptr() {
   return g_status_ptr[dev];
 }
 
+fa_status decode_check_args(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                            const int32_t* seq_lens, const void* o, int B, int Hq, int Hkv, int d, int block_size,
+                            int max_blocks, int num_blocks, int num_splits, float scale) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || max_blocks < 1 || num_blocks < 1 || num_splits < 0) return FA_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !isfinite(scale)) return FA_ERR_INVALID_ARG;
+  if ((d != 64 && d != 128) || block_size < 16 || block_size % 16 != 0) return FA_ERR_UNSUPPORTED;
+  if (Hq / Hkv > 16 || num_splits > 16) return FA_ERR_UNSUPPORTED;
+  if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !o) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o)) return FA_ERR_INVALID_ARG;
+  // the kernels index cache rows and table-row keys in 32-bit integers
+  if (static_cast<long long>(num_blocks) * block_size > 0x7fffffffLL ||
+      static_cast<long long>(max_blocks) * block_size > 0x7fffffffLL)
+    return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
 namespace {
 bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, CUtensorMapSwizzle swizzle, const void* base, int rank,
                  const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box);
@@ -297,18 +314,11 @@ int fa_paged_decode(const void* q, const void* k_cache, const void* v_cache, con
                     const int32_t* seq_lens, void* o, float* lse, int B, int Hq, int Hkv, int d, int block_size,
                     int max_blocks, int num_blocks, int num_splits, float scale, void* workspace, size_t ws_bytes,
                     void* stream) {
-  if (B < 1 || Hq < 1 || Hkv < 1 || max_blocks < 1 || num_blocks < 1 || num_splits < 0) return FA_ERR_INVALID_ARG;
-  if (Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
-  if (bad_scale(scale)) return FA_ERR_INVALID_ARG;
-  if ((d != 64 && d != 128) || block_size < 16 || block_size % 16 != 0) return FA_ERR_UNSUPPORTED;
-  if (Hq / Hkv > 16 || num_splits > 16) return FA_ERR_UNSUPPORTED;
-  if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !o) return FA_ERR_INVALID_ARG;
+  const fa_status st = fa::decode_check_args(q, k_cache, v_cache, block_table, seq_lens, o, B, Hq, Hkv, d, block_size,
+                                             max_blocks, num_blocks, num_splits, scale);
+  if (st != FA_OK) return st;
   if (num_splits != 1 && !workspace) return FA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o)) return FA_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_INVALID_ARG;
-  if (static_cast<long long>(num_blocks) * block_size > 0x7fffffffLL ||
-      static_cast<long long>(max_blocks) * block_size > 0x7fffffffLL)
-    return FA_ERR_UNSUPPORTED;
   const int S = num_splits == 0 ? 16 : num_splits;
   if (ws_bytes < fa_paged_decode_workspace_size(B, Hq, d, S)) return FA_ERR_INVALID_ARG;
   return fa::decode_launch(q, k_cache, v_cache, block_table, seq_lens, o, lse, B, Hq, Hkv, d, block_size, max_blocks,

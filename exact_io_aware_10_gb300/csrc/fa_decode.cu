@@ -519,11 +519,16 @@ float* g_scratch_ptr[64] = {};
 
 // Device address of the scratch array on the current device, looked up once
 // per device (the host-side symbol is only a stand-in, not a device address).
-float* decode_scratch_ptr() {
+// The lookup is not made while `stream` is being captured into a graph: the
+// call then returns nullptr (FA_ERR_CUDA to the caller) and leaves the capture
+// untouched.
+float* decode_scratch_ptr(cudaStream_t stream) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
   std::lock_guard<std::mutex> lk(g_scratch_mu);
   if (g_scratch_ptr[dev] == nullptr) {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone) return nullptr;
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr) return nullptr;
     g_scratch_ptr[dev] = static_cast<float*>(p);
@@ -538,18 +543,12 @@ extern "C" int fa_paged_decode_noalloc(const void* q, const void* k_cache, const
                                        const int32_t* block_table, const int32_t* seq_lens, void* o, float* lse, int B,
                                        int Hq, int Hkv, int d, int block_size, int max_blocks, int num_blocks,
                                        int num_splits, float scale, void* stream) {
-  auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
-  if (B < 1 || Hq < 1 || Hkv < 1 || max_blocks < 1 || num_blocks < 1 || num_splits < 0) return FA_ERR_INVALID_ARG;
-  if (Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
-  if (!(scale > 0.f) || !isfinite(scale)) return FA_ERR_INVALID_ARG;
-  if ((d != 64 && d != 128) || block_size < fa::kBlk || block_size % fa::kBlk != 0) return FA_ERR_UNSUPPORTED;
-  if (Hq / Hkv > 16 || num_splits > 16) return FA_ERR_UNSUPPORTED;
-  if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !o) return FA_ERR_INVALID_ARG;
-  if (!al16(q) || !al16(k_cache) || !al16(v_cache) || !al16(o)) return FA_ERR_INVALID_ARG;
-  if (static_cast<long long>(num_blocks) * block_size > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  const fa_status st = fa::decode_check_args(q, k_cache, v_cache, block_table, seq_lens, o, B, Hq, Hkv, d,
+                                             block_size, max_blocks, num_blocks, num_splits, scale);
+  if (st != FA_OK) return st;
   const int S = num_splits == 0 ? 16 : num_splits;
   if (static_cast<size_t>(B) * Hq * S > fa::kNoAllocMaxStates) return FA_ERR_UNSUPPORTED;  // scratch too small
-  float* scratch = fa::decode_scratch_ptr();
+  float* scratch = fa::decode_scratch_ptr(static_cast<cudaStream_t>(stream));
   if (scratch == nullptr) return FA_ERR_CUDA;
   return fa::decode_launch(q, k_cache, v_cache, block_table, seq_lens, o, lse, B, Hq, Hkv, d, block_size, max_blocks,
                            num_blocks, S, scale, scratch, static_cast<cudaStream_t>(stream));

@@ -68,6 +68,11 @@ fa_status decode_prepare();
 bool set_smem_limit(const void* func, int bytes);
 // Loads the tensor-map encoder entry point if needed; false if unavailable.
 bool encode_init();
+// Argument checks shared by every paged-decode entry point (with and without
+// a caller workspace); the workspace itself is checked by the caller.
+fa_status decode_check_args(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                            const int32_t* seq_lens, const void* o, int B, int Hq, int Hkv, int d, int block_size,
+                            int max_blocks, int num_blocks, int num_splits, float scale);
 fa_status decode_launch(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
                         const int32_t* seq_lens, void* o, float* lse, int B, int Hq, int Hkv, int d, int block_size,
                         int max_blocks, int num_blocks, int num_splits, float scale, void* workspace,

@@ -300,7 +300,11 @@ void fa_decode_graph_destroy(fa_decode_graph* graph);
  *   the process exits.
  *   The first call on a device looks up the array's device address (once per
  *   device, with that device current); make that first call before any stream
- *   capture.
+ *   capture.  A first call made while `stream` is being captured does not
+ *   look the address up: it returns FA_ERR_CUDA, launches nothing and leaves
+ *   the capture as it was.  The address is kept for the life of the process;
+ *   after cudaDeviceReset on a device, do not call this entry point on that
+ *   device again in the same process.
  *   All calls on a device share the array and it keeps the last call's
  *   contents (nothing in it needs clearing between calls).  Calls that overlap
  *   on the GPU -- on different streams, or from host threads without ordering

@@ -1,16 +1,17 @@
 """Backward parity: forward + backward through the C ABI against the fp64
-oracle's analytic gradients on the same seeded inputs.  Tolerance: relative
-L2 error <= 1e-2 on dQ, dK and dV (bf16 inputs, fp32 accumulation)."""
+oracle's analytic gradients on the same seeded inputs.  Tolerance, per
+(batch entry, head) of dQ, dK and dV: relative L2 error <= 1e-2 and the
+largest element error <= 2e-2 of the slice's largest element (bf16 inputs,
+fp32 accumulation; tests/gradcheck.py states the bounds and their floor)."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
 from exact_io_aware_10_gb300 import workloads as wl
+from gradcheck import check_grads, dense_slices
 
 pytestmark = pytest.mark.gpu
-
-REL_L2 = 1e-2
 
 
 def _rel(a, b):
@@ -29,11 +30,9 @@ def _run(fa, x, causal, kv_lens=None, scale=None):
     return tuple(t.float().cpu().numpy() for t in (dQ, dK, dV))
 
 
-def _check(got, ref, heads=None):
-    for g, r, name in zip(got, ref, ("dQ", "dK", "dV")):
-        assert np.isfinite(g).all(), name
-        e = _rel(g, r)
-        assert e <= REL_L2, (name, e)
+def _check(got, ref):
+    B, H = np.asarray(ref[0]).shape[:2]
+    check_grads(got, ref, dense_slices(B, H))
 
 
 @pytest.mark.parametrize("causal", [False, True])
@@ -63,6 +62,18 @@ def test_ragged_lengths_d128(fa, N):
         _check(got, ref)
 
 
+@pytest.mark.parametrize("B,H", [(1, 6), (2, 3), (1, 5)])
+@pytest.mark.parametrize("d", [64, 128])
+def test_head_group_tail(fa, B, H, d):
+    # the backward grid runs over groups of four (batch, head) pairs: B*H = 6
+    # and 5 leave a partly filled last group
+    x = wl.dense_inputs(B, H, 300, d, seed=300 + 10 * B + H + d)
+    for causal in (False, True):
+        got = _run(fa, x, causal)
+        ref = oracle.attention_backward(x.Q, x.K, x.V, x.dO, causal=causal)
+        _check(got, ref)
+
+
 def test_key_padding_bert_shape(fa):
     B, H, N, d = 16, 16, 512, 64
     kv = wl.padded_lengths(B, 128, 512, seed=wl.config_seed(0, 2))
@@ -82,8 +93,8 @@ def test_key_padding_edge_lengths(fa):
         got = _run(fa, x, causal, kv_lens=kv)
         ref = oracle.attention_backward(x.Q, x.K, x.V, x.dO, causal=causal, kv_lens=kv.numpy())
         for b in range(6):
-            sub = tuple(g[b] for g in got)
-            refb = tuple(r[b] for r in ref)
+            sub = tuple(g[b:b + 1] for g in got)
+            refb = tuple(r[b:b + 1] for r in ref)
             if int(kv[b]) == 0:
                 assert all(np.all(s == 0) for s in sub)
             else:
