@@ -13,6 +13,15 @@ also as a fraction of the measured peaks.  `value` is the fwd/bwd TFLOP/s;
 the decode figure is in `decode`.  Inputs are seeded synthetic tensors drawn
 on the device; every per-kernel input is larger than the 129 MB L2.
 
+After the step (outside `value`), the same run times the encoder- and
+decoder-shaped configurations at d = 64 (BERT-large-shaped B16 H16 N512 with
+key padding, GPT-2-medium-shaped B8 H16 N1024 / N4096 causal with boosted
+logits), forward and backward, with L2 flushed before every timed call, and
+the built extensions (ragged batch, paged prefill, block-sparse, decode-step
+graph).  `roofline` carries one block of flat keys per kernel: the forward
+(the dominant kernel), the backward call, the decode pair and the small
+configurations.
+
 `--impl reference` times the fp64 CPU oracle on a bounded sample of the same
 workload instead (rank 0 only).  Under torchrun every rank runs an
 independent replica (the path has no exchange step); rank 0 prints one JSON
@@ -68,14 +77,37 @@ DECODE_STEP = dict(layers=32, B=1, Hq=32, Hkv=8, d=128, context=2048, config_id=
 WORKLOAD = ("long-context causal prefill B1 H16 d128 (fwd+bwd N=16384, fwd N=65536) + paged GQA decode "
             "B64 Hq32 Hkv8 d128 L~U[512,32768] block16 splits16")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# GB300 nominal dense figures, the denominators the targets are also stated in
-NOMINAL = {"bf16_tflops": 2250.0, "hbm_gbs": 8000.0}
-# ncu dram bytes (read + write) per launch of the dominant kernel, with the
-# hash of the kernel source they were taken on (null once the source changes)
-TRAFFIC_RECORD = {"kernel": "fwd_kernel<128>", "source": "exact_io_aware_10_gb300/csrc/fa_fwd.cu",
-                  "sha256": "d050d5d829ff731c2cbd0c91aead004c19d72584a81e87e77242829965ede001",
-                  "bytes_per_launch_N16384": 544236032 + 46380032,
-                  "bytes_per_launch_N65536": 7733645056 + 253309184}
+# GB300 nominal dense figures, the denominators the targets are stated in.
+# bf16: NVIDIA's HGX B300 specification gives 36 PFLOPS FP16/BF16 tensor
+# throughput for eight GPUs with 2:4 sparsity, i.e. 2.25 PFLOPS dense per GPU
+# (the primary figure).  NVIDIA's GB300 NVL72 rack specification gives 360
+# PFLOPS FP16/BF16 with sparsity for 72 GPUs, i.e. 2.5 PFLOPS dense per GPU;
+# every fraction is also reported against that stricter figure.  HBM3e: 8 TB/s.
+NOMINAL = {"bf16_tflops": 2250.0, "bf16_tflops_nvl72": 2500.0, "hbm_gbs": 8000.0}
+# ncu dram bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of
+# each kernel, one launch captured per shape, with the hash of the source file
+# they were taken on: a figure turns null once its source changes.
+TRAFFIC_RECORD = {
+    "fwd": {"kernel": "fwd_kernel<128>", "source": "exact_io_aware_10_gb300/csrc/fa_fwd.cu",
+            "sha256": "d050d5d829ff731c2cbd0c91aead004c19d72584a81e87e77242829965ede001",
+            "bytes": {"N16384": 544236032 + 46380032, "N65536": 7733645056 + 253309184}},
+    "bwd": {"kernel": "bwd_main_kernel<128>", "source": "exact_io_aware_10_gb300/csrc/fa_bwd.cu",
+            "sha256": None, "bytes": {}},
+    "decode": {"kernel": "decode_split_kernel<128> + decode_combine_kernel<128>",
+               "source": "exact_io_aware_10_gb300/csrc/fa_decode.cu", "sha256": None, "bytes": {}},
+}
+# the pages' encoder and decoder training shapes (BERT-large- and GPT-2-medium-
+# shaped attention, d = 64), timed after the step, forward and backward.  Their
+# inputs are close to or below the 129 MB L2, so L2 is flushed (a 256 MiB
+# write) before every timed call.  The BERT shape's key-padding lengths are
+# uniform in [128, 512]; its throughput counts the effective FLOPs (every query
+# row against its sequence's valid keys), the formula count is reported beside.
+SMALL = {
+    "bert": dict(B=16, H=16, N=512, d=64, causal=False, kv=(128, 512), boost=False, config_id=2, seed_off=0),
+    "gpt2_N1024": dict(B=8, H=16, N=1024, d=64, causal=True, kv=None, boost=True, config_id=3, seed_off=0),
+    "gpt2_N4096": dict(B=8, H=16, N=4096, d=64, causal=True, kv=None, boost=True, config_id=3, seed_off=1),
+}
+L2_FLUSH_BYTES = 256 << 20
 
 
 def load_peaks():
@@ -416,13 +448,68 @@ def time_decode_step(dev, seed, steps, warmup, barrier, max_over_ranks):
     return out
 
 
+def time_small_configs(dev, seed, steps, warmup, barrier, max_over_ranks, world, peak_tf):
+    """Forward and backward TFLOP/s of the SMALL configurations, L2 flushed
+    before every timed call.  Returns {name: {...}}."""
+    from exact_io_aware_10_gb300 import lib
+
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    out = {}
+    for name, c in SMALL.items():
+        sd = wl.config_seed(seed, c["config_id"]) + c["seed_off"]
+        shp = (c["B"], c["H"], c["N"], c["d"])
+        if c["boost"]:
+            x = wl.boosted_inputs(*shp, seed=sd)
+            Q, K, V, dO = (t.to(dev) for t in (x.Q, x.K, x.V, x.dO))
+        else:
+            Q, K, V, dO = (wl.device_normal_bf16(shp, sd + i, dev) for i in range(4))
+        kv_host = wl.padded_lengths(c["B"], c["kv"][0], c["kv"][1], seed=sd) if c["kv"] else None
+        kv = None if kv_host is None else kv_host.to(dev)
+        O = torch.empty_like(Q)
+        L = torch.empty(shp[:3], dtype=torch.float32, device=dev)
+        dQ, dK, dV = (torch.empty_like(Q) for _ in range(3))
+        ws = torch.empty(lib.fa_bwd_workspace_size(*shp), dtype=torch.uint8, device=dev)
+        causal = c["causal"]
+
+        def run(p):
+            if p == "fwd":
+                lib.fa_fwd(Q, K, V, causal=causal, kv_lens=kv, O=O, LSE=L)
+            else:
+                lib.fa_bwd(Q, K, V, O, dO, L, causal=causal, kv_lens=kv, dQ=dQ, dK=dK, dV=dV, workspace=ws)
+
+        _, ms = time_parts(run, ("fwd", "bwd"), steps, warmup, barrier, flush=flush_buf.zero_)
+        assert lib.fa_get_device_status() == lib.FA_OK, "device status word reported an error"
+        formula = acc.fwd_flops(*shp, causal)
+        eff = acc.fwd_flops_padded(c["H"], c["N"], c["d"], kv_host.tolist()) if kv_host is not None else formula
+        r = {"shape": f"B{c['B']} H{c['H']} N{c['N']} d{c['d']}", "causal": causal,
+             "key_padding": None if kv_host is None else f"U[{c['kv'][0]},{c['kv'][1]}]",
+             "boosted_logits": c["boost"], "flops_fwd": eff, "flops_fwd_formula": formula}
+        for p, mult in (("fwd", 1.0), ("bwd", 2.5)):
+            t = max_over_ranks(ms[p])
+            tf = world * steps * mult * eff / (t * 1e-3) / 1e12
+            r[p] = {"TFLOP/s": tf, "frac": tf / world / peak_tf, "frac_of_nominal": tf / world / NOMINAL["bf16_tflops"],
+                    "ms": t / steps}
+            if kv_host is not None:
+                r[p]["formula_TFLOP/s"] = world * steps * mult * formula / (t * 1e-3) / 1e12
+        out[name] = r
+        del Q, K, V, dO, O, L, dQ, dK, dV, ws
+        torch.cuda.empty_cache()
+    del flush_buf
+    torch.cuda.empty_cache()
+    return out
+
+
 class HostBuffers:
-    """Pinned host copies of a step's inputs and outputs for the end-to-end run."""
+    """Pinned host copies of a step's inputs and outputs for the end-to-end run.
+    A decode step's inputs are its queries, block table and sequence lengths:
+    the paged K/V cache is state that stays on the device between decode
+    steps (as a serving engine keeps it), so it is not re-uploaded every step;
+    its one-time upload is timed separately (`cache_upload`)."""
 
     def __init__(self, w: Workload):
         self.w = w
         self.inputs = {"fwd16": [w.Q, w.K, w.V], "bwd16": [w.dO], "fwd64": [w.Q64, w.K64, w.V64],
-                       "decode": [w.q, w.kc, w.vc, w.table, w.seq_lens]}
+                       "decode": [w.q, w.table, w.seq_lens]}
         self.outputs = {"fwd16": [w.O, w.L], "bwd16": [w.dQ, w.dK, w.dV], "fwd64": [w.O64, w.L64],
                         "decode": [w.o, w.lse]}
         self.h_in = {k: [t.cpu().pin_memory() for t in v] for k, v in self.inputs.items()}
@@ -433,6 +520,21 @@ class HostBuffers:
         h2d = sum(t.numel() * t.element_size() for t in self.h_in[part])
         d2h = sum(t.numel() * t.element_size() for t in self.h_out[part])
         return h2d, d2h
+
+    def cache_upload(self):
+        """Bytes and seconds of one host-to-device upload of the paged K/V
+        cache from pinned memory (one copy per cache tensor)."""
+        hk, hv = (t.cpu().pin_memory() for t in (self.w.kc, self.w.vc))
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        self.w.kc.copy_(hk, non_blocking=True)
+        self.w.vc.copy_(hv, non_blocking=True)
+        b.record()
+        torch.cuda.synchronize()
+        nbytes = sum(t.numel() * t.element_size() for t in (hk, hv))
+        del hk, hv
+        return nbytes, a.elapsed_time(b) * 1e-3
 
     def run(self, part):
         for d, h in zip(self.inputs[part], self.h_in[part]):
@@ -496,7 +598,10 @@ def source_sha(rel):
         return hashlib.sha256(f.read()).hexdigest()
 
 
-def time_parts(fn_for_part, parts, steps, warmup, barrier):
+def time_parts(fn_for_part, parts, steps, warmup, barrier, flush=None):
+    """CUDA-event time of every call of every part over `steps` steps (after
+    `warmup` untimed ones), on the current stream.  `flush`, if given, runs
+    before each timed call, outside its events (an L2 flush)."""
     stream = torch.cuda.current_stream()
     for _ in range(warmup):
         for p in parts:
@@ -509,6 +614,8 @@ def time_parts(fn_for_part, parts, steps, warmup, barrier):
     t0.record(stream)
     for k in range(steps):
         for p in parts:
+            if flush is not None:
+                flush()
             ev[p][k][0].record(stream)
             fn_for_part(p)
             ev[p][k][1].record(stream)
@@ -517,6 +624,82 @@ def time_parts(fn_for_part, parts, steps, warmup, barrier):
     barrier()
     per_part = {p: sum(a.elapsed_time(b) for a, b in ev[p]) for p in parts}  # ms over all steps
     return t0.elapsed_time(t1), per_part
+
+
+def recorded_traffic(which):
+    """ncu DRAM bytes per launch recorded for kernel family `which`, keyed by
+    shape, or None when none were taken on the current source."""
+    rec = TRAFFIC_RECORD[which]
+    if not rec["sha256"] or rec["sha256"] != source_sha(rec["source"]) or not rec["bytes"]:
+        return None
+    return rec["bytes"]
+
+
+def build_roofline(part_ms, flops, dbytes, K, peaks, peak_src):
+    """The roofline record: the dominant kernel (the forward) in the standard
+    keys, then flat bwd_* and decode_* blocks for the backward call and the
+    decode pair.  achieved = algorithmic FLOPs (bytes) per call / CUDA-event
+    time per call; traffic = ncu DRAM bytes per launch (null when not taken on
+    the current source)."""
+    P, D = PREFILL, DECODE
+    peak_tf, peak_hbm = peaks["bf16_tflops"], peaks["hbm_gbs"]
+    # forward: one launch of fwd_kernel<128> per fa_fwd call, two calls per step
+    fwd_ms = part_ms["fwd16"] + part_ms["fwd64"]
+    fwd_flops_step = flops["fwd16"] + flops["fwd64"]
+    achieved = K * fwd_flops_step / (fwd_ms * 1e-3) / 1e12
+    comp = {"N16384": acc.fwd_bytes(P["B"], P["H"], P["N_fb"], P["d"]),
+            "N65536": acc.fwd_bytes(P["B"], P["H"], P["N_f"], P["d"])}
+    t_fwd = recorded_traffic("fwd")
+    traffic = sum(t_fwd[k] for k in comp) / 2.0 if t_fwd and all(k in t_fwd for k in comp) else None
+    r = {"kernel": "fwd_kernel<128> (fa_fwd)", "bound": "tensor", "achieved": achieved, "peak": peak_tf,
+         "unit": "TFLOP/s", "frac": achieved / peak_tf, "traffic": traffic,
+         "compulsory_bytes": sum(comp.values()) / 2.0,
+         "traffic_N16384": t_fwd.get("N16384") if t_fwd else None,
+         "traffic_N65536": t_fwd.get("N65536") if t_fwd else None,
+         "compulsory_N16384": comp["N16384"], "compulsory_N65536": comp["N65536"],
+         "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum, one launch per shape",
+         "peak_source": f"{peak_src} bf16_tflops (burst)",
+         "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
+         "frac_of_nominal": achieved / NOMINAL["bf16_tflops"],
+         "frac_of_nominal_nvl72": achieved / NOMINAL["bf16_tflops_nvl72"],
+         "nominal_peak": NOMINAL["bf16_tflops"],
+         "launches_per_step": 2, "flops_per_step": fwd_flops_step,
+         "fwd_N16384_TFLOP/s": K * flops["fwd16"] / (part_ms["fwd16"] * 1e-3) / 1e12,
+         "fwd_N65536_TFLOP/s": K * flops["fwd64"] / (part_ms["fwd64"] * 1e-3) / 1e12}
+    # backward: one fa_bwd call = bwd_pre, bwd_main, bwd_dq launches
+    bwd = K * flops["bwd16"] / (part_ms["bwd16"] * 1e-3) / 1e12
+    t_bwd = recorded_traffic("bwd")
+    r.update({"bwd_kernel": "bwd_pre + bwd_main_kernel<128> + bwd_dq (fa_bwd, N=16384)", "bwd_bound": "tensor",
+              "bwd_achieved": bwd, "bwd_frac": bwd / peak_tf,
+              "bwd_frac_of_sustained": bwd / peaks["bf16_tflops_sustained"],
+              "bwd_frac_of_nominal": bwd / NOMINAL["bf16_tflops"],
+              "bwd_frac_of_nominal_nvl72": bwd / NOMINAL["bf16_tflops_nvl72"],
+              "bwd_traffic": t_bwd.get("N16384") if t_bwd else None,
+              "bwd_compulsory_bytes": acc.bwd_bytes(P["B"], P["H"], P["N_fb"], P["d"]),
+              "bwd_flops_per_call": flops["bwd16"]})
+    # decode: one fa_paged_decode call = split + combine launches
+    dec = K * dbytes / (part_ms["decode"] * 1e-3) / 1e9
+    t_dec = recorded_traffic("decode")
+    r.update({"decode_kernel": "decode_split_kernel<128> + decode_combine_kernel<128> (fa_paged_decode)",
+              "decode_bound": "hbm", "decode_achieved": dec, "decode_peak": peak_hbm, "decode_unit": "GB/s",
+              "decode_frac": dec / peak_hbm, "decode_frac_of_nominal": dec / NOMINAL["hbm_gbs"],
+              "decode_traffic": t_dec.get("B64") if t_dec else None,
+              "decode_algorithmic_bytes": dbytes, "decode_peak_source": f"{peak_src} hbm_gbs"})
+    return r
+
+
+def small_roofline_keys(small):
+    """Flat roofline keys of the small configurations (TFLOP/s and fraction of
+    the measured peak per call)."""
+    r = {}
+    for name, v in small.items():
+        for p in ("fwd", "bwd"):
+            r[f"{name}_{p}_TFLOP/s"] = v[p]["TFLOP/s"]
+            r[f"{name}_{p}_frac"] = v[p]["frac"]
+            r[f"{name}_{p}_ms"] = v[p]["ms"]
+            if "formula_TFLOP/s" in v[p]:
+                r[f"{name}_{p}_formula_TFLOP/s"] = v[p]["formula_TFLOP/s"]
+    return r
 
 
 def run_ours(args):
@@ -576,32 +759,7 @@ def run_ours(args):
                          "source": peak_src},
     }
 
-    # roofline of the dominant kernel: the forward kernel (one launch per fa_fwd call)
-    fwd_ms = part_ms["fwd16"] + part_ms["fwd64"]
-    fwd_flops_step = flops["fwd16"] + flops["fwd64"]
-    achieved = K * fwd_flops_step / (fwd_ms * 1e-3) / 1e12
-    traffic = None
-    rec = TRAFFIC_RECORD
-    if rec["sha256"] and rec["sha256"] == source_sha(rec["source"]):
-        per = [rec[k] for k in ("bytes_per_launch_N16384", "bytes_per_launch_N65536") if rec[k]]
-        if len(per) == 2:
-            traffic = sum(per) / 2.0
-        elif per:
-            traffic = {"N16384_only": per[0]}
-    P = PREFILL
-    roofline = {"kernel": "fwd_kernel<128> (fa_fwd)", "bound": "tensor", "achieved": achieved, "peak": peak_tf,
-                "unit": "TFLOP/s", "frac": achieved / peak_tf, "traffic": traffic,
-                "traffic_detail": None if traffic is None else {
-                    "dram_bytes_N16384": rec["bytes_per_launch_N16384"],
-                    "dram_bytes_N65536": rec["bytes_per_launch_N65536"],
-                    "compulsory_bytes_N16384": acc.fwd_bytes(P["B"], P["H"], P["N_fb"], P["d"]),
-                    "compulsory_bytes_N65536": acc.fwd_bytes(P["B"], P["H"], P["N_f"], P["d"]),
-                    "source": "ncu dram__bytes_read.sum + dram__bytes_write.sum, one launch each "
-                              "(profiles/fwd_kernel_d128_N16384_causal.md)"},
-                "peak_source": f"{peak_src} bf16_tflops (burst)",
-                "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
-                "frac_of_nominal": achieved / NOMINAL["bf16_tflops"],
-                "launches_per_step": 2, "flops_per_step": fwd_flops_step}
+    roofline = build_roofline(part_ms, flops, dbytes, K, peaks, peak_src)
 
     # end to end: the same parts through the C ABI with pinned host buffers,
     # host->device inputs and device->host outputs inside the timed region
@@ -618,15 +776,25 @@ def run_ours(args):
     pre_ms = max_over_ranks(hb.time_pipelined(prefill_parts, e2e_steps, 1))
     dec_ms = max_over_ranks(hb.time_pipelined(("decode",), e2e_steps, 1))
     pipe_value = world * prefill_flops / (pre_ms * 1e-3) / 1e12
+    cache_bytes, cache_s = hb.cache_upload()
     e2e = {"value": pipe_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
            "decode_GB/s": world * dbytes / (dec_ms * 1e-3) / 1e9,
            "ms_per_step": pre_ms + dec_ms,
            "overlap": "inputs copied in and outputs copied out every step on separate copy streams, "
                       "overlapped with the kernels of neighbouring parts and steps",
+           "decode_note": "decode inputs per step are q, block table and lengths; the paged K/V cache stays "
+                          "resident (uploaded once, timed in decode_cache_upload_GB/s)",
+           "decode_cache_bytes": cache_bytes, "decode_cache_upload_GB/s": cache_bytes / cache_s / 1e9,
            "serial": {"value": e2e_value, "unit": "TFLOP/s",
                       "decode_GB/s": world * e2e_steps * dbytes / (e2e_part["decode"] * 1e-3) / 1e9,
                       "ms_per_step": max_over_ranks(e2e_total) / e2e_steps,
                       "note": "copies and kernels in one stream, nothing overlapped"}}
+
+    # the encoder- and decoder-shaped configurations (d = 64), after the step
+    small = None
+    if not args.skip_small_configs:
+        small = time_small_configs(dev, args.seed, args.steps, args.warmup, barrier, max_over_ranks, world, peak_tf)
+        roofline.update(small_roofline_keys(small))
 
     next_rows = None
     if not args.skip_next_rows:
@@ -648,12 +816,14 @@ def run_ours(args):
             "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic",
             "config": {"workload": WORKLOAD, "parallelism": f"replicas{world}",
-                       "l2": "every kernel's inputs exceed the 129 MB L2 (no flush needed)",
+                       "l2": "step: every kernel's inputs exceed the 129 MB L2 (no flush); small configs: "
+                             "L2 flushed before each call",
                        "value_is": "fwd+bwd TFLOP/s over parts 1-3; decode GB/s in 'decode'"},
             "decode": {"value": dec_gbs, "unit": "GB/s", "frac": dec_gbs / world / peak_hbm,
                        "peak": peak_hbm, "peak_source": f"{peak_src} hbm_gbs", "bytes_per_step": dbytes},
             "parts": parts, "roofline": roofline, "e2e": e2e, "cpu_baseline": cpu,
-            "gpu_launches": K * sum(Workload.LAUNCHES.values()), "clocks": clocks, "next_rows": next_rows,
+            "gpu_launches": K * sum(Workload.LAUNCHES.values()), "clocks": clocks, "configs": small,
+            "next_rows": next_rows,
         }
         print(json.dumps(line))
     if dist is not None:
@@ -691,20 +861,103 @@ def _oracle_decode_sample(seed, n_seq):
     return dt, acc.decode_bytes(lens, D["Hq"], D["Hkv"], D["d"], D["block"])
 
 
-def cpu_baseline_sample(budget_s=15.0, seed=0):
-    """The oracle as it stands, timed on this host's cores on bounded samples."""
-    t_start = time.perf_counter()
-    secs, fl, heads = 0.0, 0.0, 0
-    while heads < 16 and (time.perf_counter() - t_start) < budget_s * 0.7:
-        dt, f = _oracle_prefill_sample(seed, heads, 4096)
-        secs += dt
-        fl += f
-        heads += 1
+def _row_subset(N, every=64):
+    """Every `every`-th query row plus the first and the last."""
+    return np.unique(np.concatenate([np.arange(0, N, every), [0, N - 1]]))
+
+
+def _causal_row_flops(rows, d):
+    """Algorithmic forward FLOPs of the given causal rows: 4 d per visible key."""
+    return 4.0 * d * float(np.sum(np.asarray(rows) + 1))
+
+
+def cpu_baseline_sample(budget_s=30.0, seed=0):
+    """The oracle as it stands, timed on this host's cores.  Following the
+    measurement plan: the tiny, BERT-shaped and GPT-2 N=1024 configurations in
+    full (forward + backward), the GPT-2 N=4096 one on whole heads; the
+    long-context rows (16K forward, 16K backward, 64K forward) on a row subset
+    (every 64th row plus the first and the last) of as many heads as the budget
+    allows.  Sampled items report rows/s (or heads/s) and the full-size time
+    extrapolated from it, labelled as extrapolated.  `value` is the algorithmic
+    FLOPs of everything timed over the seconds it took."""
+    import oracle
+
+    out = {"unit": "TFLOP/s", "cores": NCORES, "kind": "oracle"}
+    tot_fl, tot_s = 0.0, 0.0
+    share = budget_s / 30.0  # the item budgets below are sized for 30 s
+
+    def tick():
+        return time.perf_counter()
+
+    # config 1, in full: B1 H2 N256 d64, non-causal and causal
+    x = wl.dense_inputs(1, 2, 256, 64, seed=wl.config_seed(seed, 1))
+    t0 = tick()
+    for causal in (False, True):
+        oracle.attention_forward(x.Q, x.K, x.V, causal=causal)
+        oracle.attention_backward(x.Q, x.K, x.V, x.dO, causal=causal)
+    dt = tick() - t0
+    fl = 3.5 * (acc.fwd_flops(1, 2, 256, 64, False) + acc.fwd_flops(1, 2, 256, 64, True))
+    out["cfg1_s"] = dt
+    tot_fl, tot_s = tot_fl + fl, tot_s + dt
+    # config 2, in full: B16 H16 N512 d64, key padding U[128, 512]
+    c = SMALL["bert"]
+    sd = wl.config_seed(seed, c["config_id"])
+    kv = wl.padded_lengths(c["B"], c["kv"][0], c["kv"][1], seed=sd)
+    x = wl.dense_inputs(c["B"], c["H"], c["N"], c["d"], seed=sd)
+    t0 = tick()
+    oracle.attention_forward(x.Q, x.K, x.V, kv_lens=kv.numpy())
+    oracle.attention_backward(x.Q, x.K, x.V, x.dO, kv_lens=kv.numpy())
+    dt = tick() - t0
+    out["cfg2_bert_s"] = dt
+    tot_fl, tot_s = tot_fl + 3.5 * acc.fwd_flops_padded(c["H"], c["N"], c["d"], kv.tolist()), tot_s + dt
+    # config 3, N = 1024 in full; N = 4096 on whole heads, extrapolated to all
+    for name, heads_cap in (("gpt2_N1024", None), ("gpt2_N4096", max(1, int(2 * share)))):
+        c = SMALL[name]
+        sd = wl.config_seed(seed, c["config_id"]) + c["seed_off"]
+        B, H = (c["B"], c["H"]) if heads_cap is None else (1, heads_cap)
+        x = wl.boosted_inputs(B, H, c["N"], c["d"], seed=sd)
+        t0 = tick()
+        oracle.attention_forward(x.Q, x.K, x.V, causal=True)
+        oracle.attention_backward(x.Q, x.K, x.V, x.dO, causal=True)
+        dt = tick() - t0
+        tot_fl, tot_s = tot_fl + 3.5 * acc.fwd_flops(B, H, c["N"], c["d"], True), tot_s + dt
+        if heads_cap is None:
+            out[f"cfg3_{name}_s"] = dt
+        else:
+            out[f"cfg3_{name}_heads_timed"] = B * H
+            out[f"cfg3_{name}_s_extrapolated"] = dt * c["B"] * c["H"] / (B * H)
+    # config 4 on a row subset of each head (long-context prefill, d = 128)
+    P = PREFILL
+    for item, N, bwd, cap_s in (("fwd_N16384", P["N_fb"], False, 2.0), ("bwd_N16384", P["N_fb"], True, 5.0),
+                                ("fwd_N65536", P["N_f"], False, 6.0)):
+        rows = _row_subset(N)
+        n_rows, secs, fl, heads = 0, 0.0, 0.0, 0
+        while heads < P["H"] and (heads == 0 or secs < cap_s * share):
+            g = torch.Generator().manual_seed(wl.config_seed(seed, 4) * 31 + 1000 * heads + N)
+            shp = (1, 1, N, P["d"])
+            Q, K, V, dO = (torch.randn(*shp, generator=g).to(torch.bfloat16) for _ in range(4))
+            t0 = tick()
+            if bwd:
+                oracle.attention_backward_rows(Q, K, V, dO, rows, causal=True)
+            else:
+                oracle.attention_forward_rows(Q, K, V, rows, causal=True)
+            secs += tick() - t0
+            fl += _causal_row_flops(rows, P["d"]) * (2.5 if bwd else 1.0)
+            n_rows += len(rows)
+            heads += 1
+        rate = n_rows / secs
+        out[f"{item}_rows_per_s"] = rate
+        out[f"{item}_heads_timed"] = heads
+        out[f"{item}_s_extrapolated"] = P["B"] * P["H"] * N / rate
+        tot_fl, tot_s = tot_fl + fl, tot_s + secs
+    # paged decode on two sequences
     d_dt, d_bytes = _oracle_decode_sample(seed, 2)
-    return {"value": fl / secs / 1e12, "unit": "TFLOP/s", "cores": NCORES, "kind": "oracle",
-            "sample": f"fp64 numpy oracle fwd+bwd on {heads} head(s) of the long-prefill workload, causal prefix "
-                      f"N=4096, d=128 ({secs:.1f} s); decode GB/s on 2 sequences of the decode workload",
-            "decode_GB/s": d_bytes / d_dt / 1e9}
+    out["decode_GB/s"] = d_bytes / d_dt / 1e9
+    out["value"] = tot_fl / tot_s / 1e12
+    out["seconds"] = tot_s + d_dt
+    out["sample"] = ("fp64 numpy oracle: cfg 1-2 and GPT-2 N1024 in full, N4096 on whole heads, 16K/64K on every "
+                     "64th row; *_extrapolated = full size")
+    return out
 
 
 def run_reference(args):
@@ -739,8 +992,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--seed", type=int, default=0)
-    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--cpu-seconds", type=float, default=30.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--skip-small-configs", action="store_true",
+                    help="skip the BERT- and GPT-2-shaped d = 64 forward/backward timings")
     ap.add_argument("--skip-next-rows", action="store_true",
                     help="skip the ragged-batch, paged-prefill, block-sparse and decode-step timings")
     ap.add_argument("--ref-prefix", type=int, default=2048)

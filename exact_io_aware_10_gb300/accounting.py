@@ -15,7 +15,9 @@ Conventions (matmul work only; exp, masking and reductions are not counted):
   decode    bytes = K and V of every visible key, read once per KV head
             (sum_b L_b * Hkv * d * 2 B * 2) + q + o + lse + the block-table
             entries and sequence lengths read.
-Compulsory forward bytes are Q, K, V, O (2 B each) + LSE (4 B).
+Compulsory forward bytes are Q, K, V, O (2 B each) + LSE (4 B); backward bytes
+are Q, K, V, O, dO, dQ, dK, dV (2 B each) + LSE and D = rowsum(dO * O) (4 B
+each per row).
 """
 from __future__ import annotations
 
@@ -78,8 +80,9 @@ def fwd_bytes(B, H, N, d):
 
 
 def bwd_bytes(B, H, N, d):
-    # read Q, K, V, O, dO, LSE; write dQ, dK, dV (bf16) -- compulsory only
-    return 2.0 * B * H * N * d * 8 + 4.0 * B * H * N
+    # Q, K, V, O, dO read and dQ, dK, dV written (bf16), LSE and D (fp32) --
+    # compulsory only
+    return 2.0 * B * H * N * d * 8 + 8.0 * B * H * N
 
 
 def decode_bytes(seq_lens, Hq, Hkv, d, block_size=16, with_lse=True):

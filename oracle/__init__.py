@@ -32,6 +32,7 @@ from .attention import (  # noqa: F401
     attention_forward_rows,
     attention_forward_varlen,
     attention_backward,
+    attention_backward_rows,
     attention_backward_varlen,
     streaming_row_forward,
     algorithm1_forward,

@@ -164,6 +164,38 @@ def attention_backward(Q, K, V, dO, causal=False, scale=None, kv_lens=None,
     return dQ, dK, dV
 
 
+def attention_backward_rows(Q, K, V, dO, rows, causal=False, scale=None, kv_lens=None, heads=None):
+    """The backward restricted to the selected query ``rows``: the same chain
+    rule as ``attention_backward``, evaluated for those rows alone.
+
+    Returns dQ of the rows [len(heads), len(rows), d] and the rows' share of
+    dK and dV [len(heads), N_k, d] (the sum over the selected rows of
+    scale * dS_ij Q_i and P_ij dO_i).  Summing the shares over a partition of
+    all rows gives ``attention_backward``'s dK and dV.  D_i is taken as
+    sum_j P_ij dP_ij, which equals rowsum(dO_i * O_i).
+    """
+    Q, K, V, dO = to_f64(Q), to_f64(K), to_f64(V), to_f64(dO)
+    B, H, N, d = Q.shape
+    scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
+    rows = np.asarray(rows)
+    heads = [(b, h) for b, h in _head_iter(B, H)] if heads is None else list(heads)
+    n_k = K.shape[2]
+    dQ = np.zeros((len(heads), len(rows), d))
+    dK = np.zeros((len(heads), n_k, d))
+    dV = np.zeros((len(heads), n_k, V.shape[3]))
+    for t, (b, h) in enumerate(heads):
+        L = None if kv_lens is None else int(kv_lens[b])
+        S = scale * (Q[b, h][rows] @ K[b, h].T)
+        P, _, _ = _softmax_rows(S, valid_key_mask(N, n_k, causal, L, rows=rows))
+        dP = dO[b, h][rows] @ V[b, h].T
+        D = (P * dP).sum(axis=1)
+        dS = P * (dP - D[:, None])
+        dQ[t] = scale * (dS @ K[b, h])
+        dK[t] = scale * (dS.T @ Q[b, h][rows])
+        dV[t] = P.T @ dO[b, h][rows]
+    return dQ, dK, dV
+
+
 def streaming_row_forward(q, K, V, tile, scale, key_mask=None, nan_guard=True):
     """One query row by the online-softmax loop of [S12] ("核心思路"):
     running max m, running sum l, unnormalised accumulator o; each key tile

@@ -56,3 +56,18 @@ def test_block_sparse_counts_visible_pairs(N, causal):
                                                                       if causal else True))
                for b in range(2) for h in range(2))
     assert acc.block_sparse_flops(per, 2, 2, N, 8, causal) == 4 * 8 * want
+
+
+def test_key_padding_effective_count_is_every_row_times_its_valid_keys():
+    N, H, d = 40, 3, 8
+    kv = [40, 7, 0, 23]
+    pairs = sum(_pairs(oracle.valid_key_mask(N, N, False, L)) for L in kv)
+    assert acc.fwd_flops_padded(H, N, d, kv) == 4 * d * H * pairs
+
+
+def test_compulsory_bytes_are_the_tensors_each_call_must_touch():
+    B, H, N, d = 2, 3, 50, 64
+    bf16 = B * H * N * d * 2
+    row = B * H * N * 4
+    assert acc.fwd_bytes(B, H, N, d) == 4 * bf16 + row  # Q, K, V, O + LSE
+    assert acc.bwd_bytes(B, H, N, d) == 8 * bf16 + 2 * row  # Q, K, V, O, dO, dQ, dK, dV + LSE, D

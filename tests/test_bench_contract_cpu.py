@@ -81,3 +81,29 @@ def test_product_arm_fails_loudly_without_a_gpu():
     r = _run([sys.executable, BENCH, "--steps", "3", "--warmup", "3", "--no-cpu-baseline", "--skip-next-rows"])
     assert r.returncode != 0
     assert not _json_lines(r.stdout)
+
+
+def test_roofline_record_is_flat_and_consistent():
+    # every kernel's figures sit in flat scalar keys (a reader that keeps only
+    # scalars keeps them all); fractions are achieved over the stated peaks
+    sys.path.insert(0, ROOT)
+    import bench
+
+    peaks = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+    K = 10
+    part_ms = {"fwd16": 8.0, "bwd16": 26.0, "fwd64": 115.0, "decode": 7.0}
+    flops = {"fwd16": 1.0995e12, "bwd16": 2.7488e12, "fwd64": 1.7592e13}
+    r = bench.build_roofline(part_ms, flops, 4.4e9, K, peaks, "measured")
+    small = {"bert": {"fwd": {"TFLOP/s": 400.0, "frac": 0.2, "ms": 0.04, "formula_TFLOP/s": 600.0},
+                      "bwd": {"TFLOP/s": 300.0, "frac": 0.15, "ms": 0.1}}}
+    r.update(bench.small_roofline_keys(small))
+    for k, v in r.items():
+        assert v is None or isinstance(v, (int, float, str)), (k, type(v))
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s" and r["peak"] == 1900.0
+    want = K * (flops["fwd16"] + flops["fwd64"]) / ((part_ms["fwd16"] + part_ms["fwd64"]) * 1e-3) / 1e12
+    assert abs(r["achieved"] - want) < 1e-9 * want and abs(r["frac"] - want / 1900.0) < 1e-12
+    bwd = K * flops["bwd16"] / (part_ms["bwd16"] * 1e-3) / 1e12
+    assert abs(r["bwd_achieved"] - bwd) < 1e-9 * bwd and abs(r["bwd_frac"] - bwd / 1900.0) < 1e-12
+    dec = K * 4.4e9 / (part_ms["decode"] * 1e-3) / 1e9
+    assert r["decode_bound"] == "hbm" and abs(r["decode_frac"] - dec / 6800.0) < 1e-12
+    assert r["bert_fwd_formula_TFLOP/s"] == 600.0 and r["bert_bwd_frac"] == 0.15

@@ -64,3 +64,13 @@ def test_packed_short_sequence_is_judged_on_its_own():
     with pytest.raises(AssertionError, match=r"\(1, 1\)"):
         check_grads([g, r, r], [r, r, r], packed_slices(cu, H))
     check_grads([r, r, r], [r, r, r], packed_slices(cu, H))
+
+
+def test_whole_tensor_zero_uses_the_other_gradients_scale():
+    # one key per row: dQ = dK = 0 everywhere, dV = dO
+    dv = _ref((2, 2, 1, 64))
+    z = np.zeros_like(dv)
+    res = 1e-7 * _ref(dv.shape, 9)
+    check_grads([res, res, dv], [z, z, dv], dense_slices(2, 2))
+    with pytest.raises(AssertionError, match="dQ"):
+        check_grads([1e-2 * _ref(dv.shape, 9), res, dv], [z, z, dv], dense_slices(2, 2))

@@ -267,6 +267,61 @@ def test_rowsum_identity_and_padded_keys_get_no_gradient():
     assert np.all(dK[1, :, 9:] == 0) and np.all(dV[1, :, 9:] == 0)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_rows_match_finite_differences_of_the_rows_loss(causal):
+    # the loss restricted to the selected rows, sum_{i in rows} dO_i . O_i: its
+    # gradient is dQ on those rows (zero elsewhere) and the rows' share of dK, dV
+    B, H, N, d = 1, 1, 8, 3
+    Q, K, V, dO = (_rand((B, H, N, d), s) for s in (48, 49, 50, 51))
+    rows = np.array([0, 3, 7])
+    kv = np.array([6])
+    scale = 0.7
+    gq, gk, gv = oracle.attention_backward_rows(Q, K, V, dO, rows, causal=causal, scale=scale, kv_lens=kv)
+    mask = np.zeros((N, 1))
+    mask[rows] = 1.0
+
+    def loss():
+        O, _ = oracle.attention_forward(Q, K, V, causal=causal, scale=scale, kv_lens=kv)
+        return float((O[0, 0] * dO[0, 0] * mask).sum())
+
+    h = 1e-6
+    for X, G in ((Q, None), (K, gk[0]), (V, gv[0])):
+        num = np.zeros((N, d))
+        for i in range(N):
+            for c in range(d):
+                x0 = X[0, 0, i, c]
+                X[0, 0, i, c] = x0 + h
+                fp = loss()
+                X[0, 0, i, c] = x0 - h
+                fm = loss()
+                X[0, 0, i, c] = x0
+                num[i, c] = (fp - fm) / (2 * h)
+        if G is None:  # Q: only the selected rows carry gradient
+            assert np.abs(np.delete(num, rows, axis=0)).max() <= 1e-8
+            num, G = num[rows], gq[0]
+        err = np.linalg.norm(num - G) / max(np.linalg.norm(G), 1e-30)
+        assert err <= 1e-6, err
+
+
+def test_backward_rows_over_a_partition_sum_to_the_full_backward():
+    B, H, N, d = 2, 2, 37, 8
+    Q, K, V, dO = (_rand((B, H, N, d), s) for s in (52, 53, 54, 55))
+    kv = np.array([37, 20])
+    for causal in (False, True):
+        dQ, dK, dV = oracle.attention_backward(Q, K, V, dO, causal=causal, kv_lens=kv)
+        parts = [np.arange(0, 10), np.arange(10, 11), np.arange(11, 37)]
+        acc_k, acc_v = np.zeros_like(dK), np.zeros_like(dV)
+        heads = [(b, h) for b in range(B) for h in range(H)]
+        for rows in parts:
+            gq, gk, gv = oracle.attention_backward_rows(Q, K, V, dO, rows, causal=causal, kv_lens=kv, heads=heads)
+            for t, (b, h) in enumerate(heads):
+                np.testing.assert_allclose(gq[t], dQ[b, h, rows], atol=1e-12)
+                acc_k[b, h] += gk[t]
+                acc_v[b, h] += gv[t]
+        np.testing.assert_allclose(acc_k, dK, atol=1e-12)
+        np.testing.assert_allclose(acc_v, dV, atol=1e-12)
+
+
 # ---------------------------------------------------------------- paged decode pins
 
 
