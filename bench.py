@@ -89,10 +89,11 @@ NOMINAL = {"bf16_tflops": 2250.0, "bf16_tflops_nvl72": 2500.0, "hbm_gbs": 8000.0
 # they were taken on: a figure turns null once its source changes.
 TRAFFIC_RECORD = {
     "fwd": {"kernel": "fwd_kernel<128>", "source": "exact_io_aware_10_gb300/csrc/fa_fwd.cu",
-            "sha256": "d050d5d829ff731c2cbd0c91aead004c19d72584a81e87e77242829965ede001",
-            "bytes": {"N16384": 544236032 + 46380032, "N65536": 7733645056 + 253309184}},
+            "sha256": "20da90d48ea23bebe97fc7f1d361d013e990741fed534aa33d196bf35c02c436",
+            "bytes": {"N16384": 288711936 + 47219712, "N65536": 1163000064 + 249906688}},
     "bwd": {"kernel": "bwd_main_kernel<128>", "source": "exact_io_aware_10_gb300/csrc/fa_bwd.cu",
-            "sha256": None, "bytes": {}},
+            "sha256": "6364e1a7f33ac160aaeaf86c8d3de189507bc15593615095dd06810a3c6ab096",
+            "bytes": {"N16384": 408349696 + 225830400}},
     "decode": {"kernel": "decode_split_kernel<128> + decode_combine_kernel<128>",
                "source": "exact_io_aware_10_gb300/csrc/fa_decode.cu", "sha256": None, "bytes": {}},
 }

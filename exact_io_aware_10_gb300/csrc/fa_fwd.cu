@@ -103,6 +103,7 @@ struct FwdArgs {
   const int32_t* cu_seqlens;
   int total;
   int H, N;
+  int head_group;  // heads whose CTAs are interleaved in the grid (its x extent)
   int causal;
   float scale_log2;  // scale * log2(e)
   unsigned* status;
@@ -143,14 +144,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // grid (H, query-tile pairs, B or num_seqs): the heads of one batch entry
-  // (sequence) run side by side, so concurrent CTAs share its K/V in L2
-  const int bh = blockIdx.z * gridDim.x + blockIdx.x;  // dense: batch * H + head; packed: sequence * H + head
+  // grid (heads of a group, query-tile pairs, batch entry or sequence x head
+  // group): the heads of a group run side by side, so concurrent CTAs share
+  // their K/V in L2.  A group is every head of a batch entry unless those
+  // heads' K/V would not fit in L2 together (long N), then fewer heads.
+  const int hgrp = args.head_group;
+  const int ngrp = (args.H + hgrp - 1) / hgrp;
+  const int head = static_cast<int>(blockIdx.z % ngrp) * hgrp + static_cast<int>(blockIdx.x);
+  if (head >= args.H) return;  // the last group of a head count hgrp does not divide
+  const int bh = static_cast<int>(blockIdx.z / ngrp) * args.H + head;  // dense: batch * H + head; packed: sequence * H + head
   const int b = bh / args.H;
   const int mblk = gridDim.y - 1 - blockIdx.y;  // longest causal work first
   const int N = args.N;
   const bool packed = args.cu_seqlens != nullptr;
-  const int head = bh % args.H;
 
   const bool paged = args.block_table != nullptr;
   const int kv_head = paged ? head / args.group : head;
@@ -612,6 +618,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Heads per grid group for the dense forward: all H heads of a batch entry
+// while their K and V (2 N d bf16 each per head) fit in kL2KVBudget bytes
+// together, else the largest divisor of H whose heads do (at least one).
+// In-flight CTAs then stream K/V that L2 still holds instead of re-reading it
+// from DRAM once per CTA.  The grid's z extent (B x groups) stays <= 65535.
+constexpr double kL2KVBudget = 64.0 * 1024 * 1024;
+inline int dense_head_group(int B, int H, int N, int D) {
+  const double kv_head = 4.0 * static_cast<double>(N) * D;  // K and V of one head, bf16
+  int best = H;  // every head: the grid's z extent is then B <= 65535
+  for (int g = H; g >= 1; --g) {
+    if (H % g != 0 || static_cast<long long>(B) * (H / g) > 65535) continue;
+    best = g;
+    if (g * kv_head <= kL2KVBudget) return g;
+  }
+  return best;
+}
+
 template <int D>
 fa_status fwd_launch_d(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N,
                        int causal, float scale, const int32_t* kv_lens, const uint8_t* block_mask,
@@ -641,7 +664,8 @@ fa_status fwd_launch_d(const void* Q, const void* K, const void* V, void* O, flo
   a.causal = causal ? 1 : 0;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.status = status;
-  dim3 grid(H, ceil_div(N, 2 * kRows), B);
+  a.head_group = dense_head_group(B, H, N, D);
+  dim3 grid(a.head_group, ceil_div(N, 2 * kRows), B * ceil_div(H, a.head_group));
   fwd_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, a);
   return launch_status();
 }
@@ -673,6 +697,7 @@ fa_status fwd_varlen_launch_d(const void* Q, const void* K, const void* V, void*
   a.causal = causal ? 1 : 0;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.status = status;
+  a.head_group = H;
   dim3 grid(H, ceil_div(max_seqlen, 2 * kRows), num_seqs);
   fwd_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, a);
   return launch_status();
@@ -720,6 +745,7 @@ fa_status fwd_paged_launch_d(const void* q, const void* k_cache, const void* v_c
   a.num_rows = num_rows;
   a.num_blocks = num_blocks;
   a.group = Hq / Hkv;
+  a.head_group = Hq;
   dim3 grid(Hq, ceil_div(max_seqlen_q, 2 * kRows), num_seqs);
   fwd_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, a);
   return launch_status();
