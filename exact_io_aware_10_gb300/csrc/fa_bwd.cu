@@ -155,64 +155,66 @@ __device__ __forceinline__ int packed_range(const BwdArgs& a, int b, int& tok0) 
 }
 
 // --------------------------------------------------------------------------- 1. preprocess
-// One warp per row: -D = -rowsum(dO * O) in fp32, -LSE in log2 units, dQacc row = 0.
+// -D = -rowsum(dO * O) in fp32, -LSE in log2 units, dQacc row = 0.  A row is
+// read by D / 8 lanes with 16-byte loads (16 lanes at d = 128, 8 at d = 64),
+// so one warp covers 32 / (D / 8) rows; the partial sums are combined by
+// shuffles within each row's lanes.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ O,
                                                       const __nv_bfloat16* __restrict__ dO,
                                                       const float* __restrict__ LSE, BwdArgs a, int BH) {
-  const long long gw = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  constexpr int kLanesPerRow = D / 8;               // 16-byte chunks of a bf16 row
+  constexpr int kRowsPerWarp = 32 / kLanesPerRow;  // 2 (d = 128) or 4 (d = 64)
   const int lane = threadIdx.x & 31;
+  const int sub = lane % kLanesPerRow;
+  const long long gw = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const long long gr = gw * kRowsPerWarp + lane / kLanesPerRow;  // row over [BH, Npad]
   const long long rows = static_cast<long long>(BH) * a.Npad;
-  if (gw >= rows) return;
-  const int bh = static_cast<int>(gw / a.Npad);
-  const int r = static_cast<int>(gw % a.Npad);
+  const bool have = gr < rows;
+  const int bh = have ? static_cast<int>(gr / a.Npad) : 0;
+  const int r = have ? static_cast<int>(gr % a.Npad) : 0;
   int len = a.N;
   int tok0 = 0;
-  if (a.cu_seqlens != nullptr) {
+  if (a.cu_seqlens != nullptr && have) {
     len = packed_range(a, bh / a.H, tok0);
     if (len < 0) {
-      if (r == 0 && lane == 0) atomicOr(a.status, kStatusBadArgBit);
+      if (r == 0 && sub == 0) atomicOr(a.status, kStatusBadArgBit);
       len = 0;
     }
   }
-  if (r >= len) {
-    if (lane == 0) {
-      a.Dpad[gw] = 0.f;
-      a.Lpad[gw] = -INFINITY;
-    }
-    return;
-  }
-  // [B, H, N, D] rows, or [total, H, D] rows when packed (LSE [H, total])
-  const size_t row = a.cu_seqlens != nullptr ? static_cast<size_t>(tok0 + r) * a.H + bh % a.H
-                                             : static_cast<size_t>(bh) * a.N + r;
-  const size_t lrow = a.cu_seqlens != nullptr ? static_cast<size_t>(bh % a.H) * a.total + tok0 + r : row;
-  constexpr int kPer = D / 32;  // 2 or 4 elements per lane
+  const bool live = have && r < len;
   float acc = 0.f;
-  if constexpr (kPer == 4) {
-    const uint2 o = *reinterpret_cast<const uint2*>(O + row * D + 4 * lane);
-    const uint2 g = *reinterpret_cast<const uint2*>(dO + row * D + 4 * lane);
+  size_t row = 0;
+  if (live) {
+    // [B, H, N, D] rows, or [total, H, D] rows when packed (LSE [H, total])
+    row = a.cu_seqlens != nullptr ? static_cast<size_t>(tok0 + r) * a.H + bh % a.H
+                                  : static_cast<size_t>(bh) * a.N + r;
+    const uint4 o = *reinterpret_cast<const uint4*>(O + row * D + 8 * sub);
+    const uint4 g = *reinterpret_cast<const uint4*>(dO + row * D + 8 * sub);
     const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&o);
     const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g);
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < 4; ++i) {
       const float2 of = __bfloat1622float2(o2[i]);
       const float2 gf = __bfloat1622float2(g2[i]);
       acc = fmaf(of.x, gf.x, acc);
       acc = fmaf(of.y, gf.y, acc);
     }
-    *reinterpret_cast<float4*>(a.dQacc + row * D + 4 * lane) = make_float4(0.f, 0.f, 0.f, 0.f);
-  } else {
-    const __nv_bfloat162 o = *reinterpret_cast<const __nv_bfloat162*>(O + row * D + 2 * lane);
-    const __nv_bfloat162 g = *reinterpret_cast<const __nv_bfloat162*>(dO + row * D + 2 * lane);
-    const float2 of = __bfloat1622float2(o), gf = __bfloat1622float2(g);
-    acc = fmaf(of.x, gf.x, of.y * gf.y);
-    *reinterpret_cast<float2*>(a.dQacc + row * D + 2 * lane) = make_float2(0.f, 0.f);
+    float4* q = reinterpret_cast<float4*>(a.dQacc + row * D + 8 * sub);
+    q[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    q[1] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0) {
-    a.Dpad[gw] = -acc;
-    a.Lpad[gw] = -LSE[lrow] * kLog2e;
+  for (int off = kLanesPerRow / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (have && sub == 0) {
+    if (live) {
+      const size_t lrow = a.cu_seqlens != nullptr ? static_cast<size_t>(bh % a.H) * a.total + tok0 + r : row;
+      a.Dpad[gr] = -acc;
+      a.Lpad[gr] = -LSE[lrow] * kLog2e;
+    } else {
+      a.Dpad[gr] = 0.f;
+      a.Lpad[gr] = -INFINITY;
+    }
   }
 }
 
@@ -768,7 +770,7 @@ fa_status bwd_launch_d(const void* Q, const void* K, const void* V, const void* 
   if (!set_smem_limit(reinterpret_cast<const void*>(&bwd_main_kernel<D, false>), C::kSmemBytes))
     return FA_ERR_CUDA;
   const long long pre_rows = static_cast<long long>(BH) * Npad;
-  bwd_pre_kernel<D><<<static_cast<unsigned>((pre_rows + 7) / 8), 256, 0, stream>>>(
+  bwd_pre_kernel<D><<<static_cast<unsigned>((pre_rows + 8 * (256 / D) - 1) / (8 * (256 / D))), 256, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), LSE, a, BH);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   const dim3 grid(nq * kHeadGroup, ceil_div(BH, kHeadGroup));
@@ -825,7 +827,7 @@ fa_status bwd_varlen_launch_d(const void* Q, const void* K, const void* V, const
   if (!set_smem_limit(reinterpret_cast<const void*>(&bwd_main_kernel<D, true>), C::kSmemBytes))
     return FA_ERR_CUDA;
   const long long pre_rows = static_cast<long long>(BH) * Npad;
-  bwd_pre_kernel<D><<<static_cast<unsigned>((pre_rows + 7) / 8), 256, 0, stream>>>(
+  bwd_pre_kernel<D><<<static_cast<unsigned>((pre_rows + 8 * (256 / D) - 1) / (8 * (256 / D))), 256, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), LSE, a, BH);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   const dim3 grid(nq * kHeadGroup, ceil_div(BH, kHeadGroup));
