@@ -91,11 +91,15 @@ TRAFFIC_RECORD = {
     "fwd": {"kernel": "fwd_kernel<128>", "source": "exact_io_aware_10_gb300/csrc/fa_fwd.cu",
             "sha256": "20da90d48ea23bebe97fc7f1d361d013e990741fed534aa33d196bf35c02c436",
             "bytes": {"N16384": 288711936 + 47219712, "N65536": 1163000064 + 249906688}},
-    "bwd": {"kernel": "bwd_main_kernel<128>", "source": "exact_io_aware_10_gb300/csrc/fa_bwd.cu",
-            "sha256": "6364e1a7f33ac160aaeaf86c8d3de189507bc15593615095dd06810a3c6ab096",
-            "bytes": {"N16384": 408349696 + 225830400}},
+    "bwd": {"kernel": "bwd_pre_kernel<128> + bwd_main_kernel<128> + bwd_dq_kernel",
+            "source": "exact_io_aware_10_gb300/csrc/fa_bwd.cu",
+            "sha256": "1204a888e0cf664a1638112fef28cc6841caf1319cad7421019c937ea615a100",
+            "bytes": {"N16384_main": 407740672 + 221462272, "N16384_pre": 135282176 + 86865152,
+                      "N16384_dq": 134232320 + 35462656}},
     "decode": {"kernel": "decode_split_kernel<128> + decode_combine_kernel<128>",
-               "source": "exact_io_aware_10_gb300/csrc/fa_decode.cu", "sha256": None, "bytes": {}},
+               "source": "exact_io_aware_10_gb300/csrc/fa_decode.cu",
+               "sha256": "46f760001ee8943807a4193b3045b0ff836a7f745d5d58ca79693015f36c3d05",
+               "bytes": {"B64": 4424701440 + 17752832 + 15574272 + 0}},
 }
 # the pages' encoder and decoder training shapes (BERT-large- and GPT-2-medium-
 # shaped attention, d = 64), timed after the step, forward and backward.  Their
@@ -675,7 +679,10 @@ def build_roofline(part_ms, flops, dbytes, K, peaks, peak_src):
               "bwd_frac_of_sustained": bwd / peaks["bf16_tflops_sustained"],
               "bwd_frac_of_nominal": bwd / NOMINAL["bf16_tflops"],
               "bwd_frac_of_nominal_nvl72": bwd / NOMINAL["bf16_tflops_nvl72"],
-              "bwd_traffic": t_bwd.get("N16384") if t_bwd else None,
+              "bwd_traffic": (sum(t_bwd[k] for k in ("N16384_pre", "N16384_main", "N16384_dq"))
+                              if t_bwd and all(k in t_bwd for k in ("N16384_pre", "N16384_main", "N16384_dq"))
+                              else None),
+              "bwd_main_traffic": t_bwd.get("N16384_main") if t_bwd else None,
               "bwd_compulsory_bytes": acc.bwd_bytes(P["B"], P["H"], P["N_fb"], P["d"]),
               "bwd_flops_per_call": flops["bwd16"]})
     # decode: one fa_paged_decode call = split + combine launches
