@@ -97,6 +97,20 @@ bool set_smem_limit(const void* func, int bytes) {
   return true;
 }
 
+int sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  static int counts[kMaxDevices] = {};
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lk(mu);
+  if (counts[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    counts[dev] = n;
+  }
+  return counts[dev];
+}
+
 bool encode_init() {
   std::lock_guard<std::mutex> lk(g_mu);
   if (g_encode == nullptr) {
@@ -260,7 +274,8 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
   if (B < 1 || H < 1 || N < 0 || d < 1) return 0;
   const size_t bh = static_cast<size_t>(B) * H;
   const size_t npad = (static_cast<size_t>(N) + 127) / 128 * 128;
-  return 2 * round256(bh * npad * sizeof(float)) + round256(bh * N * d * sizeof(float));
+  // -D and -LSE2 rows, the fp32 dQ accumulator, the main kernel's work counter
+  return 2 * round256(bh * npad * sizeof(float)) + round256(bh * N * d * sizeof(float)) + 256;
 }
 
 int fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE, void* dQ,
@@ -279,7 +294,7 @@ int fa_bwd(const void* Q, const void* K, const void* V, const void* O, const voi
 size_t fa_bwd_varlen_workspace_size(int num_seqs, int total, int max_seqlen, int H, int d) {
   if (num_seqs < 1 || total < 0 || max_seqlen < 0 || H < 1 || d < 1) return 0;
   const size_t rows = static_cast<size_t>(num_seqs) * H * ((static_cast<size_t>(max_seqlen) + 127) / 128 * 128);
-  return 2 * round256(rows * sizeof(float)) + round256(static_cast<size_t>(total) * H * d * sizeof(float));
+  return 2 * round256(rows * sizeof(float)) + round256(static_cast<size_t>(total) * H * d * sizeof(float)) + 256;
 }
 
 int fa_bwd_varlen(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,

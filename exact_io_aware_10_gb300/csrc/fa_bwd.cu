@@ -7,10 +7,14 @@
 //
 // Three launches on one stream:
 //  1. bwd_pre_kernel   -D_i = -sum_c dO_ic O_ic and -LSE_i * log2(e) into padded
-//                      fp32 rows (0 / -inf past N), and dQacc <- 0.
-//  2. bwd_main_kernel  one CTA per (128-key tile j, batch*head); the grid runs
-//                      over groups of four heads so the CTAs in flight share a
-//                      few heads' Q, dO and dQ accumulator in L2.  K_j and V_j stay in shared
+//                      fp32 rows (0 / -inf past N), dQacc <- 0 and the main
+//                      kernel's work counter <- 0.
+//  2. bwd_main_kernel  one persistent CTA per SM; its work items are the
+//                      (128-key tile j, batch*head) pairs, taken in order from a
+//                      counter in the workspace: groups of four heads, within
+//                      a group the key tiles with most query tiles first, so
+//                      the items in flight share a few heads' Q, dO and dQ
+//                      accumulator in L2.  K_j and V_j stay in shared
 //                      memory; the CTA streams the query tiles i that see
 //                      tile j and, per tile, runs five tcgen05 MMAs with fp32
 //                      accumulators in TMEM:
@@ -34,8 +38,8 @@
 //
 // Roles of the main kernel (20 warps = 5 warpgroups): warps 0-15 compute
 // (thread = key row of S^T / dP^T / dK / dV; warpgroup h takes query columns
-// 32h..32h+31 and head-dim columns h*d/4.. of dK/dV), warp 16 loads (TMA),
-// warp 17 issues the MMAs, warp 18 folds the next query tile's load
+// 32h..32h+31 and head-dim columns h*d/4.. of dK/dV), warp 16 takes the work
+// items from the counter and loads (TMA), warp 17 issues the MMAs, warp 18 folds the next query tile's load
 // into the dS barrier (Q watcher), warp 19 idle; the fifth warpgroup hands
 // registers to the compute warps.
 #include <cuda.h>
@@ -49,8 +53,6 @@ namespace fa {
 namespace {
 
 constexpr int kThreads = 640;
-constexpr uint32_t kRegsCompute = 96;  // 4 x 128 x 96 + 128 x 96 = 640 x 96 (the launch pool)
-constexpr uint32_t kRegsOther = 96;
 constexpr int kTile = 128;  // keys per CTA and queries per step
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -107,6 +109,13 @@ constexpr int kComputeWarps = 16;
 template <int D>
 constexpr bool kQWatch = true;
 constexpr int kHeadGroup = 4;  // heads whose CTAs are interleaved in the grid
+// register split of the main kernel: d = 64 gives the compute warps 104 (their
+// item and tile state spills at 96), d = 128 keeps 96 / 96 (the issuing thread
+// spills at 64)
+template <int D>
+constexpr uint32_t kRegsCompute = (D == 64) ? 104 : 96;
+template <int D>
+constexpr uint32_t kRegsOther = (D == 64) ? 64 : 96;  // 4 x 128 x compute + 128 x other <= 640 x 96 (the launch pool)
 
 struct BwdArgs {
   float* Dpad;      // [BH, Npad] -D, 0 past N
@@ -126,6 +135,10 @@ struct BwdArgs {
   // last: the dense kernel's register allocation is sensitive to the layout.
   const int32_t* cu_seqlens;
   int total;
+  // persistent main kernel: work-item counter (zeroed by the preprocess), the
+  // number of items and the x extent of the item grid (key tiles x kHeadGroup)
+  unsigned* sched;
+  int n_items, gx;
 };
 
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
@@ -182,6 +195,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
       len = 0;
     }
   }
+  if (a.sched != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *a.sched = 0u;
   const bool live = have && r < len;
   float acc = 0.f;
   size_t row = 0;
@@ -230,18 +244,66 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ d
   reinterpret_cast<uint2*>(dQ)[i] = w;
 }
 
-// --------------------------------------------------------------------------- 2. main
-// kPacked selects the packed ragged-batch layout at compile time, so the dense
-// instantiation carries none of its indexing.
+// --------------------------------------------------------------------------- 2. main (persistent)
+// One CTA per SM takes work items -- the (key tile, batch*head) pairs of the
+// one-CTA-per-item grid, in the same order (longest causal work first within
+// each group of heads) -- from a counter in the workspace that the preprocess
+// zeroes, so each item's fixed costs overlap the previous one: the next item's
+// K/V, Q and dO loads and its first S and dP MMAs are issued while the compute
+// warps read out and store the previous item's dK and dV, and no CTA launch,
+// barrier set-up or TMEM allocation separates two items.  Barrier phases run on
+// across items: per-tile barriers by the CTA's running count of query tiles,
+// per-item ones (K/V, FINAL and their releases) by its count of items with work.
+enum : int {
+  BAR_SCHED_FULL = kNumBars,       // + slot (2): an item index published
+  BAR_SCHED_EMPTY = kNumBars + 2,  // + slot (2): every consumer has read it
+  BAR_KV_EMPTY = kNumBars + 4,     // the item's last MMA has read K and V
+  BAR_DKV_FREE = kNumBars + 5,     // the item's dK and dV read out of TMEM
+  kNumBarsP = kNumBars + 6,
+};
+constexpr int kOffTmemSlotP = kNumBarsP * 8;
+constexpr int kOffAbortP = kOffTmemSlotP + 4;
+constexpr int kOffSchedP = kOffAbortP + 4;  // two int item slots
+static_assert(kOffSchedP + 8 <= 256, "barrier block");
+
+// Work item -> (batch*head, key tile) and its query-tile range; false for an
+// item with nothing to do (a head past B*H, a key tile past its packed
+// sequence, or bad offsets, which the preprocess reports).
+template <bool kPacked>
+struct BwdItem {
+  int bh, b, j, head, tok0, N, kv_len, i0, nt;
+  __device__ __forceinline__ bool decode(const BwdArgs& a, int item) {
+    const int x = item % a.gx, y = item / a.gx;
+    bh = y * kHeadGroup + x % kHeadGroup;
+    if (bh >= a.BH) return false;
+    b = bh / a.H;
+    j = x / kHeadGroup;
+    head = bh % a.H;
+    int n_rows = a.N;
+    tok0 = 0;
+    if constexpr (kPacked) {
+      n_rows = packed_range(a, b, tok0);
+      if (n_rows < 0 || j * kTile >= n_rows) return false;
+    }
+    N = n_rows;
+    kv_len = N;
+    if (a.kv_lens != nullptr) kv_len = min(max(a.kv_lens[b], 0), N);
+    const bool live = j * kTile < kv_len;
+    i0 = a.causal ? j : 0;
+    const int nq = kPacked ? (N + kTile - 1) / kTile : a.nq;
+    nt = live ? (nq - i0) : 0;
+    return true;
+  }
+};
+
 template <int D, bool kPacked>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                    const __grid_constant__ CUtensorMap tmdQ, const BwdArgs a) {
+                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                       const __grid_constant__ CUtensorMap tmdQ, const BwdArgs a) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   {
-    // the tiles need a 1024-byte aligned base; refuse (and report) rather than overrun
     const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
     if (pad > static_cast<uint32_t>(C::kMaxPad)) {
       if (threadIdx.x == 0) atomicOr(a.status, kStatusLaunchBit);
@@ -252,35 +314,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sbase = smem_u32(smem);
   const uint32_t barbase = sbase + C::kOffBar;
   auto bar = [&](int i) -> uint32_t { return barbase + 8u * static_cast<uint32_t>(i); };
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffBar + kOffTmemSlot);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffBar + kOffAbort);
-
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffBar + kOffTmemSlotP);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffBar + kOffAbortP);
+  volatile int* sched_slot = reinterpret_cast<volatile int*>(smem + C::kOffBar + kOffSchedP);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // grid: y = group of kHeadGroup heads, x = key tile * kHeadGroup + head in
-  // group: the CTAs in flight share a few heads' Q, dO and dQ accumulator in L2,
-  // and within a group the key tiles with most query tiles (causal) start first
-  const int bh = blockIdx.y * kHeadGroup + static_cast<int>(blockIdx.x % kHeadGroup);
-  if (bh >= a.BH) return;
-  const int b = bh / a.H;
-  const int j = static_cast<int>(blockIdx.x / kHeadGroup);
-  const int head = bh % a.H;
-  // N = rows of this batch entry (dense) or sequence (packed); tok0 = its first token
-  int n_rows = a.N, tok0 = 0;
-  if constexpr (kPacked) {
-    n_rows = packed_range(a, b, tok0);
-    if (n_rows < 0 || j * kTile >= n_rows) return;  // bad offsets (reported by the preprocess) or past the end
-  }
-  const int N = n_rows;
-  int kv_len = N;
-  if (a.kv_lens != nullptr) kv_len = min(max(a.kv_lens[b], 0), N);
-  const bool live = j * kTile < kv_len;  // any unmasked key in this tile
-  const int i0 = a.causal ? j : 0;
-  const int nq = kPacked ? (N + kTile - 1) / kTile : a.nq;
-  const int nt = live ? (nq - i0) : 0;  // query tiles to visit
-  // TMA coordinates (y, z) of 128 rows from `row`: dense maps are (d, N, B*H)
-  // -> (row, bh), packed maps (d, H, total) -> (head, tok0 + row)
-#define BWD_CRD(row) (kPacked ? head : (row)), (kPacked ? tok0 + (row) : bh)
+#define BWD_CRD(row) (kPacked ? w.head : (row)), (kPacked ? w.tok0 + (row) : w.bh)
 
   if (threadIdx.x == 0) {
     mbar_init(bar(BAR_KV), 1);
@@ -289,6 +328,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(BAR_Q_EMPTY + s), 1);
       mbar_init(bar(BAR_SIDE_FULL + s), 1);
       mbar_init(bar(BAR_SIDE_EMPTY + s), kComputeWarps);
+      mbar_init(bar(BAR_SCHED_FULL + s), 1);
+      mbar_init(bar(BAR_SCHED_EMPTY + s), kComputeWarps + 1 + (kQWatch<D> ? 1 : 0));
     }
     mbar_init(bar(BAR_DO_FULL), 1);
     mbar_init(bar(BAR_DO_EMPTY), 1);
@@ -300,6 +341,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(BAR_DQ_READ), kComputeWarps);
     mbar_init(bar(BAR_FINAL), 1);
     mbar_init(bar(BAR_DRAIN), 1);
+    mbar_init(bar(BAR_KV_EMPTY), 1);
+    mbar_init(bar(BAR_DKV_FREE), kComputeWarps);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -312,74 +355,116 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const WaitCtx wc{abort_flag, a.status};
-  const size_t side_row = static_cast<size_t>(bh) * a.Npad;
+  // consumers read item k from slot k & 1 once SCHED_FULL has completed for it
+  auto take_item = [&](int k, int& item) -> bool {
+    if (!mbar_wait(bar(BAR_SCHED_FULL + (k & 1)), static_cast<uint32_t>(k >> 1) & 1u, wc)) return false;
+    item = sched_slot[k & 1];
+    return true;
+  };
 
   if (warp >= kComputeWarps) {
-    regs_dealloc<kRegsOther>();
+    regs_dealloc<kRegsOther<D>>();
     if (warp == kComputeWarps) {
-      // ---------------------------------------------------------- producer
-      if (lane == 0 && nt > 0) {
+      // ---------------------------------------------------------- producer (and scheduler)
+      if (lane == 0) {
         tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmdO);
-        mbar_arrive_expect_tx(bar(BAR_KV), 2 * C::kTileBytes);
-        for (int s = 0; s < C::kSub; ++s) {
-          tma_load_3d(sbase + C::kOffK + s * C::kSubBytes, &tmK, bar(BAR_KV), s * 64, BWD_CRD(j * kTile));
-          tma_load_3d(sbase + C::kOffV + s * C::kSubBytes, &tmV, bar(BAR_KV), s * 64, BWD_CRD(j * kTile));
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+        int cur = static_cast<int>(atomicAdd(a.sched, 1u));
+        sched_slot[0] = cur;
+        mbar_arrive(bar(BAR_SCHED_FULL + 0));
+        int gs = 0, kf = 0, side_issued = 0, q_issued = 0, o_issued = 0, kv_issued = 0;
+        bool ok = true;
+        for (int k = 0; ok; ++k) {
+          const int item = cur;
+          if (item >= a.n_items) break;
+          // publish item k + 1 in slot (k + 1) & 1 once every consumer has read
+          // item k - 1 from it
+          if (k >= 1 && !mbar_wait(bar(BAR_SCHED_EMPTY + ((k + 1) & 1)), static_cast<uint32_t>((k - 1) >> 1) & 1u,
+                                   wc)) {
+            ok = false;
+            break;
+          }
+          cur = static_cast<int>(atomicAdd(a.sched, 1u));
+          sched_slot[(k + 1) & 1] = cur;
+          mbar_arrive(bar(BAR_SCHED_FULL + ((k + 1) & 1)));
+          BwdItem<kPacked> w;
+          if (!w.decode(a, item) || w.nt == 0) continue;
+          const size_t side_row = static_cast<size_t>(w.bh) * a.Npad;
+          // K_j, V_j once the previous item's last MMA has read the old ones
+          if (kf > 0 && !mbar_wait(bar(BAR_KV_EMPTY), static_cast<uint32_t>(kf - 1) & 1u, wc)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar(BAR_KV), 2 * C::kTileBytes);
+          for (int s = 0; s < C::kSub; ++s) {
+            tma_load_3d(sbase + C::kOffK + s * C::kSubBytes, &tmK, bar(BAR_KV), s * 64, BWD_CRD(w.j * kTile));
+            tma_load_3d(sbase + C::kOffV + s * C::kSubBytes, &tmV, bar(BAR_KV), s * 64, BWD_CRD(w.j * kTile));
+          }
+          kv_issued = kf + 1;
+          for (int it = 0; it < w.nt; ++it) {
+            const int g = gs + it;
+            const int i = w.i0 + it;
+            const int sd = g & 1;
+            if (!mbar_wait(bar(BAR_SIDE_EMPTY + sd), ((g >> 1) & 1) ^ 1, wc)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(bar(BAR_SIDE_FULL + sd), 1024);
+            bulk_load(sbase + C::kOffSide + sd * 1024, a.Lpad + side_row + i * kTile, 512, bar(BAR_SIDE_FULL + sd));
+            bulk_load(sbase + C::kOffSide + sd * 1024 + 512, a.Dpad + side_row + i * kTile, 512,
+                      bar(BAR_SIDE_FULL + sd));
+            side_issued = g + 1;
+            if (!mbar_wait(bar(BAR_Q_EMPTY + sd), ((g >> 1) & 1) ^ 1, wc)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(bar(BAR_Q_FULL + sd), C::kTileBytes);
+            for (int s = 0; s < C::kSub; ++s)
+              tma_load_3d(sbase + C::kOffRing + sd * C::kTileBytes + s * C::kSubBytes, &tmQ, bar(BAR_Q_FULL + sd),
+                          s * 64, BWD_CRD(i * kTile));
+            q_issued = g + 1;
+            if (!mbar_wait(bar(BAR_DO_EMPTY), (g & 1) ^ 1, wc)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(bar(BAR_DO_FULL), C::kTileBytes);
+            for (int s = 0; s < C::kSub; ++s)
+              tma_load_3d(sbase + C::kOffRing + 2 * C::kTileBytes + s * C::kSubBytes, &tmdO, bar(BAR_DO_FULL),
+                          s * 64, BWD_CRD(i * kTile));
+            o_issued = g + 1;
+          }
+          gs += w.nt;
+          kf += 1;
         }
-        int side_issued = 0, q_issued = 0, o_issued = 0;
-        for (int it = 0; it < nt; ++it) {
-          const int i = i0 + it;
-          const int sd = it & 1;
-          if (!mbar_wait(bar(BAR_SIDE_EMPTY + sd), ((it >> 1) & 1) ^ 1, wc)) break;
-          mbar_arrive_expect_tx(bar(BAR_SIDE_FULL + sd), 1024);
-          bulk_load(sbase + C::kOffSide + sd * 1024, a.Lpad + side_row + i * kTile, 512, bar(BAR_SIDE_FULL + sd));
-          bulk_load(sbase + C::kOffSide + sd * 1024 + 512, a.Dpad + side_row + i * kTile, 512,
-                    bar(BAR_SIDE_FULL + sd));
-          side_issued = it + 1;
-          // Q_i into Q slot it % 2 (free once dK of tile it-2 is done)
-          if (!mbar_wait(bar(BAR_Q_EMPTY + sd), ((it >> 1) & 1) ^ 1, wc)) break;
-          mbar_arrive_expect_tx(bar(BAR_Q_FULL + sd), C::kTileBytes);
-          for (int s = 0; s < C::kSub; ++s)
-            tma_load_3d(sbase + C::kOffRing + sd * C::kTileBytes + s * C::kSubBytes, &tmQ, bar(BAR_Q_FULL + sd),
-                        s * 64, BWD_CRD(i * kTile));
-          q_issued = it + 1;
-          // dO_i into the dO slot (free once dV of tile it-1 is done)
-          if (!mbar_wait(bar(BAR_DO_EMPTY), (it & 1) ^ 1, wc)) break;
-          mbar_arrive_expect_tx(bar(BAR_DO_FULL), C::kTileBytes);
-          for (int s = 0; s < C::kSub; ++s)
-            tma_load_3d(sbase + C::kOffRing + 2 * C::kTileBytes + s * C::kSubBytes, &tmdO, bar(BAR_DO_FULL), s * 64,
-                        BWD_CRD(i * kTile));
-          o_issued = it + 1;
-        }
-        drain_wait(bar(BAR_KV), 0);
+        // every issued copy lands before the CTA can exit
+        if (kv_issued > 0) drain_wait(bar(BAR_KV), static_cast<uint32_t>(kv_issued - 1) & 1u);
         for (int s = 0; s < 2 && s < q_issued; ++s) {
-          const int it_last = s + 2 * ((q_issued - 1 - s) / 2);
-          drain_wait(bar(BAR_Q_FULL + s), (it_last >> 1) & 1);
+          const int last = s + 2 * ((q_issued - 1 - s) / 2);
+          drain_wait(bar(BAR_Q_FULL + s), (last >> 1) & 1);
         }
         for (int s = 0; s < 2 && s < side_issued; ++s) {
-          const int it_last = s + 2 * ((side_issued - 1 - s) / 2);
-          drain_wait(bar(BAR_SIDE_FULL + s), (it_last >> 1) & 1);
+          const int last = s + 2 * ((side_issued - 1 - s) / 2);
+          drain_wait(bar(BAR_SIDE_FULL + s), (last >> 1) & 1);
         }
         if (o_issued > 0) drain_wait(bar(BAR_DO_FULL), (o_issued - 1) & 1);
       }
     } else if (warp == kComputeWarps + 1) {
       // ---------------------------------------------------------- MMA issuer
-      if (lane == 0 && nt > 0) {
+      if (lane == 0) {
         constexpr uint32_t idSS = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
         constexpr uint32_t idKN = idesc_bf16_f32(128, D, false, true);     // dV (TS), dK
         const uint32_t sK = sbase + C::kOffK, sV = sbase + C::kOffV, sP = sbase + C::kOffP;
-        auto q_addr = [&](int it) { return sbase + C::kOffRing + (it & 1) * C::kTileBytes; };
+        auto q_addr = [&](int g) { return sbase + C::kOffRing + (g & 1) * C::kTileBytes; };
         const uint32_t aO = sbase + C::kOffRing + 2 * C::kTileBytes;
-        // Descriptors are built once per operand tile (K-major and MN-major views)
-        // and advanced by immediates, so the issuing thread keeps the tensor pipe fed.
         const uint64_t kK = sdesc_sw128(sK, 16, 1024), kV = sdesc_sw128(sV, 16, 1024);
         const uint64_t kP = sdesc_sw128(sP, 16, 1024), kO = sdesc_sw128(aO, 16, 1024);
         const uint64_t mK = sdesc_sw128(sK, C::kSubBytes, 1024), mP = sdesc_sw128(sP, C::kSubBytes, 1024);
         const uint64_t mO = sdesc_sw128(aO, C::kSubBytes, 1024);
         const uint64_t kQ0 = sdesc_sw128(q_addr(0), 16, 1024), mQ0 = sdesc_sw128(q_addr(0), C::kSubBytes, 1024);
-        auto kq = [&](int it) { return sdesc_advance(kQ0, (it & 1) * C::kTileBytes); };
-        auto mq = [&](int it) { return sdesc_advance(mQ0, (it & 1) * C::kTileBytes); };
-        // A and B both K-major, K extent = D (head dim)
+        auto kq = [&](int g) { return sdesc_advance(kQ0, (g & 1) * C::kTileBytes); };
+        auto mq = [&](int g) { return sdesc_advance(mQ0, (g & 1) * C::kTileBytes); };
         auto mma_kmajor_d = [&](uint32_t dcol, uint64_t da, uint64_t db) {
 #pragma unroll
           for (int k = 0; k < D / 16; ++k) {
@@ -387,332 +472,360 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_ss(tmem + dcol, sdesc_advance(da, off), sdesc_advance(db, off), idSS, k > 0 ? 1u : 0u);
           }
         };
-        bool ok = mbar_wait(bar(BAR_KV), 0, wc);
-        // prologue: S_0 and dP_0
-        if (ok) ok = mbar_wait(bar(BAR_Q_FULL + 0), 0, wc);
-        if (ok) {
+        int gs = 0, kf = 0;
+        bool ok = true;
+        for (int k = 0; ok; ++k) {
+          int item = 0;
+          if (!(ok = take_item(k, item))) break;
+          mbar_arrive(bar(BAR_SCHED_EMPTY + (k & 1)));
+          if (item >= a.n_items) break;
+          BwdItem<kPacked> w;
+          if (!w.decode(a, item) || w.nt == 0) continue;
+          const int nt = w.nt;
+          if (!(ok = mbar_wait(bar(BAR_KV), static_cast<uint32_t>(kf) & 1u, wc))) break;
+          // prologue: S_0 and dP_0; dP_0 overwrites the previous item's last dQ
+          if (!(ok = mbar_wait(bar(BAR_Q_FULL + (gs & 1)), (gs >> 1) & 1, wc))) break;
           tc_fence_after();
-          mma_kmajor_d(C::kColS, kK, kq(0));
+          mma_kmajor_d(C::kColS, kK, kq(gs));
           mma_commit(bar(BAR_S));
-          ok = mbar_wait(bar(BAR_DO_FULL), 0, wc);
-        }
-        if (ok) {
+          if (!(ok = mbar_wait(bar(BAR_DO_FULL), gs & 1, wc))) break;
+          if (gs > 0 && !(ok = mbar_wait(bar(BAR_DQ_READ), (gs - 1) & 1, wc))) break;
           tc_fence_after();
           mma_kmajor_d(C::kColDP, kV, kO);
           mma_commit(bar(BAR_DP));
-        }
-        for (int it = 0; ok && it < nt; ++it) {
-          const bool next = it + 1 < nt;
-          // dV_j += P^T dO_i  (P^T packed bf16 in TMEM: warpgroup h's 32 queries in cols 32h..32h+15)
-          if (!(ok = mbar_wait(bar(BAR_P), it & 1, wc))) break;
-          tc_fence_after();
-#pragma unroll
-          for (int k = 0; k < kTile / 16; ++k) {
-            const uint32_t acol = 32 * (k >> 1) + 8 * (k & 1);
-            mma_ts(tmem + C::kColDV, tmem + C::kColS + acol, sdesc_advance(mO, k * 2048), idKN,
-                   (it > 0 || k > 0) ? 1u : 0u);
-          }
-          mma_commit(bar(BAR_DO_EMPTY));
-          // dK_j += dS^T Q_i  and  dQ_i over the dP^T columns
-          if (!(ok = mbar_wait(bar(BAR_DS), it & 1, wc))) break;
-          tc_fence_after();
-          auto issue_dk = [&]() {
-#pragma unroll
-            for (int k = 0; k < kTile / 16; ++k) {
-              const uint32_t aoff = (k >> 2) * C::kSubBytes + (k & 3) * 32;
-              mma_ss(tmem + C::kColDK, sdesc_advance(kP, aoff), sdesc_advance(mq(it), k * 2048), idKN,
-                     (it > 0 || k > 0) ? 1u : 0u);
-            }
-          };
-          if constexpr (D == 128) {
-            // dQ_i first: it is the only reader of the shared-memory dS^T, so
-            // DQ_FULL also frees that buffer for dQ staging; then dK_i with
-            // A = dS^T from TMEM (packed bf16 next to P^T, as for dV)
-            constexpr uint32_t idQT = idesc_bf16_f32(128, 128, true, true);  // A = K^T, B = dS^T
-#pragma unroll
-            for (int k = 0; k < kTile / 16; ++k)
-              mma_ss(tmem + C::kColDQ, sdesc_advance(mK, k * 2048), sdesc_advance(mP, k * 2048), idQT,
-                     k > 0 ? 1u : 0u);
-            mma_commit(bar(BAR_DQ_FULL));
-#pragma unroll
-            for (int k = 0; k < kTile / 16; ++k) {
-              const uint32_t acol = 32 * (k >> 1) + 16 + 8 * (k & 1);
-              mma_ts(tmem + C::kColDK, tmem + C::kColS + acol, sdesc_advance(mq(it), k * 2048), idKN,
-                     (it > 0 || k > 0) ? 1u : 0u);
-            }
-          } else {
-            // d = 64: dQ first, so its read-out and staged reductions (own
-            // staging buffer, not the dS^T one) start while dK runs
-            constexpr uint32_t idNN = idesc_bf16_f32(128, D, true, true);  // A = dS, B = K
-#pragma unroll
-            for (int k = 0; k < kTile / 16; ++k)
-              mma_ss(tmem + C::kColDQ, sdesc_advance(mP, k * 2048), sdesc_advance(mK, k * 2048), idNN,
-                     k > 0 ? 1u : 0u);
-            mma_commit(bar(BAR_DQ_FULL));
-            issue_dk();
-          }
-          mma_commit(bar(BAR_Q_EMPTY + (it & 1)));
-          // S_{i+1} = K_j Q_{i+1}^T over the S^T columns (after dV has read P^T).
-          // Issued behind dK_i and dQ_i, so dQ_i reaches the compute warps (which
-          // read it out next) without waiting for S_{i+1}.
-          if (next) {
-            // with the watcher: Q_i+1 has landed, the DS(i) barrier waited for above
-            // completes only after the Q watcher has seen it
-            if (!kQWatch<D> &&
-                !(ok = mbar_wait(bar(BAR_Q_FULL + ((it + 1) & 1)), ((it + 1) >> 1) & 1, wc)))
+          for (int it = 0; ok && it < nt; ++it) {
+            const int g = gs + it;
+            const bool next = it + 1 < nt;
+            if (!(ok = mbar_wait(bar(BAR_P), g & 1, wc))) break;
+            // the item's first dV and dK overwrite the accumulators: the
+            // previous item's dK and dV must have been read out
+            if (it == 0 && kf > 0 && !(ok = mbar_wait(bar(BAR_DKV_FREE), static_cast<uint32_t>(kf - 1) & 1u, wc)))
               break;
-            if (!kQWatch<D>) tc_fence_after();
-            mma_kmajor_d(C::kColS, kK, kq(it + 1));
-            mma_commit(bar(BAR_S));
-          }
-          // dP_{i+1} = V_j dO_{i+1}^T over the dP^T columns (after dQ_i has been read out)
-          if (next) {
-            if (!(ok = mbar_wait(bar(BAR_DO_FULL), (it + 1) & 1, wc))) break;
-            if (!(ok = mbar_wait(bar(BAR_DQ_READ), it & 1, wc))) break;
             tc_fence_after();
-            mma_kmajor_d(C::kColDP, kV, kO);
-            mma_commit(bar(BAR_DP));
+#pragma unroll
+            for (int k2 = 0; k2 < kTile / 16; ++k2) {
+              const uint32_t acol = 32 * (k2 >> 1) + 8 * (k2 & 1);
+              mma_ts(tmem + C::kColDV, tmem + C::kColS + acol, sdesc_advance(mO, k2 * 2048), idKN,
+                     (it > 0 || k2 > 0) ? 1u : 0u);
+            }
+            mma_commit(bar(BAR_DO_EMPTY));
+            if (!(ok = mbar_wait(bar(BAR_DS), g & 1, wc))) break;
+            tc_fence_after();
+            if constexpr (D == 128) {
+              constexpr uint32_t idQT = idesc_bf16_f32(128, 128, true, true);  // A = K^T, B = dS^T
+#pragma unroll
+              for (int k2 = 0; k2 < kTile / 16; ++k2)
+                mma_ss(tmem + C::kColDQ, sdesc_advance(mK, k2 * 2048), sdesc_advance(mP, k2 * 2048), idQT,
+                       k2 > 0 ? 1u : 0u);
+              mma_commit(bar(BAR_DQ_FULL));
+#pragma unroll
+              for (int k2 = 0; k2 < kTile / 16; ++k2) {
+                const uint32_t acol = 32 * (k2 >> 1) + 16 + 8 * (k2 & 1);
+                mma_ts(tmem + C::kColDK, tmem + C::kColS + acol, sdesc_advance(mq(g), k2 * 2048), idKN,
+                       (it > 0 || k2 > 0) ? 1u : 0u);
+              }
+            } else {
+              constexpr uint32_t idNN = idesc_bf16_f32(128, D, true, true);  // A = dS, B = K
+#pragma unroll
+              for (int k2 = 0; k2 < kTile / 16; ++k2)
+                mma_ss(tmem + C::kColDQ, sdesc_advance(mP, k2 * 2048), sdesc_advance(mK, k2 * 2048), idNN,
+                       k2 > 0 ? 1u : 0u);
+              mma_commit(bar(BAR_DQ_FULL));
+#pragma unroll
+              for (int k2 = 0; k2 < kTile / 16; ++k2) {
+                const uint32_t aoff = (k2 >> 2) * C::kSubBytes + (k2 & 3) * 32;
+                mma_ss(tmem + C::kColDK, sdesc_advance(kP, aoff), sdesc_advance(mq(g), k2 * 2048), idKN,
+                       (it > 0 || k2 > 0) ? 1u : 0u);
+              }
+            }
+            mma_commit(bar(BAR_Q_EMPTY + (g & 1)));
+            if (next) {
+              // with the watcher, DS(g) completed only after Q of tile g + 1 landed
+              if (!kQWatch<D> && !(ok = mbar_wait(bar(BAR_Q_FULL + ((g + 1) & 1)), ((g + 1) >> 1) & 1, wc)))
+                break;
+              if (!kQWatch<D>) tc_fence_after();
+              mma_kmajor_d(C::kColS, kK, kq(g + 1));
+              mma_commit(bar(BAR_S));
+              if (!(ok = mbar_wait(bar(BAR_DO_FULL), (g + 1) & 1, wc))) break;
+              if (!(ok = mbar_wait(bar(BAR_DQ_READ), g & 1, wc))) break;
+              tc_fence_after();
+              mma_kmajor_d(C::kColDP, kV, kO);
+              mma_commit(bar(BAR_DP));
+            }
           }
+          if (!ok) break;
+          mma_commit(bar(BAR_FINAL));
+          mma_commit(bar(BAR_KV_EMPTY));
+          gs += nt;
+          kf += 1;
         }
-        if (ok) mma_commit(bar(BAR_FINAL));
         mma_commit(bar(BAR_DRAIN));
         drain_wait(bar(BAR_DRAIN), 0);
       }
     } else if (kQWatch<D> && warp == kComputeWarps + 2) {
       // ---------------------------------------------------------- Q watcher
-      // Adds one arrival to DS(i), after Q_i+1 has landed, so the issuing
-      // thread's wait for dS_i also covers the next query tile (one barrier
-      // wait fewer per tile on the issuing thread).  It arrives for tile i only
-      // once DS(i - 1) has completed, so it never arrives twice in one phase.
+      // One arrival on DS(g) per tile g, after Q of tile g + 1 (same item) has
+      // landed and only once DS(g - 1) has completed.
       if (lane == 0) {
-        for (int it = 0; it < nt; ++it) {
-          if (it > 0 && !mbar_wait(bar(BAR_DS), static_cast<uint32_t>(it - 1) & 1u, wc)) break;
-          if (it + 1 < nt &&
-              !mbar_wait(bar(BAR_Q_FULL + ((it + 1) & 1)), static_cast<uint32_t>((it + 1) >> 1) & 1u, wc))
-            break;
-          mbar_arrive(bar(BAR_DS));
+        int gs = 0;
+        bool ok = true;
+        for (int k = 0; ok; ++k) {
+          int item = 0;
+          if (!(ok = take_item(k, item))) break;
+          mbar_arrive(bar(BAR_SCHED_EMPTY + (k & 1)));
+          if (item >= a.n_items) break;
+          BwdItem<kPacked> w;
+          if (!w.decode(a, item) || w.nt == 0) continue;
+          for (int it = 0; it < w.nt; ++it) {
+            const int g = gs + it;
+            if (g > 0 && !(ok = mbar_wait(bar(BAR_DS), static_cast<uint32_t>(g - 1) & 1u, wc))) break;
+            if (it + 1 < w.nt &&
+                !(ok = mbar_wait(bar(BAR_Q_FULL + ((g + 1) & 1)), static_cast<uint32_t>((g + 1) >> 1) & 1u, wc)))
+              break;
+            mbar_arrive(bar(BAR_DS));
+          }
+          gs += w.nt;
         }
       }
     }
   } else {
-    regs_alloc<kRegsCompute>();
+    regs_alloc<kRegsCompute<D>>();
     // ------------------------------------------------------------ compute warps
     const int grp = warp >> 2;  // warpgroup: query columns 32 grp .. 32 grp + 31
     const int q4 = warp & 3;
     const int r = q4 * 32 + lane;  // key row (S^T, dP^T, dK, dV); head-dim row of dQ^T (d = 128)
     const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
-    const int key = j * kTile + r;
-    const bool key_ok = key < kv_len;
-    // this thread's 32 query columns of dS^T: sub-tile grp / 2, 16-byte chunks 4 (grp & 1) .. +3
     const uint32_t dsrow = sbase + C::kOffP + (grp >> 1) * C::kSubBytes + r * 128;
     const int swz = r & 7;
     const float2 sl2v = make_float2(a.scale_log2, a.scale_log2);
     const float2 scv = make_float2(a.scale, a.scale);
     bool aborted = false;
-    for (int it = 0; it < nt; ++it) {
-      const int i = i0 + it;
-      const int sd = it & 1;
-      if (!mbar_wait(bar(BAR_SIDE_FULL + sd), (it >> 1) & 1, wc) || !mbar_wait(bar(BAR_S), it & 1, wc)) {
+    int gs = 0, kf = 0;
+    for (int k = 0; !aborted; ++k) {
+      int item = 0;
+      if (!take_item(k, item)) {
         aborted = true;
         break;
       }
-      tc_fence_after();
-      const float* nlse2 = reinterpret_cast<const float*>(smem + C::kOffSide + sd * 1024) + grp * 32;  // -LSE2
-      const float* ndsum = nlse2 + 128;                                                                // -D
-      // ---- P^T = exp2(S^T * scale * log2e - LSE2[q]) on this thread's 32 query columns
-      float p[32];
-      {
-        uint32_t sv[32];
-        tmem_ld32(tmem + lane_off + C::kColS + grp * 32, sv);
-#pragma unroll
-        for (int c = 0; c < 32; c += 4) {
-          const float4 l4 = *reinterpret_cast<const float4*>(nlse2 + c);
-          const float2 x0 = ffma2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sl2v,
-                                  make_float2(l4.x, l4.y));
-          const float2 x1 = ffma2(make_float2(__uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3])), sl2v,
-                                  make_float2(l4.z, l4.w));
-          p[c + 0] = ex2_approx(x0.x);
-          p[c + 1] = ex2_approx(x0.y);
-          p[c + 2] = ex2_approx(x1.x);
-          p[c + 3] = ex2_approx(x1.y);
-        }
-        // causal: key > query is masked; queries past N have -LSE2 = -inf -> 0
-        const int qlo = i * kTile + grp * 32;
-        const int first_vis = a.causal ? (key - qlo) : 0;  // columns c >= first_vis are visible
-        if (!key_ok || first_vis > 0) {
-#pragma unroll
-          for (int c = 0; c < 32; ++c)
-            if (!key_ok || c < first_vis) p[c] = 0.f;
-        }
-      }
-      {
-        uint32_t pk[16];
-#pragma unroll
-        for (int c = 0; c < 16; ++c) pk[c] = pack_bf16x2(p[2 * c], p[2 * c + 1]);
-        tmem_st16(tmem + lane_off + C::kColS + grp * 32, pk);  // over this thread's own S^T columns
-        tmem_st_wait();
-      }
-      tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(BAR_P));
-      // ---- dS^T = scale * P^T * (dP^T - D[q])  -> shared memory (bf16)
-      if (!mbar_wait(bar(BAR_DP), it & 1, wc)) {
-        aborted = true;
-        break;
-      }
-      tc_fence_after();
-      {
-        uint32_t dv[32];
-        tmem_ld32(tmem + lane_off + C::kColDP + grp * 32, dv);
-#pragma unroll
-        for (int c = 0; c < 32; c += 4) {
-          const float4 d4 = *reinterpret_cast<const float4*>(ndsum + c);
-          const float2 g0 = fadd2(make_float2(__uint_as_float(dv[c]), __uint_as_float(dv[c + 1])), make_float2(d4.x, d4.y));
-          const float2 g1 =
-              fadd2(make_float2(__uint_as_float(dv[c + 2]), __uint_as_float(dv[c + 3])), make_float2(d4.z, d4.w));
-          const float2 ds0 = fmul2(fmul2(make_float2(p[c], p[c + 1]), scv), g0);
-          const float2 ds1 = fmul2(fmul2(make_float2(p[c + 2], p[c + 3]), scv), g1);
-          p[c] = ds0.x;
-          p[c + 1] = ds0.y;
-          p[c + 2] = ds1.x;
-          p[c + 3] = ds1.y;
+      if (lane == 0) mbar_arrive(bar(BAR_SCHED_EMPTY + (k & 1)));
+      if (item >= a.n_items) break;
+      BwdItem<kPacked> w;
+      if (!w.decode(a, item)) continue;
+      const int N = w.N;
+      const int nt = w.nt;
+      const int key = w.j * kTile + r;
+      const bool key_ok = key < w.kv_len;
+      for (int it = 0; it < nt; ++it) {
+        const int g = gs + it;
+        const int i = w.i0 + it;
+        const int sd = g & 1;
+        if (!mbar_wait(bar(BAR_SIDE_FULL + sd), (g >> 1) & 1, wc) || !mbar_wait(bar(BAR_S), g & 1, wc)) {
+          aborted = true;
+          break;
         }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(BAR_SIDE_EMPTY + sd));
-      if constexpr (D == 128) {
-        // the previous tile's dQ reductions of warpgroups 2-3 read staging inside
-        // the dS^T buffer: their reads must be done before any warp overwrites it
-        if (it > 0) {
-          if (grp >= 2 && q4 == 0 && lane == 0) bulk_wait_read_all();
-          named_barrier_sync(1, 32 * kComputeWarps);
+        tc_fence_after();
+        const float* nlse2 = reinterpret_cast<const float*>(smem + C::kOffSide + sd * 1024) + grp * 32;  // -LSE2
+        const float* ndsum = nlse2 + 128;                                                                // -D
+        // ---- P^T = exp2(S^T * scale * log2e - LSE2[q]) on this thread's 32 query columns
+        float p[32];
+        {
+          uint32_t sv[32];
+          tmem_ld32(tmem + lane_off + C::kColS + grp * 32, sv);
+#pragma unroll
+          for (int c = 0; c < 32; c += 4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(nlse2 + c);
+            const float2 x0 = ffma2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sl2v,
+                                    make_float2(l4.x, l4.y));
+            const float2 x1 = ffma2(make_float2(__uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3])), sl2v,
+                                    make_float2(l4.z, l4.w));
+            p[c + 0] = ex2_approx(x0.x);
+            p[c + 1] = ex2_approx(x0.y);
+            p[c + 2] = ex2_approx(x1.x);
+            p[c + 3] = ex2_approx(x1.y);
+          }
+          // causal: key > query is masked; queries past N have -LSE2 = -inf -> 0
+          const int qlo = i * kTile + grp * 32;
+          const int first_vis = a.causal ? (key - qlo) : 0;  // columns c >= first_vis are visible
+          if (!key_ok || first_vis > 0) {
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+              if (!key_ok || c < first_vis) p[c] = 0.f;
+          }
         }
-      }
-      // d = 128: dS^T also goes to TMEM, next to P^T (columns 32 grp + 16 ..):
-      // dK_i reads it from there, so only dQ_i reads the shared-memory copy
+        {
+          uint32_t pk[16];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t pk[8];
-#pragma unroll
-        for (int c = 0; c < 8; ++c) pk[c] = pack_bf16x2(p[16 * h + 2 * c], p[16 * h + 2 * c + 1]);
-        if constexpr (D == 128) tmem_st8(tmem + lane_off + C::kColS + grp * 32 + 16 + 8 * h, pk);
-#pragma unroll
-        for (int c8 = 0; c8 < 2; ++c8) {
-          const int chunk = 4 * (grp & 1) + 2 * h + c8;
-          st_shared_v4(dsrow + (((chunk ^ swz)) << 4), pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
+          for (int c = 0; c < 16; ++c) pk[c] = pack_bf16x2(p[2 * c], p[2 * c + 1]);
+          tmem_st16(tmem + lane_off + C::kColS + grp * 32, pk);  // over this thread's own S^T columns
+          tmem_st_wait();
         }
-      }
-      if constexpr (D == 128) tmem_st_wait();
-      fence_proxy_async_smem();
-      if constexpr (D == 128) tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(BAR_DS));
-      // ---- dQ_i += this tile's contribution
-      if (!mbar_wait(bar(BAR_DQ_FULL), it & 1, wc)) {
-        aborted = true;
-        break;
-      }
-      tc_fence_after();
-      if constexpr (D == 128) {
-        // dQ^T: lane = head-dim index r, columns = this warpgroup's 32 queries.
-        // The TMEM columns are released as soon as the values are in registers;
-        // the warpgroup then stages its 32 x 128 fp32 box (row-major) and one
-        // thread adds it into dQacc with a TMA reduction in L2.
-        uint32_t rr[32];
-        tmem_ld32(tmem + lane_off + C::kColDQ + grp * 32, rr);
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(BAR_DQ_READ));
-        const int q0 = i * kTile + grp * 32;
-        const uint32_t stg = (grp < 2) ? sbase + C::kOffStage + grp * 16384 : sbase + C::kOffP + (grp - 2) * 16384;
-        const bool leader = (q4 == 0 && lane == 0);
-        if (grp < 2 && it > 0 && leader) bulk_wait_read_all();  // this staging slot's previous reduction
-        named_barrier_sync(2 + grp, 128);
-#pragma unroll
-        for (int q = 0; q < 32; ++q) st_shared_f32(stg + q * 512 + r * 4, __uint_as_float(rr[q]));
-        fence_proxy_async_smem();
-        named_barrier_sync(2 + grp, 128);
-        if (leader && q0 < N) {
-          // rows past a packed sequence carry exact zeros (their P is 0)
-          tma_reduce_add_3d(&tmdQ, stg, 0, BWD_CRD(q0));
-          bulk_commit();
+        if (lane == 0) mbar_arrive(bar(BAR_P));
+        // ---- dS^T = scale * P^T * (dP^T - D[q])  -> shared memory (bf16)
+        if (!mbar_wait(bar(BAR_DP), g & 1, wc)) {
+          aborted = true;
+          break;
         }
-        continue;  // DQ_READ already signalled
+        tc_fence_after();
+        {
+          uint32_t dv[32];
+          tmem_ld32(tmem + lane_off + C::kColDP + grp * 32, dv);
+#pragma unroll
+          for (int c = 0; c < 32; c += 4) {
+            const float4 d4 = *reinterpret_cast<const float4*>(ndsum + c);
+            const float2 g0 =
+                fadd2(make_float2(__uint_as_float(dv[c]), __uint_as_float(dv[c + 1])), make_float2(d4.x, d4.y));
+            const float2 g1 = fadd2(make_float2(__uint_as_float(dv[c + 2]), __uint_as_float(dv[c + 3])),
+                                    make_float2(d4.z, d4.w));
+            const float2 ds0 = fmul2(fmul2(make_float2(p[c], p[c + 1]), scv), g0);
+            const float2 ds1 = fmul2(fmul2(make_float2(p[c + 2], p[c + 3]), scv), g1);
+            p[c] = ds0.x;
+            p[c + 1] = ds0.y;
+            p[c + 2] = ds1.x;
+            p[c + 3] = ds1.y;
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(BAR_SIDE_EMPTY + sd));
+        if constexpr (D == 128) {
+          // the previous tile's dQ reductions of warpgroups 2-3 read staging inside
+          // the dS^T buffer: their reads must be done before any warp overwrites it
+          if (g > 0) {
+            if (grp >= 2 && q4 == 0 && lane == 0) bulk_wait_read_all();
+            named_barrier_sync(1, 32 * kComputeWarps);
+          }
+        }
+        // d = 128: dS^T also goes to TMEM, next to P^T (columns 32 grp + 16 ..):
+        // dK_i reads it from there, so only dQ_i reads the shared-memory copy
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t pk[8];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) pk[c] = pack_bf16x2(p[16 * h + 2 * c], p[16 * h + 2 * c + 1]);
+          if constexpr (D == 128) tmem_st8(tmem + lane_off + C::kColS + grp * 32 + 16 + 8 * h, pk);
+#pragma unroll
+          for (int c8 = 0; c8 < 2; ++c8) {
+            const int chunk = 4 * (grp & 1) + 2 * h + c8;
+            st_shared_v4(dsrow + (((chunk ^ swz)) << 4), pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2],
+                         pk[4 * c8 + 3]);
+          }
+        }
+        if constexpr (D == 128) tmem_st_wait();
+        fence_proxy_async_smem();
+        if constexpr (D == 128) tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(BAR_DS));
+        // ---- dQ_i += this tile's contribution
+        if (!mbar_wait(bar(BAR_DQ_FULL), g & 1, wc)) {
+          aborted = true;
+          break;
+        }
+        tc_fence_after();
+        if constexpr (D == 128) {
+          // dQ^T: lane = head-dim index r, columns = this warpgroup's 32 queries;
+          // staged as one 32 x 128 fp32 box per warpgroup, added by a TMA reduction
+          uint32_t rr[32];
+          tmem_ld32(tmem + lane_off + C::kColDQ + grp * 32, rr);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(BAR_DQ_READ));
+          const int q0 = i * kTile + grp * 32;
+          const uint32_t stg =
+              (grp < 2) ? sbase + C::kOffStage + grp * 16384 : sbase + C::kOffP + (grp - 2) * 16384;
+          const bool leader = (q4 == 0 && lane == 0);
+          if (grp < 2 && g > 0 && leader) bulk_wait_read_all();  // this staging slot's previous reduction
+          named_barrier_sync(2 + grp, 128);
+#pragma unroll
+          for (int q = 0; q < 32; ++q) st_shared_f32(stg + q * 512 + r * 4, __uint_as_float(rr[q]));
+          fence_proxy_async_smem();
+          named_barrier_sync(2 + grp, 128);
+          if (leader && q0 < N) {
+            tma_reduce_add_3d(&tmdQ, stg, 0, BWD_CRD(q0));
+            bulk_commit();
+          }
+        } else {
+          // dQ: lane = query row, columns = this warpgroup's 16 head-dim entries;
+          // the four warps of a TMEM lane quarter stage 32 queries x 64 fp32 as
+          // two 128-byte-swizzled halves, added by two TMA reductions
+          uint32_t rr[16];
+          tmem_ld16(tmem + lane_off + C::kColDQ + grp * 16, rr);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(BAR_DQ_READ));
+          const uint32_t stg = sbase + C::kOffStage + q4 * 8192;
+          const bool leader = (grp == 0 && lane == 0);
+          if (g > 0 && leader) bulk_wait_read_all();  // this staging box's previous reductions
+          named_barrier_sync(2 + q4, 128);
+          const uint32_t srow = stg + (grp >> 1) * 4096 + lane * 128;
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            st_shared_v4(srow + ((((grp & 1) * 4 + c) ^ (lane & 7)) << 4), rr[4 * c], rr[4 * c + 1],
+                         rr[4 * c + 2], rr[4 * c + 3]);
+          fence_proxy_async_smem();
+          named_barrier_sync(2 + q4, 128);
+          const int q0 = i * kTile + q4 * 32;
+          if (leader && q0 < N) {
+            tma_reduce_add_3d(&tmdQ, stg, 0, BWD_CRD(q0));
+            tma_reduce_add_3d(&tmdQ, stg + 4096, 32, BWD_CRD(q0));
+            bulk_commit();
+          }
+        }
+      }
+      if (aborted) break;
+      // ---- epilogue: dV_j, dK_j rows (thread = key row r), head-dim columns of
+      // this warpgroup; TMEM is released for the next item before the stores
+      const bool have = nt > 0;
+      if (have && !mbar_wait(bar(BAR_FINAL), static_cast<uint32_t>(kf) & 1u, wc)) {
+        aborted = true;
+        break;
+      }
+      tc_fence_after();
+      constexpr int kCols = D / 4;
+      // packed bf16 pairs of this thread's dV and dK columns
+      uint32_t pv[kCols / 2], pk2[kCols / 2];
+      if (have) {
+        {
+          uint32_t rr[kCols];
+          if constexpr (kCols == 32) tmem_ld32(tmem + lane_off + C::kColDV + grp * kCols, rr);
+          else tmem_ld16(tmem + lane_off + C::kColDV + grp * kCols, rr);
+#pragma unroll
+          for (int c = 0; c < kCols / 2; ++c) pv[c] = pack_bf16x2(__uint_as_float(rr[2 * c]), __uint_as_float(rr[2 * c + 1]));
+        }
+        {
+          uint32_t rr[kCols];
+          if constexpr (kCols == 32) tmem_ld32(tmem + lane_off + C::kColDK + grp * kCols, rr);
+          else tmem_ld16(tmem + lane_off + C::kColDK + grp * kCols, rr);
+#pragma unroll
+          for (int c = 0; c < kCols / 2; ++c) pk2[c] = pack_bf16x2(__uint_as_float(rr[2 * c]), __uint_as_float(rr[2 * c + 1]));
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(BAR_DKV_FREE));
       } else {
-        // dQ: lane = query row r, columns = this warpgroup's 16 head-dim
-        // entries.  The four warps of one TMEM lane quarter (q4, one per
-        // warpgroup) stage their 32 queries x 64 fp32 in shared memory, two
-        // 128-byte-swizzled halves of 32 columns (conflict-free 16-byte
-        // stores), and one of them adds the box into dQacc with two TMA
-        // reductions in L2.
-        uint32_t rr[16];
-        tmem_ld16(tmem + lane_off + C::kColDQ + grp * 16, rr);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(BAR_DQ_READ));
-        const uint32_t stg = sbase + C::kOffStage + q4 * 8192;
-        const bool leader = (grp == 0 && lane == 0);
-        if (it > 0 && leader) bulk_wait_read_all();  // this staging box's previous reductions
-        named_barrier_sync(2 + q4, 128);
-        const uint32_t srow = stg + (grp >> 1) * 4096 + lane * 128;
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-          st_shared_v4(srow + ((((grp & 1) * 4 + c) ^ (lane & 7)) << 4), rr[4 * c], rr[4 * c + 1], rr[4 * c + 2],
-                       rr[4 * c + 3]);
-        fence_proxy_async_smem();
-        named_barrier_sync(2 + q4, 128);
-        const int q0 = i * kTile + q4 * 32;
-        if (leader && q0 < N) {
-          // rows past a packed sequence carry exact zeros (their P is 0)
-          tma_reduce_add_3d(&tmdQ, stg, 0, BWD_CRD(q0));
-          tma_reduce_add_3d(&tmdQ, stg + 4096, 32, BWD_CRD(q0));
-          bulk_commit();
-        }
-        continue;  // DQ_READ already signalled
+        for (int c = 0; c < kCols / 2; ++c) pv[c] = pk2[c] = 0u;
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(BAR_DQ_READ));
+      if (key < N) {
+        const size_t krow =
+            kPacked ? static_cast<size_t>(w.tok0 + key) * a.H + w.head : static_cast<size_t>(w.bh) * N + key;
+        const size_t rowoff = (krow * D + grp * kCols) * 2;
+        uint4* dv_dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.dV) + rowoff);
+        uint4* dk_dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.dK) + rowoff);
+#pragma unroll
+        for (int q = 0; q < kCols / 8; ++q) {
+          dv_dst[q] = make_uint4(pv[4 * q], pv[4 * q + 1], pv[4 * q + 2], pv[4 * q + 3]);
+          dk_dst[q] = make_uint4(pk2[4 * q], pk2[4 * q + 1], pk2[4 * q + 2], pk2[4 * q + 3]);
+        }
+      }
+      if (have) {
+        gs += nt;
+        kf += 1;
+      }
     }
     if (lane == 0) bulk_wait_read_all();  // staging must outlive the reductions' reads
-    // ---- epilogue: dV_j, dK_j rows (thread = key row r), head-dim columns of this warpgroup
-    if (!aborted) {
-      const bool have = nt > 0;
-      if (have && !mbar_wait(bar(BAR_FINAL), 0, wc)) aborted = true;
-      if (!aborted) {
-        tc_fence_after();
-        constexpr int kCols = D / 4;
-        const bool in_range = key < N;
-        const size_t krow = kPacked ? static_cast<size_t>(tok0 + key) * a.H + head : static_cast<size_t>(bh) * N + key;
-        const size_t rowoff = krow * D + grp * kCols;
-#pragma unroll
-        for (int which = 0; which < 2; ++which) {
-          uint8_t* out = static_cast<uint8_t*>(which ? a.dK : a.dV) + rowoff * 2;
-          const uint32_t col = (which ? C::kColDK : C::kColDV) + grp * kCols;
-          uint32_t rr[kCols];
-          if (have) {
-            if constexpr (kCols == 32) {
-              tmem_ld32(tmem + lane_off + col, rr);
-            } else {
-              tmem_ld16(tmem + lane_off + col, rr);
-            }
-          } else {
-#pragma unroll
-            for (int c = 0; c < kCols; ++c) rr[c] = 0u;
-          }
-          if (in_range) {
-            uint4* dst = reinterpret_cast<uint4*>(out);
-#pragma unroll
-            for (int q = 0; q < kCols / 8; ++q)
-              dst[q] = make_uint4(pack_bf16x2(__uint_as_float(rr[8 * q + 0]), __uint_as_float(rr[8 * q + 1])),
-                                  pack_bf16x2(__uint_as_float(rr[8 * q + 2]), __uint_as_float(rr[8 * q + 3])),
-                                  pack_bf16x2(__uint_as_float(rr[8 * q + 4]), __uint_as_float(rr[8 * q + 5])),
-                                  pack_bf16x2(__uint_as_float(rr[8 * q + 6]), __uint_as_float(rr[8 * q + 7])));
-          }
-        }
-      }
-    }
   }
 
   tc_fence_before();
@@ -723,6 +836,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 #undef BWD_CRD
+
+// The scheduler counter of the persistent kernel: 256 bytes after the fp32 dQ
+// accumulator (elements floats) in the workspace, whose -D and -LSE2 rows take
+// `side` bytes each.
+inline unsigned* bwd_sched_ptr(void* workspace, size_t side, size_t elements) {
+  const size_t acc = (elements * sizeof(float) + 255) & ~static_cast<size_t>(255);
+  return reinterpret_cast<unsigned*>(static_cast<uint8_t*>(workspace) + 2 * side + acc);
+}
 
 template <int D>
 fa_status bwd_launch_d(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
@@ -767,14 +888,20 @@ fa_status bwd_launch_d(const void* Q, const void* K, const void* V, const void* 
   if (!(D == 128 ? encode_f32_tmap(&tdq, a.dQacc, 3, dims, qstrides, qbox)
                  : encode_f32_sw128_tmap(&tdq, a.dQacc, 3, dims, qstrides, qbox)))
     return FA_ERR_CUDA;
+  // work items: (key tile, batch*head) pairs, key tile * kHeadGroup + head in
+  // group fastest, then the group of heads
+  a.gx = nq * kHeadGroup;
+  a.n_items = a.gx * ceil_div(BH, kHeadGroup);
+  a.sched = bwd_sched_ptr(workspace, side, static_cast<size_t>(BH) * N * D);
   if (!set_smem_limit(reinterpret_cast<const void*>(&bwd_main_kernel<D, false>), C::kSmemBytes))
     return FA_ERR_CUDA;
   const long long pre_rows = static_cast<long long>(BH) * Npad;
   bwd_pre_kernel<D><<<static_cast<unsigned>((pre_rows + 8 * (256 / D) - 1) / (8 * (256 / D))), 256, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), LSE, a, BH);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
-  const dim3 grid(nq * kHeadGroup, ceil_div(BH, kHeadGroup));
-  bwd_main_kernel<D, false><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, a);
+  // one persistent CTA per SM (fewer when there are fewer work items)
+  const int ctas = min(a.n_items, max(sm_count(), 1));
+  bwd_main_kernel<D, false><<<ctas, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, a);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   const long long n4 = static_cast<long long>(BH) * N * D / 4;
   bwd_dq_kernel<<<static_cast<unsigned>((n4 + 255) / 256), 256, 0, stream>>>(a.dQacc,
@@ -824,14 +951,20 @@ fa_status bwd_varlen_launch_d(const void* Q, const void* K, const void* V, const
   if (!(D == 128 ? encode_f32_tmap(&tdq, a.dQacc, 3, dims, qstrides, qbox)
                  : encode_f32_sw128_tmap(&tdq, a.dQacc, 3, dims, qstrides, qbox)))
     return FA_ERR_CUDA;
+  // work items: (key tile, batch*head) pairs, key tile * kHeadGroup + head in
+  // group fastest, then the group of heads
+  a.gx = nq * kHeadGroup;
+  a.n_items = a.gx * ceil_div(BH, kHeadGroup);
+  a.sched = bwd_sched_ptr(workspace, side, static_cast<size_t>(total) * H * D);
   if (!set_smem_limit(reinterpret_cast<const void*>(&bwd_main_kernel<D, true>), C::kSmemBytes))
     return FA_ERR_CUDA;
   const long long pre_rows = static_cast<long long>(BH) * Npad;
   bwd_pre_kernel<D><<<static_cast<unsigned>((pre_rows + 8 * (256 / D) - 1) / (8 * (256 / D))), 256, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), LSE, a, BH);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
-  const dim3 grid(nq * kHeadGroup, ceil_div(BH, kHeadGroup));
-  bwd_main_kernel<D, true><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, a);
+  // one persistent CTA per SM (fewer when there are fewer work items)
+  const int ctas = min(a.n_items, max(sm_count(), 1));
+  bwd_main_kernel<D, true><<<ctas, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, a);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   const long long n4 = static_cast<long long>(total) * H * D / 4;
   bwd_dq_kernel<<<static_cast<unsigned>((n4 + 255) / 256), 256, 0, stream>>>(a.dQacc,

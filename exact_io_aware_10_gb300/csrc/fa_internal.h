@@ -66,6 +66,8 @@ fa_status decode_prepare();
 // Raises `func`'s dynamic shared-memory limit to `bytes` on the current device,
 // once per (kernel, device); false on failure.
 bool set_smem_limit(const void* func, int bytes);
+// Number of SMs of the current device (0 if CUDA fails), looked up once per device.
+int sm_count();
 // Loads the tensor-map encoder entry point if needed; false if unavailable.
 bool encode_init();
 // Argument checks shared by every paged-decode entry point (with and without
