@@ -93,9 +93,9 @@ TRAFFIC_RECORD = {
             "bytes": {"N16384": 288711936 + 47219712, "N65536": 1163000064 + 249906688}},
     "bwd": {"kernel": "bwd_pre_kernel<128> + bwd_main_kernel<128> + bwd_dq_kernel",
             "source": "exact_io_aware_10_gb300/csrc/fa_bwd.cu",
-            "sha256": "1204a888e0cf664a1638112fef28cc6841caf1319cad7421019c937ea615a100",
-            "bytes": {"N16384_main": 407740672 + 221462272, "N16384_pre": 135282176 + 86865152,
-                      "N16384_dq": 134232320 + 35462656}},
+            "sha256": "0d2e43ce607cffe912a8e04307754b8872aecf933d6592a702c1350d19a1d6bd",
+            "bytes": {"N16384_main": 406574080 + 218599168, "N16384_pre": 135284480 + 87345664,
+                      "N16384_dq": 134242816 + 35207424}},
     "decode": {"kernel": "decode_split_kernel<128> + decode_combine_kernel<128>",
                "source": "exact_io_aware_10_gb300/csrc/fa_decode.cu",
                "sha256": "46f760001ee8943807a4193b3045b0ff836a7f745d5d58ca79693015f36c3d05",
