@@ -159,9 +159,9 @@ int fa_paged_prefill(const void* q, const void* k_cache, const void* v_cache, co
 
 /*
  * Bytes of device workspace fa_bwd needs: two fp32 [B, H, Npad] row buffers
- * (D = rowsum(dO * O) and LSE in log2 units; Npad = N rounded up to 128) and
- * an fp32 [B, H, N, d] dQ accumulator, each rounded up to 256 bytes.
- * 0 on invalid sizes.
+ * (D = rowsum(dO * O) and LSE in log2 units; Npad = N rounded up to 128), an
+ * fp32 [B, H, N, d] dQ accumulator, each rounded up to 256 bytes, and 256
+ * bytes for the main kernel's work-item counter.  0 on invalid sizes.
  */
 size_t fa_bwd_workspace_size(int B, int H, int N, int d);
 
@@ -177,7 +177,8 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d);
  *   dQ, dK, dV     : [B, H, N, d] bf16, written.  Padded keys get dK = dV = 0.
  *   kv_lens        : as in fa_fwd_ex, may be NULL.
  *   workspace      : device buffer of at least fa_bwd_workspace_size() bytes,
- *                    256-byte aligned; contents on entry are ignored.
+ *                    256-byte aligned; contents on entry are ignored.  Two
+ *                    calls that overlap on the GPU must not share it.
  * Errors: FA_ERR_INVALID_ARG (including ws_bytes too small),
  * FA_ERR_UNSUPPORTED, FA_ERR_CUDA.
  */
@@ -187,8 +188,9 @@ int fa_bwd(const void* Q, const void* K, const void* V, const void* O, const voi
 
 /*
  * Bytes of device workspace fa_bwd_varlen needs: two fp32 row buffers of
- * num_sequences x H x Npad (Npad = max_seqlen rounded up to 128) and an fp32
- * [total, H, d] dQ accumulator, each rounded up to 256 bytes.  0 on invalid sizes.
+ * num_sequences x H x Npad (Npad = max_seqlen rounded up to 128), an fp32
+ * [total, H, d] dQ accumulator, each rounded up to 256 bytes, and 256 bytes for
+ * the main kernel's work-item counter.  0 on invalid sizes.
  */
 size_t fa_bwd_varlen_workspace_size(int num_seqs, int total, int max_seqlen, int H, int d);
 

@@ -152,7 +152,8 @@ def test_varlen_backward_argument_validation(so):
     p = _fake(11)
     s = ctypes.c_void_p(0)
     need = so.fa_bwd_varlen_workspace_size(2, 100, 64, 4, 128)
-    assert need == 2 * (((2 * 4 * 128 * 4) + 255) // 256 * 256) + (100 * 4 * 128 * 4 + 255) // 256 * 256
+    # -D and -LSE2 rows, the fp32 dQ accumulator, 256 bytes for the work counter
+    assert need == 2 * (((2 * 4 * 128 * 4) + 255) // 256 * 256) + (100 * 4 * 128 * 4 + 255) // 256 * 256 + 256
     assert so.fa_bwd_varlen_workspace_size(0, 100, 64, 4, 128) == 0
     f = so.fa_bwd_varlen
 
@@ -174,7 +175,7 @@ def test_backward_argument_validation(so):
     s = ctypes.c_void_p(0)
     need = so.fa_bwd_workspace_size(2, 3, 100, 64)
     bh, npad = 2 * 3, 128
-    assert need == 2 * ((bh * npad * 4 + 255) // 256) * 256 + ((bh * 100 * 64 * 4 + 255) // 256) * 256
+    assert need == 2 * ((bh * npad * 4 + 255) // 256) * 256 + ((bh * 100 * 64 * 4 + 255) // 256) * 256 + 256
     assert so.fa_bwd_workspace_size(0, 1, 1, 64) == 0
     assert so.fa_bwd(*ptrs[:9], 2, 3, 100, 64, 0, 0.1, None, ptrs[9], need - 1, s) == fl.FA_ERR_INVALID_ARG
     assert so.fa_bwd(*ptrs[:9], 2, 3, 100, 64, 0, 0.1, None, None, need, s) == fl.FA_ERR_INVALID_ARG
