@@ -20,6 +20,10 @@ BUILD_DIR = os.path.join(PKG, "_build")
 LIB_DIR = os.path.join(PKG, "lib")
 LIB_NAME = "libfa_gb300.so"
 LIB_PATH = os.path.join(LIB_DIR, LIB_NAME)
+# the same sources built with FA_DEBUG: device bounds checks on every global
+# access the kernels' threads issue (load it with FA_GB300_LIB=<this path>)
+DEBUG_BUILD_DIR = os.path.join(PKG, "_build_debug")
+DEBUG_LIB_PATH = os.path.join(LIB_DIR, "libfa_gb300_debug.so")
 
 SOURCES = ["fa_api.cu", "fa_fwd.cu", "fa_bwd.cu", "fa_decode.cu", "fa_graph.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -41,10 +45,10 @@ def _deps():
     return files
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB_PATH):
+def _stale(path) -> bool:
+    if not os.path.exists(path):
         return True
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(path)
     return any(os.path.getmtime(f) > t for f in _deps())
 
 
@@ -53,19 +57,24 @@ def _run(cmd):
     return p.returncode, p.stdout
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False) -> str:
-    """Compile every translation unit for sm_103a and link the shared library.
-    Returns the library path; raises RuntimeError with the compiler output on
-    failure."""
-    if not force and not _stale():
-        return LIB_PATH
-    os.makedirs(BUILD_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False, debug: bool = False) -> str:
+    """Compile every translation unit for sm_103a and link the shared library
+    (``debug``: the FA_DEBUG variant with device bounds checks, a separate
+    library).  Returns the library path; raises RuntimeError with the
+    compiler output on failure."""
+    lib_path = DEBUG_LIB_PATH if debug else LIB_PATH
+    build_dir = DEBUG_BUILD_DIR if debug else BUILD_DIR
+    if not force and not _stale(lib_path):
+        return lib_path
+    os.makedirs(build_dir, exist_ok=True)
     os.makedirs(LIB_DIR, exist_ok=True)
     nvcc = nvcc_path()
     extra = ["-Xptxas", "-v"] if ptxas_verbose else []
+    if debug:
+        extra.append("-DFA_DEBUG")
     jobs = []
     for src in SOURCES:
-        obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
+        obj = os.path.join(build_dir, src.replace(".cu", ".o"))
         jobs.append((src, [nvcc, *ARCH, *NVCC_FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj], obj))
     with ThreadPoolExecutor(max_workers=len(jobs)) as ex:
         results = list(ex.map(lambda j: (j[0], *_run(j[1])), jobs))
@@ -75,17 +84,18 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
             log.append(f"--- {src}\n{out}")
         if rc != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{out}")
-    tmp = LIB_PATH + ".tmp"
+    tmp = lib_path + ".tmp"
     rc, out = _run([nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp,
                     *[j[2] for j in jobs], "-ldl"])
     if rc != 0:
         raise RuntimeError(f"link failed:\n{out}")
-    os.replace(tmp, LIB_PATH)
+    os.replace(tmp, lib_path)
     if log:
         sys.stderr.write("\n".join(log) + "\n")
-    return LIB_PATH
+    return lib_path
 
 
 if __name__ == "__main__":
     force = "--force" in sys.argv
-    print(build(force=force, verbose="-v" in sys.argv, ptxas_verbose="--ptxas" in sys.argv))
+    print(build(force=force, verbose="-v" in sys.argv, ptxas_verbose="--ptxas" in sys.argv,
+                debug="--debug" in sys.argv))

@@ -145,6 +145,15 @@ bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, CUtensorMapSwizzle
 }
 }  // namespace
 
+// Lane 0 asks the bounds guard about element 3 of a 3-element extent; no
+// memory is touched either way.
+__global__ void selftest_bounds_kernel(unsigned* status) {
+  if (threadIdx.x == 0) {
+    volatile bool ok = FA_IN_BOUNDS(3, 3, status);
+    (void)ok;
+  }
+}
+
 // One CTA waits on an mbarrier that nothing ever completes; the bounded wait
 // must give up after `timeout_ns`, latch the timeout bit and let the kernel end.
 __global__ void selftest_wait_kernel(unsigned* status, unsigned long long timeout_ns) {
@@ -195,11 +204,12 @@ const char* fa_status_string(int status) {
     case FA_ERR_CUDA: return "FA_ERR_CUDA";
     case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
     case FA_ERR_BAD_BLOCK_TABLE: return "FA_ERR_BAD_BLOCK_TABLE";
+    case FA_ERR_OUT_OF_BOUNDS: return "FA_ERR_OUT_OF_BOUNDS";
     default: return "FA_ERR_UNKNOWN";
   }
 }
 
-int fa_version(void) { return 105; }
+int fa_version(void) { return 106; }
 
 int fa_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d, int causal,
               float scale, const int32_t* kv_lens, void* stream) {
@@ -340,6 +350,21 @@ int fa_paged_decode(const void* q, const void* k_cache, const void* v_cache, con
                            num_blocks, S, scale, workspace, static_cast<cudaStream_t>(stream));
 }
 
+int fa_debug_build(void) {
+#ifdef FA_DEBUG
+  return 1;
+#else
+  return 0;
+#endif
+}
+
+int fa_selftest_bounds(void* stream) {
+  unsigned* status = fa::device_status_ptr();
+  if (status == nullptr) return FA_ERR_CUDA;
+  fa::selftest_bounds_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(status);
+  return fa::launch_status();
+}
+
 int fa_selftest_wait_timeout(unsigned timeout_us, void* stream) {
   if (timeout_us == 0 || timeout_us > 1000000u) return FA_ERR_INVALID_ARG;
   unsigned* status = fa::device_status_ptr();
@@ -357,6 +382,7 @@ int fa_get_device_status(void* stream) {
     const unsigned zero = 0;
     if (cudaMemcpyToSymbol(fa::g_fa_status, &zero, sizeof(zero)) != cudaSuccess) return FA_ERR_CUDA;
   }
+  if (v & fa::kStatusBoundsBit) return FA_ERR_OUT_OF_BOUNDS;
   if (v & fa::kStatusLaunchBit) return FA_ERR_CUDA;
   if (v & fa::kStatusBadArgBit) return FA_ERR_INVALID_ARG;
   if (v & fa::kStatusTimeoutBit) return FA_ERR_TIMEOUT;

@@ -139,6 +139,13 @@ struct BwdArgs {
   // number of items and the x extent of the item grid (key tiles x kHeadGroup)
   unsigned* sched;
   int n_items, gx;
+#ifdef FA_DEBUG
+  // extents for the debug bounds checks: batch entries (sequences), rows of
+  // Q/K/V/O/dO/dQ/dK/dV and dQacc (D elements each) and of LSE, elements of
+  // each of the -D and -LSE2 row buffers
+  int dbg_nb;
+  long long dbg_rows, dbg_side;
+#endif
 };
 
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
@@ -158,6 +165,8 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 // be non-decreasing, start at 0, end at total, and no sequence may be longer
 // than N (the longest sequence the launch was sized for); otherwise len = -1.
 __device__ __forceinline__ int packed_range(const BwdArgs& a, int b, int& tok0) {
+  tok0 = 0;
+  if (!FA_IN_BOUNDS(b + 1, a.dbg_nb + 1, a.status)) return -1;
   tok0 = a.cu_seqlens[b];
   const int tok1 = a.cu_seqlens[b + 1];
   const int nseq = a.BH / a.H;
@@ -196,9 +205,14 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
     }
   }
   if (a.sched != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *a.sched = 0u;
-  const bool live = have && r < len;
+  bool live = have && r < len;
   float acc = 0.f;
   size_t row = 0;
+  if (live) {
+    const size_t row0 = a.cu_seqlens != nullptr ? static_cast<size_t>(tok0 + r) * a.H + bh % a.H
+                                                : static_cast<size_t>(bh) * a.N + r;
+    live = FA_IN_BOUNDS(static_cast<long long>(row0), a.dbg_rows, a.status);
+  }
   if (live) {
     // [B, H, N, D] rows, or [total, H, D] rows when packed (LSE [H, total])
     row = a.cu_seqlens != nullptr ? static_cast<size_t>(tok0 + r) * a.H + bh % a.H
@@ -224,7 +238,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
     if (live) {
       const size_t lrow = a.cu_seqlens != nullptr ? static_cast<size_t>(bh % a.H) * a.total + tok0 + r : row;
       a.Dpad[gr] = -acc;
-      a.Lpad[gr] = -LSE[lrow] * kLog2e;
+      a.Lpad[gr] = FA_IN_BOUNDS(static_cast<long long>(lrow), a.dbg_rows, a.status) ? -LSE[lrow] * kLog2e : 0.f;
     } else {
       a.Dpad[gr] = 0.f;
       a.Lpad[gr] = -INFINITY;
@@ -287,7 +301,7 @@ struct BwdItem {
     }
     N = n_rows;
     kv_len = N;
-    if (a.kv_lens != nullptr) kv_len = min(max(a.kv_lens[b], 0), N);
+    if (a.kv_lens != nullptr && FA_IN_BOUNDS(b, a.dbg_nb, a.status)) kv_len = min(max(a.kv_lens[b], 0), N);
     const bool live = j * kTile < kv_len;
     i0 = a.causal ? j : 0;
     const int nq = kPacked ? (N + kTile - 1) / kTile : a.nq;
@@ -411,10 +425,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(bar(BAR_SIDE_FULL + sd), 1024);
-            bulk_load(sbase + C::kOffSide + sd * 1024, a.Lpad + side_row + i * kTile, 512, bar(BAR_SIDE_FULL + sd));
-            bulk_load(sbase + C::kOffSide + sd * 1024 + 512, a.Dpad + side_row + i * kTile, 512,
-                      bar(BAR_SIDE_FULL + sd));
+            if (FA_IN_BOUNDS(static_cast<long long>(side_row) + i * kTile + kTile - 1, a.dbg_side, a.status)) {
+              mbar_arrive_expect_tx(bar(BAR_SIDE_FULL + sd), 1024);
+              bulk_load(sbase + C::kOffSide + sd * 1024, a.Lpad + side_row + i * kTile, 512,
+                        bar(BAR_SIDE_FULL + sd));
+              bulk_load(sbase + C::kOffSide + sd * 1024 + 512, a.Dpad + side_row + i * kTile, 512,
+                        bar(BAR_SIDE_FULL + sd));
+            } else {
+              mbar_arrive(bar(BAR_SIDE_FULL + sd));  // no copy: complete the phase
+            }
             side_issued = g + 1;
             if (!mbar_wait(bar(BAR_Q_EMPTY + sd), ((g >> 1) & 1) ^ 1, wc)) {
               ok = false;
@@ -808,9 +827,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < kCols / 2; ++c) pv[c] = pk2[c] = 0u;
       }
-      if (key < N) {
-        const size_t krow =
-            kPacked ? static_cast<size_t>(w.tok0 + key) * a.H + w.head : static_cast<size_t>(w.bh) * N + key;
+      const size_t krow =
+          kPacked ? static_cast<size_t>(w.tok0 + key) * a.H + w.head : static_cast<size_t>(w.bh) * N + key;
+      if (key < N && FA_IN_BOUNDS(static_cast<long long>(krow), a.dbg_rows, a.status)) {
         const size_t rowoff = (krow * D + grp * kCols) * 2;
         uint4* dv_dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.dV) + rowoff);
         uint4* dk_dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.dK) + rowoff);
@@ -871,6 +890,11 @@ fa_status bwd_launch_d(const void* Q, const void* K, const void* V, const void* 
   a.causal = causal ? 1 : 0;
   a.scale = scale;
   a.scale_log2 = scale * kLog2e;
+#ifdef FA_DEBUG
+  a.dbg_nb = B;
+  a.dbg_rows = static_cast<long long>(BH) * N;
+  a.dbg_side = static_cast<long long>(BH) * Npad;
+#endif
   a.status = device_status_ptr();
   if (a.status == nullptr) return FA_ERR_CUDA;
 
@@ -936,6 +960,11 @@ fa_status bwd_varlen_launch_d(const void* Q, const void* K, const void* V, const
   a.causal = causal ? 1 : 0;
   a.scale = scale;
   a.scale_log2 = scale * kLog2e;
+#ifdef FA_DEBUG
+  a.dbg_nb = num_seqs;
+  a.dbg_rows = static_cast<long long>(total) * H;
+  a.dbg_side = static_cast<long long>(BH) * Npad;
+#endif
   a.status = device_status_ptr();
   if (a.status == nullptr) return FA_ERR_CUDA;
   // packed [total, H, D]: TMA dims (D, H, total), 128 consecutive tokens of one head

@@ -124,7 +124,7 @@ __global__ void __launch_bounds__(kThreads, 3)
   const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   // the work is cut into 16-token chunks; chunk c lives in cache block
   // table[c * 16 / block_size] at row (c * 16) % block_size
-  const int L = min(max(a.seq_lens[b], 0), a.max_blocks * a.block_size);
+  const int L = FA_IN_BOUNDS(b, a.B, a.status) ? min(max(a.seq_lens[b], 0), a.max_blocks * a.block_size) : 0;
   const int nb = (L + kBlk - 1) / kBlk;
   const int S_b = splits_for(nb, a.S, a.min_blocks);
   if (s >= S_b) return;  // this sequence uses fewer splits
@@ -169,7 +169,11 @@ __global__ void __launch_bounds__(kThreads, 3)
         const int st = i % kStages;
         if (!mbar_wait(empty(st), ((i / kStages) & 1) ^ 1, wc)) break;
         const int chunk_key = (lo + i) * kBlk;
-        const int phys = __ldg(table + (kUnit ? lo + i : chunk_key / a.block_size));
+        const int te = kUnit ? lo + i : chunk_key / a.block_size;
+        const int phys = FA_IN_BOUNDS(static_cast<long long>(b) * a.max_blocks + te,
+                                      static_cast<long long>(a.B) * a.max_blocks, a.status)
+                             ? __ldg(table + te)
+                             : -1;
         if (phys >= 0 && phys < a.num_blocks) {
           mbar_arrive_expect_tx(full(st), kStageBytes);
           const uint32_t dst = sbase + st * kStageBytes;
@@ -200,7 +204,10 @@ __global__ void __launch_bounds__(kThreads, 3)
     {
       const uint32_t* q0 = reinterpret_cast<const uint32_t*>(a.q + (static_cast<size_t>(b) * a.Hq + h0 + r0) * D);
       const uint32_t* q8 = reinterpret_cast<const uint32_t*>(a.q + (static_cast<size_t>(b) * a.Hq + h0 + r0 + 8) * D);
-      const bool v0 = r0 < a.G, v8 = r0 + 8 < a.G;
+      const bool v0 = r0 < a.G &&
+                      FA_IN_BOUNDS(static_cast<long long>(b) * a.Hq + h0 + r0, static_cast<long long>(a.B) * a.Hq, a.status);
+      const bool v8 = r0 + 8 < a.G && FA_IN_BOUNDS(static_cast<long long>(b) * a.Hq + h0 + r0 + 8,
+                                                   static_cast<long long>(a.B) * a.Hq, a.status);
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks) {
         const int col = (16 * ks + c2) >> 1;  // in bf16 pairs
@@ -218,7 +225,11 @@ __global__ void __launch_bounds__(kThreads, 3)
       if (!mbar_wait(full(st), (i / kStages) & 1, wc)) break;
       const uint32_t stK = sbase + st * kStageBytes;
       const uint32_t stV = stK + C::kHalves * kHalfBytes;
-      const int phys = __ldg(table + (kUnit ? lo + i : (lo + i) * kBlk / a.block_size));
+      const int te = kUnit ? lo + i : (lo + i) * kBlk / a.block_size;
+      const int phys = FA_IN_BOUNDS(static_cast<long long>(b) * a.max_blocks + te,
+                                    static_cast<long long>(a.B) * a.max_blocks, a.status)
+                           ? __ldg(table + te)
+                           : -1;
       const bool bad = !(phys >= 0 && phys < a.num_blocks);
       // ---- S = Q K^T over 16 keys (two n8 tiles)
       float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -322,6 +333,7 @@ __global__ void __launch_bounds__(kThreads, 3)
       }
       if (a.direct) {
         const size_t row = static_cast<size_t>(b) * a.Hq + g * a.G + r;
+        if (!FA_IN_BOUNDS(static_cast<long long>(row), static_cast<long long>(a.B) * a.Hq, a.status)) continue;
         const float inv = (l > 0.f) ? 1.f / l : 0.f;
         a.o[row * D + dcol] = __float2bfloat16_rn(o * inv);
         if (a.lse != nullptr && dcol == 0)
@@ -329,6 +341,7 @@ __global__ void __launch_bounds__(kThreads, 3)
         continue;
       }
       const size_t idx = (static_cast<size_t>(b) * a.Hq + g * a.G + r) * a.S + s;
+      if (!FA_IN_BOUNDS(static_cast<long long>(idx), static_cast<long long>(a.B) * a.Hq * a.S, a.status)) continue;
       a.part_o[idx * D + dcol] = o;
       if (dcol == 0) {
         a.part_ml[2 * idx] = m;
@@ -349,11 +362,13 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecArgs a) {
   const int lane = threadIdx.x & 31;
   if (gw >= a.B * a.Hq) return;
   const int b = gw / a.Hq;
-  const int L = min(max(a.seq_lens[b], 0), a.max_blocks * a.block_size);
+  const int L = FA_IN_BOUNDS(b, a.B, a.status) ? min(max(a.seq_lens[b], 0), a.max_blocks * a.block_size) : 0;
   const int S_b = splits_for((L + kBlk - 1) / kBlk, a.S, a.min_blocks);
   const float* po = a.part_o + static_cast<size_t>(gw) * a.S * D;
   const float* pml = a.part_ml + static_cast<size_t>(gw) * a.S * 2;
   float m = -INFINITY;
+  if (!FA_IN_BOUNDS(static_cast<long long>(gw) * a.S + S_b - 1, static_cast<long long>(a.B) * a.Hq * a.S, a.status))
+    return;
   for (int s = 0; s < S_b; ++s)
     if (pml[2 * s + 1] > 0.f) m = fmaxf(m, pml[2 * s]);
   float o[kPer];

@@ -118,6 +118,12 @@ struct FwdArgs {
   const uint8_t* block_mask;
   long long mask_stride;
   int nkb;
+#ifdef FA_DEBUG
+  // extents for the debug bounds checks: batch entries (sequences), rows of
+  // O (D elements each), elements of LSE, bytes of the block mask
+  int dbg_nb;
+  long long dbg_o_rows, dbg_lse_len, dbg_mask_bytes;
+#endif
 };
 
 // Wait for a barrier phase ignoring the abort flag, for at most ~50 ms; used
@@ -166,9 +172,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   // is the square top-left mask, qoff = kv_len - Lq the bottom-right one of a
   // query chunk at the end of its context); tok0 = first query token (packed)
   // kv_lens: the dense key-padding lengths or the paged context lengths
-  const int kv_given = (args.kv_lens != nullptr) ? args.kv_lens[b] : N;
+  const int kv_given =
+      (args.kv_lens != nullptr && FA_IN_BOUNDS(b, args.dbg_nb, args.status)) ? args.kv_lens[b] : N;
   int Lq = N, kv_len = N, tok0 = 0, qoff = 0;
   if (packed) {
+    if (!FA_IN_BOUNDS(b + 1, args.dbg_nb + 1, args.status)) return;
     tok0 = args.cu_seqlens[b];
     const int tok1 = args.cu_seqlens[b + 1];
     kv_len = paged ? kv_given : tok1 - tok0;
@@ -214,8 +222,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 4
         for (int bt = 0; bt < 32; ++bt) {
           const int j = 32 * w + bt;
-          if (j < n_t[0] && mrow[static_cast<size_t>(2 * mblk) * args.nkb + j]) r0 |= 1u << bt;
-          if (j < n_t[1] && mrow[static_cast<size_t>(2 * mblk + 1) * args.nkb + j]) r1 |= 1u << bt;
+          if (j < n_t[0] &&
+              FA_IN_BOUNDS(bh * args.mask_stride + (2LL * mblk) * args.nkb + j, args.dbg_mask_bytes, args.status) &&
+              mrow[static_cast<size_t>(2 * mblk) * args.nkb + j])
+            r0 |= 1u << bt;
+          if (j < n_t[1] &&
+              FA_IN_BOUNDS(bh * args.mask_stride + (2LL * mblk + 1) * args.nkb + j, args.dbg_mask_bytes,
+                           args.status) &&
+              mrow[static_cast<size_t>(2 * mblk + 1) * args.nkb + j])
+            r1 |= 1u << bt;
         }
       }
       const uint32_t u = r0 | r1;
@@ -322,7 +337,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int boxes = paged ? kKeys / args.box_rows : 0;
     auto table_window = [&](int w) -> int {
       const int e = 32 * w + lane;
-      return (e < n_entries) ? trow[e] : -1;
+      return (e < n_entries && FA_IN_BOUNDS(static_cast<long long>(b) * args.max_blocks + e,
+                                            static_cast<long long>(args.dbg_nb) * args.max_blocks, args.status))
+                 ? trow[e]
+                 : -1;
     };
     int win = 0, cur = -1, nxt = -1;
     if (paged) {
@@ -594,7 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 16; ++i)
             w[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * inv, __uint_as_float(r[2 * i + 1]) * inv);
-          if (in_range) {
+          if (in_range && FA_IN_BOUNDS(static_cast<long long>(orow_idx), args.dbg_o_rows, args.status)) {
             uint4* dst = reinterpret_cast<uint4*>(orow + c0 * 2);
 #pragma unroll
             for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
@@ -604,7 +622,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float lse = empty ? -INFINITY : (m_ref + lg2_approx(l_sum)) * 0.69314718055994531f;
           const size_t lidx = packed ? static_cast<size_t>(head) * args.total + tok0 + row
                                      : static_cast<size_t>(bh) * N + row;
-          args.LSE[lidx] = lse;
+          if (FA_IN_BOUNDS(static_cast<long long>(lidx), args.dbg_lse_len, args.status)) args.LSE[lidx] = lse;
         }
       }
     }
@@ -665,6 +683,12 @@ fa_status fwd_launch_d(const void* Q, const void* K, const void* V, void* O, flo
   a.scale_log2 = scale * 1.4426950408889634f;
   a.status = status;
   a.head_group = dense_head_group(B, H, N, D);
+#ifdef FA_DEBUG
+  a.dbg_nb = B;
+  a.dbg_o_rows = a.dbg_lse_len = static_cast<long long>(B) * H * N;
+  a.dbg_mask_bytes = block_mask == nullptr ? 0 : (mask_stride != 0 ? static_cast<long long>(B) * H * mask_stride
+                                                                     : static_cast<long long>(a.nkb) * a.nkb);
+#endif
   dim3 grid(a.head_group, ceil_div(N, 2 * kRows), B * ceil_div(H, a.head_group));
   fwd_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, a);
   return launch_status();
@@ -698,6 +722,11 @@ fa_status fwd_varlen_launch_d(const void* Q, const void* K, const void* V, void*
   a.scale_log2 = scale * 1.4426950408889634f;
   a.status = status;
   a.head_group = H;
+#ifdef FA_DEBUG
+  a.dbg_nb = num_seqs;
+  a.dbg_o_rows = a.dbg_lse_len = static_cast<long long>(total) * H;
+  a.dbg_mask_bytes = 0;
+#endif
   dim3 grid(H, ceil_div(max_seqlen, 2 * kRows), num_seqs);
   fwd_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, a);
   return launch_status();
@@ -746,6 +775,11 @@ fa_status fwd_paged_launch_d(const void* q, const void* k_cache, const void* v_c
   a.num_blocks = num_blocks;
   a.group = Hq / Hkv;
   a.head_group = Hq;
+#ifdef FA_DEBUG
+  a.dbg_nb = num_seqs;
+  a.dbg_o_rows = a.dbg_lse_len = static_cast<long long>(total_q) * Hq;
+  a.dbg_mask_bytes = 0;
+#endif
   dim3 grid(Hq, ceil_div(max_seqlen_q, 2 * kRows), num_seqs);
   fwd_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, a);
   return launch_status();

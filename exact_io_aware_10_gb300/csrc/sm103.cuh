@@ -88,6 +88,23 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, WaitCtx
   return mbar_wait_slow(bar, parity, ctx);
 }
 
+// ------------------------------------------------------------------ debug bounds checks
+// Built with FA_DEBUG, the kernels guard every global load or store their
+// threads issue (TMA copies clip at the tensor edges by themselves) with
+// FA_IN_BOUNDS(i, n, status): an element index outside [0, n) latches
+// kStatusBoundsBit in the status word and the access is skipped.  Without
+// FA_DEBUG the guard is the constant true and the kernels are unchanged.
+#ifdef FA_DEBUG
+__device__ __forceinline__ bool fa_in_bounds(long long i, long long n, unsigned* status) {
+  if (i >= 0 && i < n) return true;
+  atomicOr(status, kStatusBoundsBit);
+  return false;
+}
+#define FA_IN_BOUNDS(i, n, status) ::fa::fa_in_bounds((i), (n), (status))
+#else
+#define FA_IN_BOUNDS(i, n, status) true
+#endif
+
 // ------------------------------------------------------------------ programmatic dependent launch
 // For kernels launched with the programmatic stream serialization attribute:
 // griddep_wait() returns once the grids this one depends on have completed

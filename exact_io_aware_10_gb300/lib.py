@@ -23,6 +23,7 @@ FA_ERR_UNSUPPORTED = 2
 FA_ERR_CUDA = 3
 FA_ERR_TIMEOUT = 4
 FA_ERR_BAD_BLOCK_TABLE = 5
+FA_ERR_OUT_OF_BOUNDS = 6
 
 # name -> (restype, argtypes); mirrors include/fa.h
 _vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
@@ -46,6 +47,8 @@ SIGNATURES = {
     "fa_paged_decode": (_i, [_vp] * 7 + [_i] * 8 + [_f, _vp, _sz, _vp]),
     "fa_get_device_status": (_i, [_vp]),
     "fa_selftest_wait_timeout": (_i, [ctypes.c_uint, _vp]),
+    "fa_debug_build": (_i, []),
+    "fa_selftest_bounds": (_i, [_vp]),
     "fa_paged_decode_noalloc": (_i, [_vp] * 7 + [_i] * 8 + [_f, _vp]),
 }
 
@@ -59,7 +62,10 @@ class FAError(RuntimeError):
 
 
 def library_path() -> str:
-    return _build.LIB_PATH
+    """The shared library this binding loads: the release build, or the build
+    named by the FA_GB300_LIB environment variable (e.g. the debug build with
+    device bounds checks, ``build.build(debug=True)``)."""
+    return os.environ.get("FA_GB300_LIB") or _build.LIB_PATH
 
 
 def load():

@@ -42,7 +42,9 @@ typedef enum fa_status {
   FA_ERR_UNSUPPORTED = 2,     /* valid request outside what the kernels cover (e.g. d = 96) */
   FA_ERR_CUDA = 3,            /* a CUDA runtime/driver call or launch failed */
   FA_ERR_TIMEOUT = 4,         /* device: a bounded pipeline wait gave up */
-  FA_ERR_BAD_BLOCK_TABLE = 5  /* device: a block-table entry was outside [0, num_blocks) */
+  FA_ERR_BAD_BLOCK_TABLE = 5, /* device: a block-table entry was outside [0, num_blocks) */
+  FA_ERR_OUT_OF_BOUNDS = 6    /* device, debug builds only: a kernel computed an index outside one of
+                                 its buffers; the access was skipped (see fa_debug_build) */
 } fa_status;
 
 /* Human-readable name of a status code; never NULL. */
@@ -331,10 +333,31 @@ int fa_selftest_wait_timeout(unsigned timeout_us, void* stream);
 /*
  * Synchronises `stream`, then returns and clears the device status word of
  * the current device: FA_OK, or the most severe condition latched since the
- * last call -- FA_ERR_CUDA (a kernel could not set up its shared memory, or the
- * query itself failed), FA_ERR_TIMEOUT, FA_ERR_BAD_BLOCK_TABLE.
+ * last call -- FA_ERR_OUT_OF_BOUNDS (debug builds), FA_ERR_CUDA (a kernel could
+ * not set up its shared memory, or the query itself failed),
+ * FA_ERR_INVALID_ARG (device-side offsets check), FA_ERR_TIMEOUT,
+ * FA_ERR_BAD_BLOCK_TABLE.
  */
 int fa_get_device_status(void* stream);
+
+/*
+ * 1 if this library was built with device bounds checks (FA_DEBUG), else 0.
+ * In such a build every global load or store a kernel's threads issue is
+ * checked against the extent of its buffer; an index outside it skips the
+ * access and latches FA_ERR_OUT_OF_BOUNDS (read with fa_get_device_status).
+ * TMA copies clip at the tensor edges by themselves.  The checks stand in for
+ * a memory checker; release builds carry none of them.
+ * (Not an operation of the pages; it checks this library.)
+ */
+int fa_debug_build(void);
+
+/*
+ * Self-test of the bounds checks: one thread asks the device guard about an
+ * index past the end of a 3-element extent, without touching memory.  In a
+ * debug build the status word then reads FA_ERR_OUT_OF_BOUNDS; in a release
+ * build FA_OK.  (Not an operation of the pages.)
+ */
+int fa_selftest_bounds(void* stream);
 
 #ifdef __cplusplus
 }

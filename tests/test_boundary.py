@@ -3,6 +3,8 @@ include/fa.h, and rejects invalid arguments before touching the GPU."""
 import ctypes
 import os
 import re
+import subprocess
+import sys
 
 import pytest
 
@@ -41,10 +43,10 @@ def test_library_exports_every_declared_symbol(so):
 
 def test_status_strings(so):
     for code, name in [(0, "FA_OK"), (1, "FA_ERR_INVALID_ARG"), (2, "FA_ERR_UNSUPPORTED"), (3, "FA_ERR_CUDA"),
-                       (4, "FA_ERR_TIMEOUT"), (5, "FA_ERR_BAD_BLOCK_TABLE")]:
+                       (4, "FA_ERR_TIMEOUT"), (5, "FA_ERR_BAD_BLOCK_TABLE"), (6, "FA_ERR_OUT_OF_BOUNDS")]:
         assert so.fa_status_string(code).decode() == name
     assert so.fa_status_string(99).decode() == "FA_ERR_UNKNOWN"
-    assert so.fa_version() == 105
+    assert so.fa_version() == 106
 
 
 def _fake(n=1):
@@ -235,3 +237,12 @@ def test_host_tensors_are_refused(so):
     x = torch.zeros(1, 1, 16, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError, match="CUDA"):
         fl.fa_fwd(x, x, x)
+
+
+def test_debug_build_compiles_and_reports_itself():
+    # the FA_DEBUG variant (device bounds checks) builds from the same sources;
+    # loading it needs no GPU
+    path = fab.build(debug=True)
+    r = subprocess.run([sys.executable, "-c", f"import ctypes; print(ctypes.CDLL({path!r}).fa_debug_build())"],
+                       capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0 and r.stdout.strip() == "1", r.stdout + r.stderr
