@@ -314,7 +314,8 @@ template <int D, bool kPacked>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                       const __grid_constant__ CUtensorMap tmdQ, const BwdArgs a) {
+                       const __grid_constant__ CUtensorMap tmdQ, const __grid_constant__ CUtensorMap tmdK,
+                       const __grid_constant__ CUtensorMap tmdV, const BwdArgs a) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   {
@@ -827,16 +828,61 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < kCols / 2; ++c) pv[c] = pk2[c] = 0u;
       }
-      const size_t krow =
-          kPacked ? static_cast<size_t>(w.tok0 + key) * a.H + w.head : static_cast<size_t>(w.bh) * N + key;
-      if (key < N && FA_IN_BOUNDS(static_cast<long long>(krow), a.dbg_rows, a.status)) {
-        const size_t rowoff = (krow * D + grp * kCols) * 2;
-        uint4* dv_dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.dV) + rowoff);
-        uint4* dk_dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.dK) + rowoff);
+      if constexpr (kPacked) {
+        // packed: rows past the sequence belong to the next one, so each
+        // thread stores its own row
+        const size_t krow = static_cast<size_t>(w.tok0 + key) * a.H + w.head;
+        if (key < N && FA_IN_BOUNDS(static_cast<long long>(krow), a.dbg_rows, a.status)) {
+          const size_t rowoff = (krow * D + grp * kCols) * 2;
+          uint4* dv_dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.dV) + rowoff);
+          uint4* dk_dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.dK) + rowoff);
 #pragma unroll
-        for (int q = 0; q < kCols / 8; ++q) {
-          dv_dst[q] = make_uint4(pv[4 * q], pv[4 * q + 1], pv[4 * q + 2], pv[4 * q + 3]);
-          dk_dst[q] = make_uint4(pk2[4 * q], pk2[4 * q + 1], pk2[4 * q + 2], pk2[4 * q + 3]);
+          for (int q = 0; q < kCols / 8; ++q) {
+            dv_dst[q] = make_uint4(pv[4 * q], pv[4 * q + 1], pv[4 * q + 2], pv[4 * q + 3]);
+            dk_dst[q] = make_uint4(pk2[4 * q], pk2[4 * q + 1], pk2[4 * q + 2], pk2[4 * q + 3]);
+          }
+        }
+      } else {
+        // dense: dV and dK are staged as 128-byte-swizzled tiles and written by
+        // TMA stores (rows past N clipped), full lines instead of 16-byte
+        // pieces 2 d bytes apart.  d = 128: dV in the dQ staging buffer, dK in
+        // the dS^T buffer, one 64-column sub-tile per warpgroup leader, each in
+        // the region its own next dQ staging reuses; d = 64: both in the
+        // staging buffer, 64-row halves by the four lane-quarter leaders.
+        const bool qleader = (D == 128) ? (q4 == 0 && lane == 0) : (grp == 0 && lane == 0);
+        // the last tile's dQ reductions have read their staging boxes
+        if (qleader) bulk_wait_read_all();
+        named_barrier_sync(1, 32 * kComputeWarps);
+        const uint32_t vbase = sbase + C::kOffStage;
+        const uint32_t kbase = (D == 128) ? sbase + C::kOffP : sbase + C::kOffStage + kTile * 128;
+#pragma unroll
+        for (int h2 = 0; h2 < kCols / 8; ++h2) {
+          // 16-byte chunk of this thread's columns: d = 128: sub-tile grp / 2,
+          // chunks 4 (grp & 1) + h2; d = 64: chunks 2 grp + h2 of the one sub-tile
+          const int sub = (D == 128) ? (grp >> 1) : 0;
+          const int chunk = (D == 128) ? 4 * (grp & 1) + h2 : 2 * grp + h2;
+          const uint32_t off = sub * C::kSubBytes + r * 128 + ((chunk ^ swz) << 4);
+          st_shared_v4(vbase + off, pv[4 * h2], pv[4 * h2 + 1], pv[4 * h2 + 2], pv[4 * h2 + 3]);
+          st_shared_v4(kbase + off, pk2[4 * h2], pk2[4 * h2 + 1], pk2[4 * h2 + 2], pk2[4 * h2 + 3]);
+        }
+        fence_proxy_async_smem();
+        named_barrier_sync(1, 32 * kComputeWarps);
+        if (qleader) {
+          const int row0 = w.j * kTile;
+          if constexpr (D == 128) {
+            // warpgroups 0-1: dV sub-tile grp; 2-3: dK sub-tile grp - 2
+            if (grp < 2)
+              tma_store_3d(&tmdV, vbase + grp * C::kSubBytes, 64 * grp, row0, w.bh);
+            else
+              tma_store_3d(&tmdK, kbase + (grp - 2) * C::kSubBytes, 64 * (grp - 2), row0, w.bh);
+          } else {
+            // lane quarters 0-1: dV rows 64 q4 ..; 2-3: dK rows 64 (q4 - 2) ..
+            if (q4 < 2)
+              tma_store_3d(&tmdV, vbase + q4 * 64 * 128, 0, row0 + 64 * q4, w.bh);
+            else
+              tma_store_3d(&tmdK, kbase + (q4 - 2) * 64 * 128, 0, row0 + 64 * (q4 - 2), w.bh);
+          }
+          bulk_commit();
         }
       }
       if (have) {
@@ -901,7 +947,7 @@ fa_status bwd_launch_d(const void* Q, const void* K, const void* V, const void* 
   const uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(N), static_cast<uint64_t>(BH)};
   const uint64_t strides[2] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(N) * D * 2};
   const uint32_t box[3] = {64, kTile, 1};
-  CUtensorMap tq, tk, tv, tdo, tdq;
+  CUtensorMap tq, tk, tv, tdo, tdq, tdk, tdv;
   if (!encode_bf16_tmap(&tq, Q, 3, dims, strides, box) || !encode_bf16_tmap(&tk, K, 3, dims, strides, box) ||
       !encode_bf16_tmap(&tv, V, 3, dims, strides, box) || !encode_bf16_tmap(&tdo, dO, 3, dims, strides, box))
     return FA_ERR_CUDA;
@@ -917,6 +963,11 @@ fa_status bwd_launch_d(const void* Q, const void* K, const void* V, const void* 
   a.gx = nq * kHeadGroup;
   a.n_items = a.gx * ceil_div(BH, kHeadGroup);
   a.sched = bwd_sched_ptr(workspace, side, static_cast<size_t>(BH) * N * D);
+  // dK, dV as TMA store targets: 64-column boxes of a key tile's rows (d = 64:
+  // 64-row halves)
+  const uint32_t sbox[3] = {64, D == 128 ? 128u : 64u, 1};
+  if (!encode_bf16_tmap(&tdk, dK, 3, dims, strides, sbox) || !encode_bf16_tmap(&tdv, dV, 3, dims, strides, sbox))
+    return FA_ERR_CUDA;
   if (!set_smem_limit(reinterpret_cast<const void*>(&bwd_main_kernel<D, false>), C::kSmemBytes))
     return FA_ERR_CUDA;
   const long long pre_rows = static_cast<long long>(BH) * Npad;
@@ -925,7 +976,7 @@ fa_status bwd_launch_d(const void* Q, const void* K, const void* V, const void* 
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   // one persistent CTA per SM (fewer when there are fewer work items)
   const int ctas = min(a.n_items, max(sm_count(), 1));
-  bwd_main_kernel<D, false><<<ctas, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, a);
+  bwd_main_kernel<D, false><<<ctas, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, tdk, tdv, a);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   const long long n4 = static_cast<long long>(BH) * N * D / 4;
   bwd_dq_kernel<<<static_cast<unsigned>((n4 + 255) / 256), 256, 0, stream>>>(a.dQacc,
@@ -971,7 +1022,7 @@ fa_status bwd_varlen_launch_d(const void* Q, const void* K, const void* V, const
   const uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(H), static_cast<uint64_t>(total)};
   const uint64_t strides[2] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(H) * D * 2};
   const uint32_t box[3] = {64, 1, kTile};
-  CUtensorMap tq, tk, tv, tdo, tdq;
+  CUtensorMap tq, tk, tv, tdo, tdq, tdk, tdv;
   if (!encode_bf16_tmap(&tq, Q, 3, dims, strides, box) || !encode_bf16_tmap(&tk, K, 3, dims, strides, box) ||
       !encode_bf16_tmap(&tv, V, 3, dims, strides, box) || !encode_bf16_tmap(&tdo, dO, 3, dims, strides, box))
     return FA_ERR_CUDA;
@@ -985,6 +1036,9 @@ fa_status bwd_varlen_launch_d(const void* Q, const void* K, const void* V, const
   a.gx = nq * kHeadGroup;
   a.n_items = a.gx * ceil_div(BH, kHeadGroup);
   a.sched = bwd_sched_ptr(workspace, side, static_cast<size_t>(total) * H * D);
+  // (the packed kernel stores dK, dV row by row; these maps are not used)
+  if (!encode_bf16_tmap(&tdk, dK, 3, dims, strides, box) || !encode_bf16_tmap(&tdv, dV, 3, dims, strides, box))
+    return FA_ERR_CUDA;
   if (!set_smem_limit(reinterpret_cast<const void*>(&bwd_main_kernel<D, true>), C::kSmemBytes))
     return FA_ERR_CUDA;
   const long long pre_rows = static_cast<long long>(BH) * Npad;
@@ -993,7 +1047,7 @@ fa_status bwd_varlen_launch_d(const void* Q, const void* K, const void* V, const
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   // one persistent CTA per SM (fewer when there are fewer work items)
   const int ctas = min(a.n_items, max(sm_count(), 1));
-  bwd_main_kernel<D, true><<<ctas, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, a);
+  bwd_main_kernel<D, true><<<ctas, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, tdk, tdv, a);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   const long long n4 = static_cast<long long>(total) * H * D / 4;
   bwd_dq_kernel<<<static_cast<unsigned>((n4 + 255) / 256), 256, 0, stream>>>(a.dQacc,

@@ -144,6 +144,15 @@ __device__ __forceinline__ void tma_reduce_add_3d(const void* tmap, uint32_t src
                "r"(src), "r"(x), "r"(y), "r"(z)
                : "memory");
 }
+// Copy of a shared-memory box into a 3-D tensor in global memory (the box
+// laid out as the tensor map's swizzle dictates); rows outside the tensor are
+// clipped.  Completion is tracked per thread with bulk groups.
+__device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t src, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)),
+               "r"(src), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until this thread's committed bulk operations have finished reading shared memory.
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
