@@ -145,8 +145,23 @@ struct BwdArgs {
   // each of the -D and -LSE2 row buffers
   int dbg_nb;
   long long dbg_rows, dbg_side;
+  int dbg_stall_item;                   // the MMA warp stops before this work item (-1: never)
+  unsigned long long dbg_timeout_ns;    // wait limit of this launch (0: the default)
 #endif
 };
+
+#ifdef FA_DEBUG
+// One-shot stall armed by fa_debug_stall_backward, taken by the next launch
+// of the main kernel (host side, not thread-safe: a debug hook).
+int g_stall_item = -1;
+unsigned long long g_stall_timeout_ns = 0;
+void take_backward_stall(BwdArgs& a) {
+  a.dbg_stall_item = g_stall_item;
+  a.dbg_timeout_ns = g_stall_timeout_ns;
+  g_stall_item = -1;
+  g_stall_timeout_ns = 0;
+}
+#endif
 
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   const unsigned long long t0 = global_timer_ns();
@@ -369,8 +384,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+#ifdef FA_DEBUG
+  const WaitCtx wc{abort_flag, a.status, a.dbg_timeout_ns != 0 ? a.dbg_timeout_ns : kWaitTimeoutNs};
+#else
   const WaitCtx wc{abort_flag, a.status};
+#endif
   // consumers read item k from slot k & 1 once SCHED_FULL has completed for it
+  // (the compute warps' version ignores the abort flag, like their other waits)
+  auto take_item_alike = [&](int k, int& item) -> bool {
+    if (!mbar_wait_alike(bar(BAR_SCHED_FULL + (k & 1)), static_cast<uint32_t>(k >> 1) & 1u, wc)) return false;
+    item = sched_slot[k & 1];
+    return true;
+  };
   auto take_item = [&](int k, int& item) -> bool {
     if (!mbar_wait(bar(BAR_SCHED_FULL + (k & 1)), static_cast<uint32_t>(k >> 1) & 1u, wc)) return false;
     item = sched_slot[k & 1];
@@ -499,6 +524,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(ok = take_item(k, item))) break;
           mbar_arrive(bar(BAR_SCHED_EMPTY + (k & 1)));
           if (item >= a.n_items) break;
+#ifdef FA_DEBUG
+          if (item == a.dbg_stall_item) {  // injected stall: this warp issues nothing more
+            ok = false;
+            break;
+          }
+#endif
           BwdItem<kPacked> w;
           if (!w.decode(a, item) || w.nt == 0) continue;
           const int nt = w.nt;
@@ -619,11 +650,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int swz = r & 7;
     const float2 sl2v = make_float2(a.scale_log2, a.scale_log2);
     const float2 scv = make_float2(a.scale, a.scale);
+    // The compute warps wait on the same phases in the same order and hold
+    // named barriers between their waits.  Their waits ignore the CTA's abort
+    // flag and give up only at their own limit, so a phase that never
+    // completes stops all of them at the same wait and none is left at a
+    // barrier for a thread that has gone.
     bool aborted = false;
     int gs = 0, kf = 0;
     for (int k = 0; !aborted; ++k) {
       int item = 0;
-      if (!take_item(k, item)) {
+      if (!take_item_alike(k, item)) {
         aborted = true;
         break;
       }
@@ -640,7 +676,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int g = gs + it;
         const int i = w.i0 + it;
         const int sd = g & 1;
-        if (!mbar_wait(bar(BAR_SIDE_FULL + sd), (g >> 1) & 1, wc) || !mbar_wait(bar(BAR_S), g & 1, wc)) {
+        if (!mbar_wait_alike(bar(BAR_SIDE_FULL + sd), (g >> 1) & 1, wc) || !mbar_wait_alike(bar(BAR_S), g & 1, wc)) {
           aborted = true;
           break;
         }
@@ -684,7 +720,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(BAR_P));
         // ---- dS^T = scale * P^T * (dP^T - D[q])  -> shared memory (bf16)
-        if (!mbar_wait(bar(BAR_DP), g & 1, wc)) {
+        if (!mbar_wait_alike(bar(BAR_DP), g & 1, wc)) {
           aborted = true;
           break;
         }
@@ -739,7 +775,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(BAR_DS));
         // ---- dQ_i += this tile's contribution
-        if (!mbar_wait(bar(BAR_DQ_FULL), g & 1, wc)) {
+        if (!mbar_wait_alike(bar(BAR_DQ_FULL), g & 1, wc)) {
           aborted = true;
           break;
         }
@@ -798,7 +834,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- epilogue: dV_j, dK_j rows (thread = key row r), head-dim columns of
       // this warpgroup; TMEM is released for the next item before the stores
       const bool have = nt > 0;
-      if (have && !mbar_wait(bar(BAR_FINAL), static_cast<uint32_t>(kf) & 1u, wc)) {
+      if (have && !mbar_wait_alike(bar(BAR_FINAL), static_cast<uint32_t>(kf) & 1u, wc)) {
         aborted = true;
         break;
       }
@@ -940,6 +976,7 @@ fa_status bwd_launch_d(const void* Q, const void* K, const void* V, const void* 
   a.dbg_nb = B;
   a.dbg_rows = static_cast<long long>(BH) * N;
   a.dbg_side = static_cast<long long>(BH) * Npad;
+  take_backward_stall(a);
 #endif
   a.status = device_status_ptr();
   if (a.status == nullptr) return FA_ERR_CUDA;
@@ -1015,6 +1052,7 @@ fa_status bwd_varlen_launch_d(const void* Q, const void* K, const void* V, const
   a.dbg_nb = num_seqs;
   a.dbg_rows = static_cast<long long>(total) * H;
   a.dbg_side = static_cast<long long>(BH) * Npad;
+  take_backward_stall(a);
 #endif
   a.status = device_status_ptr();
   if (a.status == nullptr) return FA_ERR_CUDA;
@@ -1056,6 +1094,18 @@ fa_status bwd_varlen_launch_d(const void* Q, const void* K, const void* V, const
 }
 
 }  // namespace
+
+bool arm_backward_stall(int item, unsigned long long timeout_ns) {
+#ifdef FA_DEBUG
+  g_stall_item = item;
+  g_stall_timeout_ns = timeout_ns;
+  return true;
+#else
+  (void)item;
+  (void)timeout_ns;
+  return false;
+#endif
+}
 
 fa_status bwd_varlen_launch(const void* Q, const void* K, const void* V, const void* O, const void* dO,
                             const float* LSE, void* dQ, void* dK, void* dV, const int32_t* cu_seqlens, int num_seqs,

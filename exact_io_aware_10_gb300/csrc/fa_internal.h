@@ -68,6 +68,11 @@ fa_status decode_prepare();
 bool set_smem_limit(const void* func, int bytes);
 // Number of SMs of the current device (0 if CUDA fails), looked up once per device.
 int sm_count();
+
+// FA_DEBUG builds: arm a one-shot stall of the backward main kernel's MMA warp
+// before work item `item`, with wait limit `timeout_ns` for that launch;
+// false (nothing armed) in release builds.
+bool arm_backward_stall(int item, unsigned long long timeout_ns);
 // Loads the tensor-map encoder entry point if needed; false if unavailable.
 bool encode_init();
 // Argument checks shared by every paged-decode entry point (with and without

@@ -88,6 +88,27 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, WaitCtx
   return mbar_wait_slow(bar, parity, ctx);
 }
 
+static __device__ __forceinline__ bool mbar_wait_alike_slow(uint32_t bar, uint32_t parity, WaitCtx ctx) {
+  const unsigned long long t0 = global_timer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_test(bar, parity)) return true;
+    if ((i & 63u) == 0 && global_timer_ns() - t0 > ctx.timeout_ns) {
+      *ctx.abort_flag = 1;
+      atomicOr(ctx.status, kStatusTimeoutBit);
+      return false;
+    }
+  }
+}
+
+// Like mbar_wait, but blind to the abort flag: false only once this wait's own
+// limit has run out (it then sets the flag and the status bit).  Threads that
+// wait on the same phases in the same order therefore give up at the same
+// wait, which threads that also meet at named barriers need.
+__device__ __forceinline__ bool mbar_wait_alike(uint32_t bar, uint32_t parity, WaitCtx ctx) {
+  if (mbar_test(bar, parity)) return true;
+  return mbar_wait_alike_slow(bar, parity, ctx);
+}
+
 // ------------------------------------------------------------------ debug bounds checks
 // Built with FA_DEBUG, the kernels guard every global load or store their
 // threads issue (TMA copies clip at the tensor edges by themselves) with

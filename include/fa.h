@@ -359,6 +359,22 @@ int fa_debug_build(void);
  */
 int fa_selftest_bounds(void* stream);
 
+/*
+ * Failure injection for the backward pass (debug builds only): the next
+ * launch of the backward's main kernel (fa_bwd or fa_bwd_varlen, any stream)
+ * runs with every bounded pipeline wait limited to `timeout_us` microseconds
+ * (1 .. 1,000,000), and the tensor-core issuing warp of the CTA that takes
+ * work item `item` (>= 0; item 0 is always taken) stops issuing there, as if
+ * it hung.  The waits that depend on it give up, FA_ERR_TIMEOUT is latched in
+ * the device status word, every CTA ends normally and the context stays
+ * usable; that call's gradients are undefined.  One-shot: the launch after it
+ * runs normally.  Host-side state, not thread-safe.
+ * Returns FA_OK once armed, FA_ERR_INVALID_ARG for arguments out of range,
+ * FA_ERR_UNSUPPORTED in a release build (nothing armed).
+ * (Not an operation of the pages; it tests this library's failure path.)
+ */
+int fa_debug_stall_backward(int item, unsigned timeout_us);
+
 #ifdef __cplusplus
 }
 #endif

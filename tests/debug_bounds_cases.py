@@ -6,8 +6,10 @@ Every case must leave the status word at FA_OK -- or, for the cases that feed
 a bad block-table entry or bad packed offsets on purpose, at the error those
 inputs are defined to report -- and never at FA_ERR_OUT_OF_BOUNDS.  The bad
 inputs are ones the kernels already detect and skip without touching memory
-outside the buffers; the debug build confirms that they do.  Prints one line
-per case and exits non-zero on the first failure."""
+outside the buffers; the debug build confirms that they do.  The last cases
+stall the backward's MMA warp through the debug build's injection hook: the
+call must end with FA_ERR_TIMEOUT and the next one must match a clean run.
+Prints one line per case and exits non-zero on the first failure."""
 from __future__ import annotations
 
 import os
@@ -122,6 +124,42 @@ def decode_cases():
     check("decode bad table entry", expect=(fa.FA_ERR_BAD_BLOCK_TABLE,))
 
 
+def stall_cases(so):
+    # the backward's MMA warp stops at work item 0 (debug hook) with 20 ms wait
+    # limits: the call reports FA_ERR_TIMEOUT, every CTA ends, and the next
+    # call gives the gradients of a clean run
+    def dense(d):
+        x = wl.dense_inputs(2, 4, 1000, d, seed=40 + d)
+        Q, K, V, dO = (t.to(DEV) for t in (x.Q, x.K, x.V, x.dO))
+        O, L = fa.fa_fwd(Q, K, V, causal=True)
+        return lambda: fa.fa_bwd(Q, K, V, O, dO, L, causal=True)
+
+    def packed(d):
+        x = wl.varlen_inputs([700, 1, 300, 129], 4, d, seed=50 + d)
+        Q, K, V, dO, cu = (t.to(DEV) for t in (x.Q, x.K, x.V, x.dO, x.cu_seqlens))
+        O, L = fa.fa_fwd_varlen(Q, K, V, cu, x.max_seqlen, causal=True)
+        return lambda: fa.fa_bwd_varlen(Q, K, V, O, dO, L, cu, x.max_seqlen, causal=True)
+
+    for kind, make in (("dense", dense), ("packed", packed)):
+        for d in (64, 128):
+            run = make(d)
+            ref = [t.float() for t in run()]
+            check(f"{kind} d={d} backward before the stall")
+            if so.fa_debug_stall_backward(0, 20000) != fa.FA_OK:
+                print("FAIL the stall injection did not arm")
+                sys.exit(1)
+            run()
+            check(f"{kind} d={d} backward with its MMA warp stalled", expect=(fa.FA_ERR_TIMEOUT,))
+            got = [t.float() for t in run()]
+            check(f"{kind} d={d} backward after the stall")
+            for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
+                err = (g - r).abs().max().item()
+                tol = 1e-2 * r.abs().max().item() + 1e-6
+                if not err <= tol:
+                    print(f"FAIL {kind} d={d} {name} after the stall: max error {err:.3g} > {tol:.3g}")
+                    sys.exit(1)
+
+
 if __name__ == "__main__":
     so = fa.load()
     if so.fa_debug_build() != 1:
@@ -140,4 +178,5 @@ if __name__ == "__main__":
     varlen_cases()
     paged_prefill_cases()
     decode_cases()
+    stall_cases(so)
     print("all cases in bounds")

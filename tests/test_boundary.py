@@ -46,7 +46,7 @@ def test_status_strings(so):
                        (4, "FA_ERR_TIMEOUT"), (5, "FA_ERR_BAD_BLOCK_TABLE"), (6, "FA_ERR_OUT_OF_BOUNDS")]:
         assert so.fa_status_string(code).decode() == name
     assert so.fa_status_string(99).decode() == "FA_ERR_UNKNOWN"
-    assert so.fa_version() == 106
+    assert so.fa_version() == 107
 
 
 def _fake(n=1):
@@ -211,6 +211,11 @@ def test_selftest_argument_validation(so):
     s = ctypes.c_void_p(0)
     assert so.fa_selftest_wait_timeout(0, s) == fl.FA_ERR_INVALID_ARG
     assert so.fa_selftest_wait_timeout(2000000, s) == fl.FA_ERR_INVALID_ARG
+    # the backward stall injection exists in debug builds only
+    assert so.fa_debug_stall_backward(-1, 1000) == fl.FA_ERR_INVALID_ARG
+    assert so.fa_debug_stall_backward(0, 0) == fl.FA_ERR_INVALID_ARG
+    assert so.fa_debug_stall_backward(0, 2000000) == fl.FA_ERR_INVALID_ARG
+    assert so.fa_debug_stall_backward(0, 1000) == fl.FA_ERR_UNSUPPORTED
 
 
 def test_binding_has_every_name_the_bench_and_smoke_use():
@@ -243,6 +248,8 @@ def test_debug_build_compiles_and_reports_itself():
     # the FA_DEBUG variant (device bounds checks) builds from the same sources;
     # loading it needs no GPU
     path = fab.build(debug=True)
-    r = subprocess.run([sys.executable, "-c", f"import ctypes; print(ctypes.CDLL({path!r}).fa_debug_build())"],
-                       capture_output=True, text=True, timeout=120)
-    assert r.returncode == 0 and r.stdout.strip() == "1", r.stdout + r.stderr
+    code = (f"import ctypes; so = ctypes.CDLL({path!r}); "
+            "print(so.fa_debug_build(), so.fa_debug_stall_backward(0, 1000), so.fa_debug_stall_backward(-1, 1000))")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=120)
+    # debug build; the stall injection arms (host state only) and checks its arguments
+    assert r.returncode == 0 and r.stdout.split() == ["1", str(fl.FA_OK), str(fl.FA_ERR_INVALID_ARG)], r.stdout + r.stderr
