@@ -89,17 +89,17 @@ NOMINAL = {"bf16_tflops": 2250.0, "bf16_tflops_nvl72": 2500.0, "hbm_gbs": 8000.0
 # they were taken on: a figure turns null once its source changes.
 TRAFFIC_RECORD = {
     "fwd": {"kernel": "fwd_kernel<128>", "source": "exact_io_aware_10_gb300/csrc/fa_fwd.cu",
-            "sha256": "20da90d48ea23bebe97fc7f1d361d013e990741fed534aa33d196bf35c02c436",
-            "bytes": {"N16384": 288711936 + 47219712, "N65536": 1163000064 + 249906688}},
+            "sha256": "b72d4a837b595444e629704a910b3f699e0c75f521223891f8f67bd0164f1b8e",
+            "bytes": {"N16384": 290484480 + 47442944, "N65536": 1168669952 + 249959680}},
     "bwd": {"kernel": "bwd_pre_kernel<128> + bwd_main_kernel<128> + bwd_dq_kernel",
             "source": "exact_io_aware_10_gb300/csrc/fa_bwd.cu",
-            "sha256": "0d2e43ce607cffe912a8e04307754b8872aecf933d6592a702c1350d19a1d6bd",
-            "bytes": {"N16384_main": 406574080 + 218599168, "N16384_pre": 135284480 + 87345664,
-                      "N16384_dq": 134242816 + 35207424}},
+            "sha256": "779390600a9a5a602a9e6c63669b9e3ae1dc1db0094e4ac012c5a48bdff121db",
+            "bytes": {"N16384_main": 408455424 + 221728256, "N16384_pre": 135309056 + 87567360,
+                      "N16384_dq": 134226688 + 35302400}},
     "decode": {"kernel": "decode_split_kernel<128> + decode_combine_kernel<128>",
                "source": "exact_io_aware_10_gb300/csrc/fa_decode.cu",
-               "sha256": "46f760001ee8943807a4193b3045b0ff836a7f745d5d58ca79693015f36c3d05",
-               "bytes": {"B64": 4424701440 + 17752832 + 15574272 + 0}},
+               "sha256": "6e8b1c0a29bb49b7c95dd9085703f8d4c69609ebf81e1879d21d22f2a02f8709",
+               "bytes": {"B64": 4424737536 + 17819392 + 15574272 + 0}},
 }
 # the pages' encoder and decoder training shapes (BERT-large- and GPT-2-medium-
 # shaped attention, d = 64), timed after the step, forward and backward.  Their
