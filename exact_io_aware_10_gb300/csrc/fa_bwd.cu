@@ -5,7 +5,9 @@
 //     dV = P^T dO,  dP = dO V^T,  D = rowsum(dO * O),  dS = P * (dP - D),
 //     dK = scale dS^T Q,  dQ = scale dS K.
 //
-// Three launches on one stream:
+// Three launches on one stream, the second and third as programmatic
+// dependents of the one before (their launch and set-up overlap its tail;
+// griddepcontrol.wait precedes every read of its results):
 //  1. bwd_pre_kernel   -D_i = -sum_c dO_ic O_ic and -LSE_i * log2(e) into padded
 //                      fp32 rows (0 / -inf past N), dQacc <- 0 and the main
 //                      kernel's work counter <- 0.
@@ -45,6 +47,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <math.h>
+
+#include <utility>
 
 #include "fa_internal.h"
 #include "sm103.cuh"
@@ -202,6 +206,9 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
                                                       const float* __restrict__ LSE, BwdArgs a, int BH) {
   constexpr int kLanesPerRow = D / 8;               // 16-byte chunks of a bf16 row
   constexpr int kRowsPerWarp = 32 / kLanesPerRow;  // 2 (d = 128) or 4 (d = 64)
+  // the main kernel (which waits for this grid's completion before it reads
+  // anything written here) may be scheduled once every CTA has started
+  griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int sub = lane % kLanesPerRow;
   const long long gw = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
@@ -265,6 +272,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
 __global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ dQacc, __nv_bfloat16* __restrict__ dQ,
                                                      long long n4) {
   const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  griddep_wait();  // a programmatic dependent of the main kernel: its reductions are complete
   if (i >= n4) return;
   const float4 v = reinterpret_cast<const float4*>(dQacc)[i];
   uint2 w;
@@ -383,6 +391,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // launched as a programmatic dependent of the preprocess: the set-up above
+  // overlaps its tail; its outputs (work counter, -D and -LSE2 rows, zeroed
+  // accumulator) are complete and visible from here on
+  griddep_wait();
   const uint32_t tmem = *tmem_slot;
 #ifdef FA_DEBUG
   const WaitCtx wc{abort_flag, a.status, a.dbg_timeout_ns != 0 ? a.dbg_timeout_ns : kWaitTimeoutNs};
@@ -929,6 +941,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) bulk_wait_read_all();  // staging must outlive the reductions' reads
   }
 
+  griddep_launch_dependents();  // the dQ conversion may start launching (it waits for completion)
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -937,6 +950,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 #undef BWD_CRD
+
+// Launches `kernel` as a programmatic dependent of the work before it in the
+// stream: it may be scheduled before that work completes and must wait for it
+// (griddepcontrol.wait) before touching its results.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                             Args&&... args) {
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = pdl;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  if (e != cudaSuccess) cudaGetLastError();
+  return e;
+}
 
 // The scheduler counter of the persistent kernel: 256 bytes after the fp32 dQ
 // accumulator (elements floats) in the workspace, whose -D and -LSE2 rows take
@@ -1013,11 +1047,13 @@ fa_status bwd_launch_d(const void* Q, const void* K, const void* V, const void* 
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   // one persistent CTA per SM (fewer when there are fewer work items)
   const int ctas = min(a.n_items, max(sm_count(), 1));
-  bwd_main_kernel<D, false><<<ctas, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, tdk, tdv, a);
-  if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+  if (launch_dependent(bwd_main_kernel<D, false>, dim3(ctas), dim3(kThreads), C::kSmemBytes, stream, tq, tk, tv, tdo,
+                       tdq, tdk, tdv, a) != cudaSuccess)
+    return FA_ERR_CUDA;
   const long long n4 = static_cast<long long>(BH) * N * D / 4;
-  bwd_dq_kernel<<<static_cast<unsigned>((n4 + 255) / 256), 256, 0, stream>>>(a.dQacc,
-                                                                             static_cast<__nv_bfloat16*>(dQ), n4);
+  if (launch_dependent(bwd_dq_kernel, dim3(static_cast<unsigned>((n4 + 255) / 256)), dim3(256), 0, stream,
+                       static_cast<const float*>(a.dQacc), static_cast<__nv_bfloat16*>(dQ), n4) != cudaSuccess)
+    return FA_ERR_CUDA;
   return launch_status();
 }
 
@@ -1085,11 +1121,13 @@ fa_status bwd_varlen_launch_d(const void* Q, const void* K, const void* V, const
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   // one persistent CTA per SM (fewer when there are fewer work items)
   const int ctas = min(a.n_items, max(sm_count(), 1));
-  bwd_main_kernel<D, true><<<ctas, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, tdk, tdv, a);
-  if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+  if (launch_dependent(bwd_main_kernel<D, true>, dim3(ctas), dim3(kThreads), C::kSmemBytes, stream, tq, tk, tv, tdo,
+                       tdq, tdk, tdv, a) != cudaSuccess)
+    return FA_ERR_CUDA;
   const long long n4 = static_cast<long long>(total) * H * D / 4;
-  bwd_dq_kernel<<<static_cast<unsigned>((n4 + 255) / 256), 256, 0, stream>>>(a.dQacc,
-                                                                             static_cast<__nv_bfloat16*>(dQ), n4);
+  if (launch_dependent(bwd_dq_kernel, dim3(static_cast<unsigned>((n4 + 255) / 256)), dim3(256), 0, stream,
+                       static_cast<const float*>(a.dQacc), static_cast<__nv_bfloat16*>(dQ), n4) != cudaSuccess)
+    return FA_ERR_CUDA;
   return launch_status();
 }
 
