@@ -263,7 +263,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     return x == 0 ? 0 : (w << 5) + __ffs(x) - 1;
   };
 
-  if (threadIdx.x == 0) {
+  // the producer thread sets up the barriers and, unless the key tiles come
+  // from a block mask counted above, issues both Q tiles' copies at once, so
+  // their latency overlaps the rest of the set-up
+  if (warp == 8 && lane == 0) {
     mbar_init(bar(BAR_Q), 1);
     for (int s = 0; s < C::kGroupBars; ++s) {
       mbar_init(bar(BAR_KV_FULL + s), 1);
@@ -277,15 +280,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(BAR_DRAIN), 1);
     *abort_flag = 0;
     fence_mbar_init();
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    const uint32_t qbytes = (valid_t[0] ? C::kTileBytes : 0) + (valid_t[1] ? C::kTileBytes : 0);
+    if (!sparse && qbytes != 0 && max(n_t[0], n_t[1]) > 0) {
+      mbar_arrive_expect_tx(bar(BAR_Q), qbytes);
+      for (int t = 0; t < 2; ++t) {
+        if (!valid_t[t]) continue;
+        const int row = (2 * mblk + t) * kRows;
+        for (int s = 0; s < C::kSub; ++s) {
+          const uint32_t dst = sbase + C::kOffQ + t * C::kTileBytes + s * C::kSubBytes;
+          if (packed)
+            tma_load_3d(dst, &tmQ, bar(BAR_Q), s * 64, head, tok0 + row);
+          else
+            tma_load_3d(dst, &tmQ, bar(BAR_Q), s * 64, row, bh);
+        }
+      }
+    }
   }
   if (warp == 0) {
     tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
     tmem_relinquish();
-  }
-  if (warp == 8 && lane == 0) {
-    tma_prefetch_desc(&tmQ);
-    tma_prefetch_desc(&tmK);
-    tma_prefetch_desc(&tmV);
   }
   tc_fence_before();
   __syncthreads();
@@ -313,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t qbytes = 0;
     for (int t = 0; t < 2; ++t)
       if (valid_t[t]) qbytes += C::kTileBytes;
-    if (lane == 0 && qbytes != 0 && nmax > 0) {
+    if (lane == 0 && sparse && qbytes != 0 && nmax > 0) {  // (dense: issued in the set-up)
       mbar_arrive_expect_tx(bar(BAR_Q), qbytes);
       for (int t = 0; t < 2; ++t) {
         if (!valid_t[t]) continue;
