@@ -264,8 +264,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   // the producer thread sets up the barriers and, unless the key tiles come
-  // from a block mask counted above, issues both Q tiles' copies at once, so
-  // their latency overlaps the rest of the set-up
+  // from a block mask counted above, issues both Q tiles' copies at once (and,
+  // for K/V in the Q layout, the first key tile's K), so their latency
+  // overlaps the rest of the set-up
+  const bool early_k = !sparse && !paged && max(n_t[0], n_t[1]) > 0;
   if (warp == 8 && lane == 0) {
     mbar_init(bar(BAR_Q), 1);
     for (int s = 0; s < C::kGroupBars; ++s) {
@@ -296,6 +298,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           else
             tma_load_3d(dst, &tmQ, bar(BAR_Q), s * 64, row, bh);
         }
+      }
+    }
+    if (early_k) {  // K of key tile 0 into ring slot 0: group 0 of the producer's stream
+      mbar_arrive_expect_tx(bar(BAR_KV_FULL + 0), C::kTileBytes);
+      for (int s = 0; s < C::kSub; ++s) {
+        const uint32_t dst = sbase + C::kOffKV + s * C::kSubBytes;
+        if (packed)
+          tma_load_3d(dst, &tmK, bar(BAR_KV_FULL + 0), s * 64, head, tok0);
+        else
+          tma_load_3d(dst, &tmK, bar(BAR_KV_FULL + 0), s * 64, 0, bh);
       }
     }
   }
@@ -400,6 +412,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               bad_table = true;
           }
         }
+      }
+      if (p == 0 && early_k) {  // group 0 was issued in the set-up
+        groups = 1;
+        continue;
       }
       const uint32_t fb = bar(BAR_KV_FULL + gb);
       if (lane == 0) mbar_arrive_expect_tx(fb, (has_v ? C::kTileBytes : 0) + (has_k ? C::kTileBytes : 0));
