@@ -89,13 +89,13 @@ NOMINAL = {"bf16_tflops": 2250.0, "bf16_tflops_nvl72": 2500.0, "hbm_gbs": 8000.0
 # they were taken on: a figure turns null once its source changes.
 TRAFFIC_RECORD = {
     "fwd": {"kernel": "fwd_kernel<128>", "source": "exact_io_aware_10_gb300/csrc/fa_fwd.cu",
-            "sha256": "b72d4a837b595444e629704a910b3f699e0c75f521223891f8f67bd0164f1b8e",
-            "bytes": {"N16384": 290484480 + 47442944, "N65536": 1168669952 + 249959680}},
+            "sha256": "810103c9a811dc7070af0a02a46cf28c57fc79cb2b3b43062523501fd85a6f02",
+            "bytes": {"N16384": 292225536 + 47164416, "N65536": 1162675968 + 249976320}},
     "bwd": {"kernel": "bwd_pre_kernel<128> + bwd_main_kernel<128> + bwd_dq_kernel",
             "source": "exact_io_aware_10_gb300/csrc/fa_bwd.cu",
-            "sha256": "779390600a9a5a602a9e6c63669b9e3ae1dc1db0094e4ac012c5a48bdff121db",
-            "bytes": {"N16384_main": 408455424 + 221728256, "N16384_pre": 135309056 + 87567360,
-                      "N16384_dq": 134226688 + 35302400}},
+            "sha256": "10fbfb335a105ce5398437cc6af8c774dafa2956067816ae21b8aaa21ab6bd16",
+            "bytes": {"N16384_main": 407458048 + 222651136, "N16384_pre": 135284480 + 87094016,
+                      "N16384_dq": 134230272 + 35260416}},
     "decode": {"kernel": "decode_split_kernel<128> + decode_combine_kernel<128>",
                "source": "exact_io_aware_10_gb300/csrc/fa_decode.cu",
                "sha256": "6e8b1c0a29bb49b7c95dd9085703f8d4c69609ebf81e1879d21d22f2a02f8709",
