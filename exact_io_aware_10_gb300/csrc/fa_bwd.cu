@@ -104,8 +104,6 @@ enum : int {
   BAR_DRAIN = 18,
   kNumBars = 19,
 };
-constexpr int kOffTmemSlot = kNumBars * 8;
-constexpr int kOffAbort = kOffTmemSlot + 4;
 constexpr int kComputeWarps = 16;
 // warp 18 folds the wait for the next query tile into the dS barrier
 // (measured: 2 % faster at d = 128; at d = 64 2 % slower while dQ went out as
@@ -231,14 +229,12 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
   float acc = 0.f;
   size_t row = 0;
   if (live) {
-    const size_t row0 = a.cu_seqlens != nullptr ? static_cast<size_t>(tok0 + r) * a.H + bh % a.H
-                                                : static_cast<size_t>(bh) * a.N + r;
-    live = FA_IN_BOUNDS(static_cast<long long>(row0), a.dbg_rows, a.status);
-  }
-  if (live) {
     // [B, H, N, D] rows, or [total, H, D] rows when packed (LSE [H, total])
     row = a.cu_seqlens != nullptr ? static_cast<size_t>(tok0 + r) * a.H + bh % a.H
                                   : static_cast<size_t>(bh) * a.N + r;
+    live = FA_IN_BOUNDS(static_cast<long long>(row), a.dbg_rows, a.status);
+  }
+  if (live) {
     const uint4 o = *reinterpret_cast<const uint4*>(O + row * D + 8 * sub);
     const uint4 g = *reinterpret_cast<const uint4*>(dO + row * D + 8 * sub);
     const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&o);
