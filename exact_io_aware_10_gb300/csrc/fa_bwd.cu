@@ -79,7 +79,11 @@ struct BwdCfg {
   static constexpr int kStageBytes = (D == 128) ? 2 * 16384 : 4 * 8192;
   static constexpr int kOffSide = kOffStage + kStageBytes;  // 2 x (-LSE2[128], -D[128])
   static constexpr int kOffBar = kOffSide + 2 * 1024;
-  static constexpr int kUsedBytes = kOffBar + 256;
+  // d = 64 has room for a second K, V pair: consecutive work items alternate
+  // between the two, so the next item's K and V load while the current one runs
+  static constexpr int kKVBufs = (D == 64) ? 2 : 1;
+  static constexpr int kOffKV1 = (kOffBar + 256 + 1023) / 1024 * 1024;
+  static constexpr int kUsedBytes = (kKVBufs == 2) ? kOffKV1 + 2 * kTileBytes : kOffBar + 256;
   static constexpr int kSmemBytes = (kUsedBytes + 1024 <= 232448) ? kUsedBytes + 1024 : 232448;
   static constexpr int kMaxPad = kSmemBytes - kUsedBytes;  // alignment padding the allocation can absorb
   static constexpr uint32_t kTmemCols = 512;
@@ -292,7 +296,9 @@ enum : int {
   BAR_SCHED_EMPTY = kNumBars + 2,  // + slot (2): every consumer has read it
   BAR_KV_EMPTY = kNumBars + 4,     // the item's last MMA has read K and V
   BAR_DKV_FREE = kNumBars + 5,     // the item's dK and dV read out of TMEM
-  kNumBarsP = kNumBars + 6,
+  BAR_KV1 = kNumBars + 6,          // d = 64: the second K, V pair (BAR_KV, BAR_KV_EMPTY: the first)
+  BAR_KV_EMPTY1 = kNumBars + 7,
+  kNumBarsP = kNumBars + 8,
 };
 constexpr int kOffTmemSlotP = kNumBarsP * 8;
 constexpr int kOffAbortP = kOffTmemSlotP + 4;
@@ -376,6 +382,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(BAR_FINAL), 1);
     mbar_init(bar(BAR_DRAIN), 1);
     mbar_init(bar(BAR_KV_EMPTY), 1);
+    mbar_init(bar(BAR_KV1), 1);
+    mbar_init(bar(BAR_KV_EMPTY1), 1);
     mbar_init(bar(BAR_DKV_FREE), kComputeWarps);
     *abort_flag = 0;
     fence_mbar_init();
@@ -409,6 +417,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     item = sched_slot[k & 1];
     return true;
   };
+  // K, V buffer of the kf-th item with work, and how many times it was used before
+  auto kv_slot = [](int kf) { return C::kKVBufs == 2 ? (kf & 1) : 0; };
+  auto kv_use = [](int kf) { return C::kKVBufs == 2 ? (kf >> 1) : kf; };
+  auto kv_full = [&](int slot) { return bar(slot ? BAR_KV1 : BAR_KV); };
+  auto kv_empty = [&](int slot) { return bar(slot ? BAR_KV_EMPTY1 : BAR_KV_EMPTY); };
 
   if (warp >= kComputeWarps) {
     regs_dealloc<kRegsOther<D>>();
@@ -440,15 +453,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           BwdItem<kPacked> w;
           if (!w.decode(a, item) || w.nt == 0) continue;
           const size_t side_row = static_cast<size_t>(w.bh) * a.Npad;
-          // K_j, V_j once the previous item's last MMA has read the old ones
-          if (kf > 0 && !mbar_wait(bar(BAR_KV_EMPTY), static_cast<uint32_t>(kf - 1) & 1u, wc)) {
+          // K_j, V_j once the last MMA of the item that used this buffer before has read it
+          const int ks = kv_slot(kf), ku = kv_use(kf);
+          if (ku > 0 && !mbar_wait(kv_empty(ks), static_cast<uint32_t>(ku - 1) & 1u, wc)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(bar(BAR_KV), 2 * C::kTileBytes);
+          const uint32_t kvb = sbase + (ks ? C::kOffKV1 : C::kOffK);
+          mbar_arrive_expect_tx(kv_full(ks), 2 * C::kTileBytes);
           for (int s = 0; s < C::kSub; ++s) {
-            tma_load_3d(sbase + C::kOffK + s * C::kSubBytes, &tmK, bar(BAR_KV), s * 64, BWD_CRD(w.j * kTile));
-            tma_load_3d(sbase + C::kOffV + s * C::kSubBytes, &tmV, bar(BAR_KV), s * 64, BWD_CRD(w.j * kTile));
+            tma_load_3d(kvb + s * C::kSubBytes, &tmK, kv_full(ks), s * 64, BWD_CRD(w.j * kTile));
+            tma_load_3d(kvb + C::kTileBytes + s * C::kSubBytes, &tmV, kv_full(ks), s * 64, BWD_CRD(w.j * kTile));
           }
           kv_issued = kf + 1;
           for (int it = 0; it < w.nt; ++it) {
@@ -492,7 +507,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           kf += 1;
         }
         // every issued copy lands before the CTA can exit
-        if (kv_issued > 0) drain_wait(bar(BAR_KV), static_cast<uint32_t>(kv_issued - 1) & 1u);
+        for (int s = 0; s < C::kKVBufs && s < kv_issued; ++s) {
+          const int last = s + C::kKVBufs * ((kv_issued - 1 - s) / C::kKVBufs);  // its last item
+          drain_wait(kv_full(s), static_cast<uint32_t>(kv_use(last)) & 1u);
+        }
         for (int s = 0; s < 2 && s < q_issued; ++s) {
           const int last = s + 2 * ((q_issued - 1 - s) / 2);
           drain_wait(bar(BAR_Q_FULL + s), (last >> 1) & 1);
@@ -511,9 +529,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t sK = sbase + C::kOffK, sV = sbase + C::kOffV, sP = sbase + C::kOffP;
         auto q_addr = [&](int g) { return sbase + C::kOffRing + (g & 1) * C::kTileBytes; };
         const uint32_t aO = sbase + C::kOffRing + 2 * C::kTileBytes;
-        const uint64_t kK = sdesc_sw128(sK, 16, 1024), kV = sdesc_sw128(sV, 16, 1024);
+        const uint64_t kK0 = sdesc_sw128(sK, 16, 1024), kV0 = sdesc_sw128(sV, 16, 1024);
         const uint64_t kP = sdesc_sw128(sP, 16, 1024), kO = sdesc_sw128(aO, 16, 1024);
-        const uint64_t mK = sdesc_sw128(sK, C::kSubBytes, 1024), mP = sdesc_sw128(sP, C::kSubBytes, 1024);
+        const uint64_t mK0 = sdesc_sw128(sK, C::kSubBytes, 1024), mP = sdesc_sw128(sP, C::kSubBytes, 1024);
         const uint64_t mO = sdesc_sw128(aO, C::kSubBytes, 1024);
         const uint64_t kQ0 = sdesc_sw128(q_addr(0), 16, 1024), mQ0 = sdesc_sw128(q_addr(0), C::kSubBytes, 1024);
         auto kq = [&](int g) { return sdesc_advance(kQ0, (g & 1) * C::kTileBytes); };
@@ -541,7 +559,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           BwdItem<kPacked> w;
           if (!w.decode(a, item) || w.nt == 0) continue;
           const int nt = w.nt;
-          if (!(ok = mbar_wait(bar(BAR_KV), static_cast<uint32_t>(kf) & 1u, wc))) break;
+          const int ks = kv_slot(kf);
+          if (!(ok = mbar_wait(kv_full(ks), static_cast<uint32_t>(kv_use(kf)) & 1u, wc))) break;
+          // descriptors of this item's K, V buffer: the first pair's advanced by the offset
+          // (start address in 16-byte units, the descriptor's low bits)
+          const uint32_t kvo = ks ? static_cast<uint32_t>((C::kOffKV1 - C::kOffK) >> 4) : 0u;
+          // (formed at each use, not kept live: the issuing thread's registers are tight)
+          auto at_kv = [&](uint64_t d0) {
+            if constexpr (C::kKVBufs == 1) return d0;
+            uint64_t r;
+            asm volatile("add.u64 %0, %1, %2;" : "=l"(r) : "l"(d0), "l"(static_cast<uint64_t>(kvo)));
+            return r;
+          };
+#define kK at_kv(kK0)
+#define kV at_kv(kV0)
+#define mK at_kv(mK0)
           // prologue: S_0 and dP_0; dP_0 overwrites the previous item's last dQ
           if (!(ok = mbar_wait(bar(BAR_Q_FULL + (gs & 1)), (gs >> 1) & 1, wc))) break;
           tc_fence_after();
@@ -614,7 +646,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (!ok) break;
           mma_commit(bar(BAR_FINAL));
-          mma_commit(bar(BAR_KV_EMPTY));
+          mma_commit(kv_empty(ks));
+#undef kK
+#undef kV
+#undef mK
           gs += nt;
           kf += 1;
         }
