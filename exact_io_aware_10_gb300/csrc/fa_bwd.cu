@@ -17,7 +17,8 @@
 //                      a group the key tiles with most query tiles first, so
 //                      the items in flight share a few heads' Q, dO and dQ
 //                      accumulator in L2.  K_j and V_j stay in shared
-//                      memory; the CTA streams the query tiles i that see
+//                      memory (d = 64: two K, V buffers, so the next item's
+//                      load overlaps this one); the CTA streams the query tiles i that see
 //                      tile j and, per tile, runs five tcgen05 MMAs with fp32
 //                      accumulators in TMEM:
 //                        S^T  = K_j Q_i^T          (TMEM cols   0..127)
