@@ -93,9 +93,9 @@ TRAFFIC_RECORD = {
             "bytes": {"N16384": 292225536 + 47164416, "N65536": 1162675968 + 249976320}},
     "bwd": {"kernel": "bwd_pre_kernel<128> + bwd_main_kernel<128> + bwd_dq_kernel",
             "source": "exact_io_aware_10_gb300/csrc/fa_bwd.cu",
-            "sha256": "0c71d8e88fae3cc839c741e4f744874fa52767c5c2d93555855d83208e914b21",
-            "bytes": {"N16384_main": 408014336 + 220774144, "N16384_pre": 135283200 + 87257344,
-                      "N16384_dq": 134224896 + 35167744}},
+            "sha256": "e06c225b62ba9dc12391b443c261099cb44fdbbf8d89955939bb8233bcad4638",
+            "bytes": {"N16384_main": 408278784 + 221385728, "N16384_pre": 135286272 + 87011584,
+                      "N16384_dq": 134232320 + 35276032}},
     "decode": {"kernel": "decode_split_kernel<128> + decode_combine_kernel<128>",
                "source": "exact_io_aware_10_gb300/csrc/fa_decode.cu",
                "sha256": "6e8b1c0a29bb49b7c95dd9085703f8d4c69609ebf81e1879d21d22f2a02f8709",
