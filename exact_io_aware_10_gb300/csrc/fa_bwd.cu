@@ -17,8 +17,8 @@
 //                      a group the key tiles with most query tiles first, so
 //                      the items in flight share a few heads' Q, dO and dQ
 //                      accumulator in L2.  K_j and V_j stay in shared
-//                      memory (d = 64: two K, V buffers, so the next item's
-//                      load overlaps this one); the CTA streams the query tiles i that see
+//                      memory (d = 64, short items: two K, V buffers, so the
+//                      next item's load overlaps this one); the CTA streams the query tiles i that see
 //                      tile j and, per tile, runs five tcgen05 MMAs with fp32
 //                      accumulators in TMEM:
 //                        S^T  = K_j Q_i^T          (TMEM cols   0..127)
@@ -110,6 +110,7 @@ enum : int {
   kNumBars = 19,
 };
 constexpr int kComputeWarps = 16;
+constexpr int kAltMaxTiles = 8;  // d = 64: items of at most this many query tiles alternate K, V buffers
 // warp 18 folds the wait for the next query tile into the dS barrier
 // (measured: 2 % faster at d = 128; at d = 64 2 % slower while dQ went out as
 // per-thread reductions, 1.4-2.3 % faster with the staged TMA reductions)
@@ -419,8 +420,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     return true;
   };
   // K, V buffer of the kf-th item with work, and how many times it was used before
-  auto kv_slot = [](int kf) { return C::kKVBufs == 2 ? (kf & 1) : 0; };
-  auto kv_use = [](int kf) { return C::kKVBufs == 2 ? (kf >> 1) : kf; };
+  // (alternating only pays for short items: at most kAltMaxTiles query tiles)
+  const bool kv_alt = C::kKVBufs == 2 && a.nq <= kAltMaxTiles;
+  auto kv_slot = [&](int kf) { return kv_alt ? (kf & 1) : 0; };
+  auto kv_use = [&](int kf) { return kv_alt ? (kf >> 1) : kf; };
   auto kv_full = [&](int slot) { return bar(slot ? BAR_KV1 : BAR_KV); };
   auto kv_empty = [&](int slot) { return bar(slot ? BAR_KV_EMPTY1 : BAR_KV_EMPTY); };
 
@@ -508,8 +511,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           kf += 1;
         }
         // every issued copy lands before the CTA can exit
-        for (int s = 0; s < C::kKVBufs && s < kv_issued; ++s) {
-          const int last = s + C::kKVBufs * ((kv_issued - 1 - s) / C::kKVBufs);  // its last item
+        const int kv_bufs = kv_alt ? 2 : 1;
+        for (int s = 0; s < kv_bufs && s < kv_issued; ++s) {
+          const int last = s + kv_bufs * ((kv_issued - 1 - s) / kv_bufs);  // its last item
           drain_wait(kv_full(s), static_cast<uint32_t>(kv_use(last)) & 1u);
         }
         for (int s = 0; s < 2 && s < q_issued; ++s) {
