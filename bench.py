@@ -93,9 +93,9 @@ TRAFFIC_RECORD = {
             "bytes": {"N16384": 292225536 + 47164416, "N65536": 1162675968 + 249976320}},
     "bwd": {"kernel": "bwd_pre_kernel<128> + bwd_main_kernel<128> + bwd_dq_kernel",
             "source": "exact_io_aware_10_gb300/csrc/fa_bwd.cu",
-            "sha256": "e06c225b62ba9dc12391b443c261099cb44fdbbf8d89955939bb8233bcad4638",
-            "bytes": {"N16384_main": 408278784 + 221385728, "N16384_pre": 135286272 + 87011584,
-                      "N16384_dq": 134232320 + 35276032}},
+            "sha256": "722976fd7bd9ac70f476cf737504b82e9fd81e17cc862492b6614651dafbc013",
+            "bytes": {"N16384_main": 407897856 + 221731584, "N16384_pre": 135282944 + 87246080,
+                      "N16384_dq": 134223872 + 35233024}},
     "decode": {"kernel": "decode_split_kernel<128> + decode_combine_kernel<128>",
                "source": "exact_io_aware_10_gb300/csrc/fa_decode.cu",
                "sha256": "6e8b1c0a29bb49b7c95dd9085703f8d4c69609ebf81e1879d21d22f2a02f8709",
