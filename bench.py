@@ -89,8 +89,8 @@ NOMINAL = {"bf16_tflops": 2250.0, "bf16_tflops_nvl72": 2500.0, "hbm_gbs": 8000.0
 # they were taken on: a figure turns null once its source changes.
 TRAFFIC_RECORD = {
     "fwd": {"kernel": "fwd_kernel<128>", "source": "exact_io_aware_10_gb300/csrc/fa_fwd.cu",
-            "sha256": "810103c9a811dc7070af0a02a46cf28c57fc79cb2b3b43062523501fd85a6f02",
-            "bytes": {"N16384": 292225536 + 47164416, "N65536": 1162675968 + 249976320}},
+            "sha256": "26630fc7dc7b0f6442529e1db8b7efb0e9a6d59cb55ab7bcf80077e599bed526",
+            "bytes": {"N16384": 294786304 + 47980032, "N65536": 1169585920 + 249820672}},
     "bwd": {"kernel": "bwd_pre_kernel<128> + bwd_main_kernel<128> + bwd_dq_kernel",
             "source": "exact_io_aware_10_gb300/csrc/fa_bwd.cu",
             "sha256": "722976fd7bd9ac70f476cf737504b82e9fd81e17cc862492b6614651dafbc013",

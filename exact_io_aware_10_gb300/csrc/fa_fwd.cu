@@ -123,8 +123,23 @@ struct FwdArgs {
   // O (D elements each), elements of LSE, bytes of the block mask
   int dbg_nb;
   long long dbg_o_rows, dbg_lse_len, dbg_mask_bytes;
+  long long dbg_stall_cta;            // the MMA warp of this CTA (linear index) issues nothing (-1: none)
+  unsigned long long dbg_timeout_ns;  // wait limit of this launch (0: the default)
 #endif
 };
+
+#ifdef FA_DEBUG
+// One-shot stall armed by fa_debug_stall_forward, taken by the next forward
+// launch (host side, not thread-safe: a debug hook).
+long long g_fwd_stall_cta = -1;
+unsigned long long g_fwd_stall_timeout_ns = 0;
+void take_forward_stall(FwdArgs& a) {
+  a.dbg_stall_cta = g_fwd_stall_cta;
+  a.dbg_timeout_ns = g_fwd_stall_timeout_ns;
+  g_fwd_stall_cta = -1;
+  g_fwd_stall_timeout_ns = 0;
+}
+#endif
 
 // Wait for a barrier phase ignoring the abort flag, for at most ~50 ms; used
 // only on the exit path to let in-flight asynchronous work land.
@@ -324,7 +339,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const int nmax = max(n_t[0], n_t[1]);
   const uint32_t tmem = *tmem_slot;
+#ifdef FA_DEBUG
+  const WaitCtx wc{abort_flag, args.status, args.dbg_timeout_ns != 0 ? args.dbg_timeout_ns : kWaitTimeoutNs};
+#else
   const WaitCtx wc{abort_flag, args.status};
+#endif
 
   if (warp >= 8) {
    regs_dealloc<kRegsOther>();
@@ -476,6 +495,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ts(dcol, acol + 8 * k, sdesc_advance(db, k * 16 * 128), idPV, (acc || k > 0) ? 1u : 0u);
       };
       bool ok = mbar_wait(bar(BAR_Q), 0, wc);
+#ifdef FA_DEBUG
+      const long long cta = blockIdx.x + static_cast<long long>(gridDim.x) *
+                                             (blockIdx.y + static_cast<long long>(gridDim.y) * blockIdx.z);
+      if (cta == args.dbg_stall_cta) ok = false;  // injected stall: this warp issues nothing
+#endif
       if (ok) ok = mbar_wait(bar(BAR_KV_FULL + 0), 0, wc);  // group 0: K_0
       if (ok) {
         tc_fence_after();
@@ -720,6 +744,7 @@ fa_status fwd_launch_d(const void* Q, const void* K, const void* V, void* O, flo
   a.dbg_o_rows = a.dbg_lse_len = static_cast<long long>(B) * H * N;
   a.dbg_mask_bytes = block_mask == nullptr ? 0 : (mask_stride != 0 ? static_cast<long long>(B) * H * mask_stride
                                                                      : static_cast<long long>(a.nkb) * a.nkb);
+  take_forward_stall(a);
 #endif
   dim3 grid(a.head_group, ceil_div(N, 2 * kRows), B * ceil_div(H, a.head_group));
   fwd_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, a);
@@ -758,6 +783,7 @@ fa_status fwd_varlen_launch_d(const void* Q, const void* K, const void* V, void*
   a.dbg_nb = num_seqs;
   a.dbg_o_rows = a.dbg_lse_len = static_cast<long long>(total) * H;
   a.dbg_mask_bytes = 0;
+  take_forward_stall(a);
 #endif
   dim3 grid(H, ceil_div(max_seqlen, 2 * kRows), num_seqs);
   fwd_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, a);
@@ -811,6 +837,7 @@ fa_status fwd_paged_launch_d(const void* q, const void* k_cache, const void* v_c
   a.dbg_nb = num_seqs;
   a.dbg_o_rows = a.dbg_lse_len = static_cast<long long>(total_q) * Hq;
   a.dbg_mask_bytes = 0;
+  take_forward_stall(a);
 #endif
   dim3 grid(Hq, ceil_div(max_seqlen_q, 2 * kRows), num_seqs);
   fwd_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, a);
@@ -818,6 +845,18 @@ fa_status fwd_paged_launch_d(const void* q, const void* k_cache, const void* v_c
 }
 
 }  // namespace
+
+bool arm_forward_stall(long long cta, unsigned long long timeout_ns) {
+#ifdef FA_DEBUG
+  g_fwd_stall_cta = cta;
+  g_fwd_stall_timeout_ns = timeout_ns;
+  return true;
+#else
+  (void)cta;
+  (void)timeout_ns;
+  return false;
+#endif
+}
 
 fa_status fwd_paged_launch(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
                            const int32_t* cu_seqlens_q, const int32_t* seq_lens_k, void* o, float* lse,

@@ -375,6 +375,23 @@ int fa_selftest_bounds(void* stream);
  */
 int fa_debug_stall_backward(int item, unsigned timeout_us);
 
+/*
+ * Failure injection for the forward pass (debug builds only): the next
+ * forward launch (fa_fwd, fa_fwd_ex, fa_fwd_block_sparse, fa_fwd_varlen or
+ * fa_paged_prefill, any stream) runs with every bounded pipeline wait limited
+ * to `timeout_us` microseconds (1 .. 1,000,000), and the tensor-core issuing
+ * warp of the CTA with linear block index `cta` (blockIdx.x + gridDim.x *
+ * (blockIdx.y + gridDim.y * blockIdx.z); CTA 0 holds the first head's longest
+ * query-tile pair, or the first sequence's last one) issues nothing, as if it
+ * hung.  The waits that depend on it give up, FA_ERR_TIMEOUT is latched in the
+ * device status word, every CTA ends normally and the context stays usable;
+ * that call's outputs are undefined.  One-shot; host-side state, not
+ * thread-safe.  Returns FA_OK once armed, FA_ERR_INVALID_ARG for arguments out
+ * of range, FA_ERR_UNSUPPORTED in a release build (nothing armed).
+ * (Not an operation of the pages; it tests this library's failure path.)
+ */
+int fa_debug_stall_forward(int cta, unsigned timeout_us);
+
 #ifdef __cplusplus
 }
 #endif

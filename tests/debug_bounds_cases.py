@@ -7,8 +7,9 @@ a bad block-table entry or bad packed offsets on purpose, at the error those
 inputs are defined to report -- and never at FA_ERR_OUT_OF_BOUNDS.  The bad
 inputs are ones the kernels already detect and skip without touching memory
 outside the buffers; the debug build confirms that they do.  The last cases
-stall the backward's MMA warp through the debug build's injection hook: the
-call must end with FA_ERR_TIMEOUT and the next one must match a clean run.
+stall the backward's, then the forward's, MMA warp through the debug build's
+injection hooks: the call must end with FA_ERR_TIMEOUT and the next one must
+match a clean run.
 Prints one line per case and exits non-zero on the first failure."""
 from __future__ import annotations
 
@@ -160,6 +161,37 @@ def stall_cases(so):
                     sys.exit(1)
 
 
+def forward_stall_cases(so):
+    # the forward's MMA warp in CTA 0 issues nothing (debug hook) with 20 ms wait
+    # limits: the call reports FA_ERR_TIMEOUT, every CTA ends, the next call is clean
+    def dense(d):
+        x = wl.dense_inputs(2, 4, 1000, d, seed=60 + d)
+        Q, K, V = (t.to(DEV) for t in (x.Q, x.K, x.V))
+        return lambda: fa.fa_fwd(Q, K, V, causal=True)
+
+    def packed(d):
+        x = wl.varlen_inputs([700, 1, 300, 129], 4, d, seed=70 + d)  # sequence 0 is the longest
+        Q, K, V, cu = (t.to(DEV) for t in (x.Q, x.K, x.V, x.cu_seqlens))
+        return lambda: fa.fa_fwd_varlen(Q, K, V, cu, x.max_seqlen, causal=True)
+
+    for kind, make in (("dense", dense), ("packed", packed)):
+        for d in (64, 128):
+            run = make(d)
+            ref = [t.float() for t in run()]
+            check(f"{kind} d={d} forward before the stall")
+            if so.fa_debug_stall_forward(0, 20000) != fa.FA_OK:
+                print("FAIL the forward stall injection did not arm")
+                sys.exit(1)
+            run()
+            check(f"{kind} d={d} forward with its MMA warp stalled", expect=(fa.FA_ERR_TIMEOUT,))
+            got = [t.float() for t in run()]
+            check(f"{kind} d={d} forward after the stall")
+            for name, g, r in zip(("O", "LSE"), got, ref):
+                if not torch.equal(g, r):
+                    print(f"FAIL {kind} d={d} {name} after the stall differs from the clean run")
+                    sys.exit(1)
+
+
 if __name__ == "__main__":
     so = fa.load()
     if so.fa_debug_build() != 1:
@@ -179,4 +211,5 @@ if __name__ == "__main__":
     paged_prefill_cases()
     decode_cases()
     stall_cases(so)
+    forward_stall_cases(so)
     print("all cases in bounds")
