@@ -98,8 +98,8 @@ TRAFFIC_RECORD = {
                       "N16384_dq": 134223872 + 35233024}},
     "decode": {"kernel": "decode_split_kernel<128> + decode_combine_kernel<128>",
                "source": "exact_io_aware_10_gb300/csrc/fa_decode.cu",
-               "sha256": "6e8b1c0a29bb49b7c95dd9085703f8d4c69609ebf81e1879d21d22f2a02f8709",
-               "bytes": {"B64": 4424737536 + 17819392 + 15574272 + 0}},
+               "sha256": "96643620437889a50b50449cfba8585c7840c835eb6f35ec53c73832317d557e",
+               "bytes": {"B64": 4425079040 + 17810688 + 15574272 + 0}},
 }
 # the pages' encoder and decoder training shapes (BERT-large- and GPT-2-medium-
 # shaped attention, d = 64), timed after the step, forward and backward.  Their

@@ -209,7 +209,7 @@ const char* fa_status_string(int status) {
   }
 }
 
-int fa_version(void) { return 108; }
+int fa_version(void) { return 109; }
 
 int fa_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d, int causal,
               float scale, const int32_t* kv_lens, void* stream) {
@@ -375,6 +375,12 @@ int fa_debug_stall_forward(int cta, unsigned timeout_us) {
   if (cta < 0 || timeout_us == 0 || timeout_us > 1000000u) return FA_ERR_INVALID_ARG;
   return fa::arm_forward_stall(cta, static_cast<unsigned long long>(timeout_us) * 1000ull) ? FA_OK
                                                                                            : FA_ERR_UNSUPPORTED;
+}
+
+int fa_debug_stall_decode(int cta, unsigned timeout_us) {
+  if (cta < 0 || timeout_us == 0 || timeout_us > 1000000u) return FA_ERR_INVALID_ARG;
+  return fa::arm_decode_stall(cta, static_cast<unsigned long long>(timeout_us) * 1000ull) ? FA_OK
+                                                                                         : FA_ERR_UNSUPPORTED;
 }
 
 int fa_selftest_wait_timeout(unsigned timeout_us, void* stream) {

@@ -75,7 +75,24 @@ struct DecArgs {
   int min_blocks;  // smallest split, in blocks
   float scale_log2;
   unsigned* status;
+#ifdef FA_DEBUG
+  long long dbg_stall_cta;            // the producer of this split CTA (linear index) loads nothing (-1: none)
+  unsigned long long dbg_timeout_ns;  // wait limit of this launch (0: the default)
+#endif
 };
+
+#ifdef FA_DEBUG
+// One-shot stall armed by fa_debug_stall_decode, taken by the next decode
+// launch (host side, not thread-safe: a debug hook).
+long long g_dec_stall_cta = -1;
+unsigned long long g_dec_stall_timeout_ns = 0;
+void take_decode_stall(DecArgs& a) {
+  a.dbg_stall_cta = g_dec_stall_cta;
+  a.dbg_timeout_ns = g_dec_stall_timeout_ns;
+  g_dec_stall_cta = -1;
+  g_dec_stall_timeout_ns = 0;
+}
+#endif
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
@@ -150,7 +167,11 @@ __global__ void __launch_bounds__(kThreads, 3)
     fence_mbar_init();
   }
   __syncthreads();
+#ifdef FA_DEBUG
+  const WaitCtx wc{abort_flag, a.status, a.dbg_timeout_ns != 0 ? a.dbg_timeout_ns : kWaitTimeoutNs};
+#else
   const WaitCtx wc{abort_flag, a.status};
+#endif
 
   // per-thread softmax state for rows r0 = lane / 4 and r0 + 8 of the group
   float m_run[2] = {-INFINITY, -INFINITY};
@@ -165,7 +186,13 @@ __global__ void __launch_bounds__(kThreads, 3)
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       int issued = 0;
-      for (int i = 0; i < nblk; ++i) {
+      int n_load = nblk;
+#ifdef FA_DEBUG
+      const long long cta = blockIdx.x + static_cast<long long>(gridDim.x) *
+                                             (blockIdx.y + static_cast<long long>(gridDim.y) * blockIdx.z);
+      if (cta == a.dbg_stall_cta) n_load = 0;  // injected stall: this warp loads nothing
+#endif
+      for (int i = 0; i < n_load; ++i) {
         const int st = i % kStages;
         if (!mbar_wait(empty(st), ((i / kStages) & 1) ^ 1, wc)) break;
         const int chunk_key = (lo + i) * kBlk;
@@ -457,6 +484,9 @@ fa_status decode_launch_d(const void* q, const void* k_cache, const void* v_cach
   a.min_blocks = (static_cast<long long>(B) * Hkv >= kFewUnits) ? kMinBlocksPerSplit : kMinBlocksPerSplitFew;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.status = status;
+#ifdef FA_DEBUG
+  take_decode_stall(a);
+#endif
   // Both kernels are programmatic dependents of whatever precedes them in the
   // stream: their launch and start-up overlap the previous kernel's tail (a
   // decode step is a chain of short kernels, one pair per layer).
@@ -552,6 +582,18 @@ float* decode_scratch_ptr(cudaStream_t stream) {
 }
 
 }  // namespace
+
+bool arm_decode_stall(long long cta, unsigned long long timeout_ns) {
+#ifdef FA_DEBUG
+  g_dec_stall_cta = cta;
+  g_dec_stall_timeout_ns = timeout_ns;
+  return true;
+#else
+  (void)cta;
+  (void)timeout_ns;
+  return false;
+#endif
+}
 }  // namespace fa
 
 extern "C" int fa_paged_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,

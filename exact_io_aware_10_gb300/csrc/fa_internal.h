@@ -76,6 +76,9 @@ bool arm_backward_stall(int item, unsigned long long timeout_ns);
 // FA_DEBUG builds: arm a one-shot stall of the forward's MMA warp in CTA
 // `cta` (linear block index) with wait limit `timeout_ns`; false in release.
 bool arm_forward_stall(long long cta, unsigned long long timeout_ns);
+// FA_DEBUG builds: arm a one-shot stall of the paged decode split kernel's
+// producer in CTA `cta` (linear block index); false in release builds.
+bool arm_decode_stall(long long cta, unsigned long long timeout_ns);
 // Loads the tensor-map encoder entry point if needed; false if unavailable.
 bool encode_init();
 // Argument checks shared by every paged-decode entry point (with and without

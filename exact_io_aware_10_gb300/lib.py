@@ -51,6 +51,7 @@ SIGNATURES = {
     "fa_selftest_bounds": (_i, [_vp]),
     "fa_debug_stall_backward": (_i, [_i, ctypes.c_uint]),
     "fa_debug_stall_forward": (_i, [_i, ctypes.c_uint]),
+    "fa_debug_stall_decode": (_i, [_i, ctypes.c_uint]),
     "fa_paged_decode_noalloc": (_i, [_vp] * 7 + [_i] * 8 + [_f, _vp]),
 }
 

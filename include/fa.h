@@ -392,6 +392,23 @@ int fa_debug_stall_backward(int item, unsigned timeout_us);
  */
 int fa_debug_stall_forward(int cta, unsigned timeout_us);
 
+/*
+ * Failure injection for paged decode (debug builds only): the next decode
+ * launch (fa_paged_decode or fa_paged_decode_noalloc, any stream; a decode
+ * graph created next captures it) runs with every bounded pipeline wait
+ * limited to `timeout_us` microseconds (1 .. 1,000,000), and the TMA warp of
+ * the split kernel's CTA with linear block index `cta` (split + splits *
+ * (KV head + Hkv * sequence); CTA 0 is the first sequence's first split)
+ * loads nothing, as if it hung.  Its consumers' waits give up,
+ * FA_ERR_TIMEOUT is latched in the device status word, every CTA ends
+ * normally and the context stays usable; that call's output is undefined.
+ * One-shot; host-side state, not thread-safe.  Returns FA_OK once armed,
+ * FA_ERR_INVALID_ARG for arguments out of range, FA_ERR_UNSUPPORTED in a
+ * release build (nothing armed).
+ * (Not an operation of the pages; it tests this library's failure path.)
+ */
+int fa_debug_stall_decode(int cta, unsigned timeout_us);
+
 #ifdef __cplusplus
 }
 #endif

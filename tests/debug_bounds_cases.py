@@ -7,9 +7,9 @@ a bad block-table entry or bad packed offsets on purpose, at the error those
 inputs are defined to report -- and never at FA_ERR_OUT_OF_BOUNDS.  The bad
 inputs are ones the kernels already detect and skip without touching memory
 outside the buffers; the debug build confirms that they do.  The last cases
-stall the backward's, then the forward's, MMA warp through the debug build's
-injection hooks: the call must end with FA_ERR_TIMEOUT and the next one must
-match a clean run.
+stall the backward's and the forward's MMA warp and the decode split kernel's
+TMA warp through the debug build's injection hooks: the call must end with
+FA_ERR_TIMEOUT and the next one must match a clean run.
 Prints one line per case and exits non-zero on the first failure."""
 from __future__ import annotations
 
@@ -192,6 +192,28 @@ def forward_stall_cases(so):
                     sys.exit(1)
 
 
+def decode_stall_cases(so):
+    # the decode split kernel's TMA warp in CTA 0 (first sequence, first split)
+    # loads nothing: FA_ERR_TIMEOUT, every CTA ends, the next call is clean
+    for d in (64, 128):
+        for splits in (1, 4):
+            P = wl.paged_inputs(2, 16, 4, d, 1, 1, block_size=16, seed=80 + d, seq_lens=[900, 2500])
+            q, kc, vc, bt, sl = (t.to(DEV) for t in (P.q, P.k_cache, P.v_cache, P.block_table, P.seq_lens))
+            ref = [t.float() for t in fa.fa_paged_decode(q, kc, vc, bt, sl, num_splits=splits)]
+            check(f"decode d={d} splits={splits} before the stall")
+            if so.fa_debug_stall_decode(0, 20000) != fa.FA_OK:
+                print("FAIL the decode stall injection did not arm")
+                sys.exit(1)
+            fa.fa_paged_decode(q, kc, vc, bt, sl, num_splits=splits)
+            check(f"decode d={d} splits={splits} with its TMA warp stalled", expect=(fa.FA_ERR_TIMEOUT,))
+            got = [t.float() for t in fa.fa_paged_decode(q, kc, vc, bt, sl, num_splits=splits)]
+            check(f"decode d={d} splits={splits} after the stall")
+            for name, g, r in zip(("o", "lse"), got, ref):
+                if not torch.equal(g, r):
+                    print(f"FAIL decode d={d} splits={splits} {name} after the stall differs from the clean run")
+                    sys.exit(1)
+
+
 if __name__ == "__main__":
     so = fa.load()
     if so.fa_debug_build() != 1:
@@ -212,4 +234,5 @@ if __name__ == "__main__":
     decode_cases()
     stall_cases(so)
     forward_stall_cases(so)
+    decode_stall_cases(so)
     print("all cases in bounds")

@@ -46,7 +46,7 @@ def test_status_strings(so):
                        (4, "FA_ERR_TIMEOUT"), (5, "FA_ERR_BAD_BLOCK_TABLE"), (6, "FA_ERR_OUT_OF_BOUNDS")]:
         assert so.fa_status_string(code).decode() == name
     assert so.fa_status_string(99).decode() == "FA_ERR_UNKNOWN"
-    assert so.fa_version() == 108
+    assert so.fa_version() == 109
 
 
 def _fake(n=1):
@@ -219,6 +219,8 @@ def test_selftest_argument_validation(so):
     assert so.fa_debug_stall_forward(-1, 1000) == fl.FA_ERR_INVALID_ARG
     assert so.fa_debug_stall_forward(0, 0) == fl.FA_ERR_INVALID_ARG
     assert so.fa_debug_stall_forward(0, 1000) == fl.FA_ERR_UNSUPPORTED
+    assert so.fa_debug_stall_decode(-1, 1000) == fl.FA_ERR_INVALID_ARG
+    assert so.fa_debug_stall_decode(0, 1000) == fl.FA_ERR_UNSUPPORTED
 
 
 def test_binding_has_every_name_the_bench_and_smoke_use():
@@ -253,8 +255,9 @@ def test_debug_build_compiles_and_reports_itself():
     path = fab.build(debug=True)
     code = (f"import ctypes; so = ctypes.CDLL({path!r}); "
             "print(so.fa_debug_build(), so.fa_debug_stall_backward(0, 1000), so.fa_debug_stall_backward(-1, 1000), "
-            "so.fa_debug_stall_forward(0, 1000), so.fa_debug_stall_forward(0, 2000000))")
+            "so.fa_debug_stall_forward(0, 1000), so.fa_debug_stall_forward(0, 2000000), "
+            "so.fa_debug_stall_decode(0, 1000), so.fa_debug_stall_decode(0, 0))")
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=120)
     # debug build; the stall injections arm (host state only) and check their arguments
     ok, bad = str(fl.FA_OK), str(fl.FA_ERR_INVALID_ARG)
-    assert r.returncode == 0 and r.stdout.split() == ["1", ok, bad, ok, bad], r.stdout + r.stderr
+    assert r.returncode == 0 and r.stdout.split() == ["1", ok, bad, ok, bad, ok, bad], r.stdout + r.stderr

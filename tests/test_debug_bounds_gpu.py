@@ -5,9 +5,9 @@ stands in for a memory checker, which this pool does not offer.  The edge-case
 workloads (ragged and one-row problems, key padding, empty and one-token
 sequences, all block sizes, split counts, bad table entries and bad offsets
 that the kernels are defined to detect) run against it in a process of their
-own (tests/debug_bounds_cases.py), followed by the backward's and the
-forward's failure paths: the MMA warp is stalled by the debug build's
-injection hooks, the bounded waits give up, the call reports FA_ERR_TIMEOUT
+own (tests/debug_bounds_cases.py), followed by the backward's, the forward's
+and paged decode's failure paths: a warp the others wait on is stalled by
+the debug build's injection hooks, the bounded waits give up, the call reports FA_ERR_TIMEOUT
 without hanging, and the next call matches a clean run."""
 import os
 import subprocess
@@ -39,3 +39,4 @@ def test_debug_build_keeps_every_edge_case_in_bounds():
     assert "ok   bounds guard self-test: FA_ERR_OUT_OF_BOUNDS" in r.stdout
     assert "ok   packed d=128 backward with its MMA warp stalled: FA_ERR_TIMEOUT" in r.stdout
     assert "ok   packed d=128 forward with its MMA warp stalled: FA_ERR_TIMEOUT" in r.stdout
+    assert "ok   decode d=128 splits=4 with its TMA warp stalled: FA_ERR_TIMEOUT" in r.stdout
