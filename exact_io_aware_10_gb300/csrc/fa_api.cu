@@ -314,7 +314,8 @@ int fa_bwd_varlen(const void* Q, const void* K, const void* V, const void* O, co
   if (bad_scale(scale)) return FA_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
   if (num_seqs > 65535 || static_cast<long long>(num_seqs) * H > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
-  if ((static_cast<long long>(max_seqlen) + 127) / 128 * 4 > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  // (the work-item grid's x extent, key tiles x 8 heads, must fit an int)
+  if ((static_cast<long long>(max_seqlen) + 127) / 128 * 8 > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
   if (total == 0 || max_seqlen == 0) return FA_OK;
   if (!Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV || !cu_seqlens || !workspace)
     return FA_ERR_INVALID_ARG;

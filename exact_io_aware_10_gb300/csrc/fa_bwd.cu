@@ -13,8 +13,9 @@
 //                      kernel's work counter <- 0.
 //  2. bwd_main_kernel  one persistent CTA per SM; its work items are the
 //                      (128-key tile j, batch*head) pairs, taken in order from a
-//                      counter in the workspace: groups of four heads, within
-//                      a group the key tiles with most query tiles first, so
+//                      counter in the workspace: groups of heads (16, 8 or 4 by
+//                      the L2 budget), within a group the key tiles with most
+//                      query tiles first, so
 //                      the items in flight share a few heads' Q, dO and dQ
 //                      accumulator in L2.  K_j and V_j stay in shared
 //                      memory (d = 64, short items: two K, V buffers, so the
@@ -116,7 +117,17 @@ constexpr int kAltMaxTiles = 8;  // d = 64: items of at most this many query til
 // per-thread reductions, 1.4-2.3 % faster with the staged TMA reductions)
 template <int D>
 constexpr bool kQWatch = true;
-constexpr int kHeadGroup = 4;  // heads whose CTAs are interleaved in the grid
+// Heads whose work items are interleaved: the items in flight then share
+// those heads' Q, dO and fp32 dQ accumulator (N d 8 bytes a head) in L2.  The
+// largest of 16, 8 and 4 heads whose share stays within kL2HeadBudget; 8 for
+// the packed layout (measured best on the long ragged mix).
+constexpr double kL2HeadBudget = 256.0 * 1024 * 1024;
+inline int bwd_head_group(int N, int D, bool packed) {
+  if (packed) return 8;
+  for (int g = 16; g > 4; g /= 2)
+    if (static_cast<double>(g) * N * D * 8.0 <= kL2HeadBudget) return g;
+  return 4;
+}
 // register split of the main kernel: d = 64 gives the compute warps 104 (their
 // item and tile state spills at 96), d = 128 keeps 96 / 96 (the issuing thread
 // spills at 64)
@@ -144,7 +155,7 @@ struct BwdArgs {
   const int32_t* cu_seqlens;
   int total;
   // persistent main kernel: work-item counter (zeroed by the preprocess), the
-  // number of items and the x extent of the item grid (key tiles x kHeadGroup)
+  // number of items and the x extent of the item grid (key tiles x heads per group)
   unsigned* sched;
   int n_items, gx;
 #ifdef FA_DEBUG
@@ -314,11 +325,12 @@ template <bool kPacked>
 struct BwdItem {
   int bh, b, j, head, tok0, N, kv_len, i0, nt;
   __device__ __forceinline__ bool decode(const BwdArgs& a, int item) {
+    const int hg = a.gx / a.nq;  // heads per group
     const int x = item % a.gx, y = item / a.gx;
-    bh = y * kHeadGroup + x % kHeadGroup;
+    bh = y * hg + x % hg;
     if (bh >= a.BH) return false;
     b = bh / a.H;
-    j = x / kHeadGroup;
+    j = x / hg;
     head = bh % a.H;
     int n_rows = a.N;
     tok0 = 0;
@@ -1065,10 +1077,11 @@ fa_status bwd_launch_d(const void* Q, const void* K, const void* V, const void* 
   if (!(D == 128 ? encode_f32_tmap(&tdq, a.dQacc, 3, dims, qstrides, qbox)
                  : encode_f32_sw128_tmap(&tdq, a.dQacc, 3, dims, qstrides, qbox)))
     return FA_ERR_CUDA;
-  // work items: (key tile, batch*head) pairs, key tile * kHeadGroup + head in
-  // group fastest, then the group of heads
-  a.gx = nq * kHeadGroup;
-  a.n_items = a.gx * ceil_div(BH, kHeadGroup);
+  // work items: (key tile, batch*head) pairs, key tile * heads per group + head
+  // in group fastest, then the group of heads
+  const int hg = bwd_head_group(N, D, false);
+  a.gx = nq * hg;
+  a.n_items = a.gx * ceil_div(BH, hg);
   a.sched = bwd_sched_ptr(workspace, side, static_cast<size_t>(BH) * N * D);
   // dK, dV as TMA store targets: 64-column boxes of a key tile's rows (d = 64:
   // 64-row halves)
@@ -1141,10 +1154,11 @@ fa_status bwd_varlen_launch_d(const void* Q, const void* K, const void* V, const
   if (!(D == 128 ? encode_f32_tmap(&tdq, a.dQacc, 3, dims, qstrides, qbox)
                  : encode_f32_sw128_tmap(&tdq, a.dQacc, 3, dims, qstrides, qbox)))
     return FA_ERR_CUDA;
-  // work items: (key tile, batch*head) pairs, key tile * kHeadGroup + head in
-  // group fastest, then the group of heads
-  a.gx = nq * kHeadGroup;
-  a.n_items = a.gx * ceil_div(BH, kHeadGroup);
+  // work items: (key tile, batch*head) pairs, key tile * heads per group + head
+  // in group fastest, then the group of heads
+  const int hg = bwd_head_group(max_seqlen, D, true);
+  a.gx = nq * hg;
+  a.n_items = a.gx * ceil_div(BH, hg);
   a.sched = bwd_sched_ptr(workspace, side, static_cast<size_t>(total) * H * D);
   // (the packed kernel stores dK, dV row by row; these maps are not used)
   if (!encode_bf16_tmap(&tdk, dK, 3, dims, strides, box) || !encode_bf16_tmap(&tdv, dV, 3, dims, strides, box))
