@@ -119,9 +119,11 @@ template <int D>
 constexpr bool kQWatch = true;
 // Heads whose work items are interleaved: the items in flight then share
 // those heads' Q, dO and fp32 dQ accumulator (N d 8 bytes a head) in L2.  The
-// largest of 16, 8 and 4 heads whose share stays within kL2HeadBudget; 8 for
-// the packed layout (measured best on the long ragged mix).
-constexpr double kL2HeadBudget = 256.0 * 1024 * 1024;
+// largest of 16, 8 and 4 heads whose share fits kL2HeadBudget, well inside the
+// 129 MB L2 (a share the size of L2 already doubles the main kernel's DRAM
+// traffic through dQ reductions that miss it); 8 for the packed layout
+// (measured best on the long ragged mix).
+constexpr double kL2HeadBudget = 96.0 * 1024 * 1024;
 inline int bwd_head_group(int N, int D, bool packed) {
   if (packed) return 8;
   for (int g = 16; g > 4; g /= 2)
