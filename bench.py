@@ -93,9 +93,9 @@ TRAFFIC_RECORD = {
             "bytes": {"N16384": 294786304 + 47980032, "N65536": 1169585920 + 249820672}},
     "bwd": {"kernel": "bwd_pre_kernel<128> + bwd_main_kernel<128> + bwd_dq_kernel",
             "source": "exact_io_aware_10_gb300/csrc/fa_bwd.cu",
-            "sha256": "366380d02d4dc25aec8ccebffa6e9d714e73c8520d45abebb9c0198db3f574be",
-            "bytes": {"N16384_main": 408584448 + 221137664, "N16384_pre": 135282688 + 87886592,
-                      "N16384_dq": 134228736 + 35183104}},
+            "sha256": "b80c3f350e35ffe702e01ce477881e52f37febbf87a07351068eeb8b05309b10",
+            "bytes": {"N16384_main": 407478016 + 222058752, "N16384_pre": 135283968 + 87193600,
+                      "N16384_dq": 134224384 + 35507712}},
     "decode": {"kernel": "decode_split_kernel<128> + decode_combine_kernel<128>",
                "source": "exact_io_aware_10_gb300/csrc/fa_decode.cu",
                "sha256": "96643620437889a50b50449cfba8585c7840c835eb6f35ec53c73832317d557e",

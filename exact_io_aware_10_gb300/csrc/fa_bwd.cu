@@ -590,18 +590,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             asm volatile("add.u64 %0, %1, %2;" : "=l"(r) : "l"(d0), "l"(static_cast<uint64_t>(kvo)));
             return r;
           };
-#define kK at_kv(kK0)
-#define kV at_kv(kV0)
-#define mK at_kv(mK0)
           // prologue: S_0 and dP_0; dP_0 overwrites the previous item's last dQ
           if (!(ok = mbar_wait(bar(BAR_Q_FULL + (gs & 1)), (gs >> 1) & 1, wc))) break;
           tc_fence_after();
-          mma_kmajor_d(C::kColS, kK, kq(gs));
+          mma_kmajor_d(C::kColS, at_kv(kK0), kq(gs));
           mma_commit(bar(BAR_S));
           if (!(ok = mbar_wait(bar(BAR_DO_FULL), gs & 1, wc))) break;
           if (gs > 0 && !(ok = mbar_wait(bar(BAR_DQ_READ), (gs - 1) & 1, wc))) break;
           tc_fence_after();
-          mma_kmajor_d(C::kColDP, kV, kO);
+          mma_kmajor_d(C::kColDP, at_kv(kV0), kO);
           mma_commit(bar(BAR_DP));
           for (int it = 0; ok && it < nt; ++it) {
             const int g = gs + it;
@@ -625,7 +622,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               constexpr uint32_t idQT = idesc_bf16_f32(128, 128, true, true);  // A = K^T, B = dS^T
 #pragma unroll
               for (int k2 = 0; k2 < kTile / 16; ++k2)
-                mma_ss(tmem + C::kColDQ, sdesc_advance(mK, k2 * 2048), sdesc_advance(mP, k2 * 2048), idQT,
+                mma_ss(tmem + C::kColDQ, sdesc_advance(at_kv(mK0), k2 * 2048), sdesc_advance(mP, k2 * 2048), idQT,
                        k2 > 0 ? 1u : 0u);
               mma_commit(bar(BAR_DQ_FULL));
 #pragma unroll
@@ -638,7 +635,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               constexpr uint32_t idNN = idesc_bf16_f32(128, D, true, true);  // A = dS, B = K
 #pragma unroll
               for (int k2 = 0; k2 < kTile / 16; ++k2)
-                mma_ss(tmem + C::kColDQ, sdesc_advance(mP, k2 * 2048), sdesc_advance(mK, k2 * 2048), idNN,
+                mma_ss(tmem + C::kColDQ, sdesc_advance(mP, k2 * 2048), sdesc_advance(at_kv(mK0), k2 * 2048), idNN,
                        k2 > 0 ? 1u : 0u);
               mma_commit(bar(BAR_DQ_FULL));
 #pragma unroll
@@ -654,21 +651,18 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (!kQWatch<D> && !(ok = mbar_wait(bar(BAR_Q_FULL + ((g + 1) & 1)), ((g + 1) >> 1) & 1, wc)))
                 break;
               if (!kQWatch<D>) tc_fence_after();
-              mma_kmajor_d(C::kColS, kK, kq(g + 1));
+              mma_kmajor_d(C::kColS, at_kv(kK0), kq(g + 1));
               mma_commit(bar(BAR_S));
               if (!(ok = mbar_wait(bar(BAR_DO_FULL), (g + 1) & 1, wc))) break;
               if (!(ok = mbar_wait(bar(BAR_DQ_READ), g & 1, wc))) break;
               tc_fence_after();
-              mma_kmajor_d(C::kColDP, kV, kO);
+              mma_kmajor_d(C::kColDP, at_kv(kV0), kO);
               mma_commit(bar(BAR_DP));
             }
           }
           if (!ok) break;
           mma_commit(bar(BAR_FINAL));
           mma_commit(kv_empty(ks));
-#undef kK
-#undef kV
-#undef mK
           gs += nt;
           kf += 1;
         }
