@@ -778,14 +778,16 @@ fa_status fwd_varlen_launch_d(const void* Q, const void* K, const void* V, void*
   a.causal = causal ? 1 : 0;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.status = status;
-  a.head_group = H;
+  // a sequence's heads run side by side, grouped like the dense layout's by
+  // the K/V of the longest sequence (which bounds every sequence's)
+  a.head_group = dense_head_group(num_seqs, H, max_seqlen, D);
 #ifdef FA_DEBUG
   a.dbg_nb = num_seqs;
   a.dbg_o_rows = a.dbg_lse_len = static_cast<long long>(total) * H;
   a.dbg_mask_bytes = 0;
   take_forward_stall(a);
 #endif
-  dim3 grid(H, ceil_div(max_seqlen, 2 * kRows), num_seqs);
+  dim3 grid(a.head_group, ceil_div(max_seqlen, 2 * kRows), num_seqs * ceil_div(H, a.head_group));
   fwd_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, a);
   return launch_status();
 }
