@@ -89,8 +89,8 @@ NOMINAL = {"bf16_tflops": 2250.0, "bf16_tflops_nvl72": 2500.0, "hbm_gbs": 8000.0
 # they were taken on: a figure turns null once its source changes.
 TRAFFIC_RECORD = {
     "fwd": {"kernel": "fwd_kernel<128>", "source": "exact_io_aware_10_gb300/csrc/fa_fwd.cu",
-            "sha256": "26630fc7dc7b0f6442529e1db8b7efb0e9a6d59cb55ab7bcf80077e599bed526",
-            "bytes": {"N16384": 294786304 + 47980032, "N65536": 1169585920 + 249820672}},
+            "sha256": "3630e69b48727d7ff1bb1c895d15cacd699d08e2946a893bf3bd288a84579226",
+            "bytes": {"N16384": 290745600 + 47855104, "N65536": 1167099136 + 250001664}},
     "bwd": {"kernel": "bwd_pre_kernel<128> + bwd_main_kernel<128> + bwd_dq_kernel",
             "source": "exact_io_aware_10_gb300/csrc/fa_bwd.cu",
             "sha256": "b80c3f350e35ffe702e01ce477881e52f37febbf87a07351068eeb8b05309b10",
